@@ -1,0 +1,446 @@
+/*
+ * CPU oracle for sparse-attention token selection over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE. This file is the plain, slow reference definition that the
+ * CUDA path is checked against. Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark load it; the library never does. It shares no
+ * code, header or constant with the CUDA sources.
+ *
+ * What it computes, step by step, for every query row r of request i
+ * (rows [qsl[i], qsl[i+1]); rows past qsl[num_reqs] are padding):
+ *
+ *   1. ctx = positions[r] + 1. ("Row context == position + 1", vLLM page
+ *      flashinfer_mla_sparse_sm90, _kv_lens_host.)
+ *   2. ctx <= index_topk: the row selects every token 0 .. ctx-1 (same docstring:
+ *      "contexts up to index_topk select everything").
+ *   3. otherwise P = ctx / kpool complete pools are visible. Pool j lives in the
+ *      request's logical key page j / 64 at row j % 64 (ReVolta PR #59, "Change":
+ *      64-key tiles through a page table). Its score is
+ *          s_j = sum_{h<4} sum_{d<128} q[r,h,d] * k[j,d]
+ *      accumulated sequentially in fp32 (the fp16 x fp16 product is exact in
+ *      fp32). A pool whose key page is out of range scores -inf.
+ *   4. K = index_topk / kpool pools are kept: the K best under the total order
+ *      (score descending, pool index ascending). A full sort by that order is used
+ *      on purpose: it is a different algorithm from the GPU's radix select.
+ *   5. Expansion: each kept pool p gives tokens p*kpool .. p*kpool+kpool-1, and the
+ *      trailing incomplete pool's tokens P*kpool .. ctx-1 are always added
+ *      (_kv_lens_host: "the top index_topk pool-expanded tokens plus the trailing
+ *      incomplete pool"). Tokens are listed in ascending order and the row is
+ *      padded with -1 to the output width.
+ *   6. Remap (sparse_utils, triton_convert_req_index_to_global_index):
+ *          slot = block_table[i, t / block_size] * block_stride_rows + t % block_size
+ *      and -1 when t == -1 or the block is out of bounds: the logical block is past
+ *      max_blocks_per_req, or the physical id is outside [0, num_kv_blocks).
+ *   7. valid count = number of entries that are not -1 ("the count of valid
+ *      (non -1) indices per row").
+ *
+ * Readings where the pages are silent: the score has no weights, ReLU or scale;
+ * only complete pools are scored; ties go to the lower pool index; -0.0 equals
+ * +0.0; NaN (outside the input contract) ranks below -inf.
+ *
+ * Parity pins: see tests/test_oracle_pins.py. Nothing here is unpinned.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_ST_KEYPAGE_OOB 1
+#define ORC_ST_CTX_OVER_BOUND 2
+#define ORC_ST_BAD_QSL 8
+
+/* IEEE 754 binary16 -> float, from the format's definition (1 sign bit, 5 exponent
+ * bits with bias 15, 10 fraction bits). Every binary16 value is exact in float. */
+float orc_half_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);                 /* subnormal: frac * 2^-24 */
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);  /* (1 + frac/1024) * 2^(expo-15) */
+    return (float)(sign ? -v : v);
+}
+
+void orc_half_to_float_array(const uint16_t *h, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_half_to_float(h[i]);
+}
+
+/* Score of one pool against one query row: sum over heads, then over dimensions,
+ * in fp32, in that order. Also returns sum |q*k| in fp64, the scale of the score's
+ * rounding error. */
+float orc_pool_score(const uint16_t *q_row, const uint16_t *key, int heads, int dim,
+                     double *abs_terms)
+{
+    float s = 0.0f;
+    double a = 0.0;
+    for (int h = 0; h < heads; ++h) {
+        for (int d = 0; d < dim; ++d) {
+            float qv = orc_half_to_float(q_row[h * dim + d]);
+            float kv = orc_half_to_float(key[d]);
+            float prod = qv * kv;
+            s = s + prod;
+            a += fabs((double)qv * (double)kv);
+        }
+    }
+    s = s + 0.0f; /* -0.0 -> +0.0 */
+    if (abs_terms)
+        *abs_terms = a;
+    return s;
+}
+
+typedef struct {
+    float s;
+    int32_t j;
+} orc_pool;
+
+/* Total order used for selection: higher score first, lower index first on ties;
+ * NaN after everything (it is outside the input contract). */
+static int orc_better(const orc_pool *a, const orc_pool *b)
+{
+    int an = isnan(a->s), bn = isnan(b->s);
+    if (an != bn)
+        return bn;             /* the non-NaN one is better */
+    if (!an && a->s != b->s)
+        return a->s > b->s;
+    return a->j < b->j;
+}
+
+static int orc_cmp_pool(const void *pa, const void *pb)
+{
+    const orc_pool *a = (const orc_pool *)pa, *b = (const orc_pool *)pb;
+    if (a->j == b->j)
+        return 0;
+    return orc_better(a, b) ? -1 : 1;
+}
+
+static int orc_cmp_int(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+/* The K best pools of scores[0..P) under the order above, returned in ascending
+ * pool index. Returns the number written (min(K, P)). */
+int orc_topk_pools(const float *scores, int32_t P, int32_t K, int32_t *out)
+{
+    if (P <= 0 || K <= 0)
+        return 0;
+    orc_pool *v = (orc_pool *)malloc(sizeof(orc_pool) * (size_t)P);
+    if (!v)
+        return -1;
+    for (int32_t j = 0; j < P; ++j) {
+        v[j].s = scores[j];
+        v[j].j = j;
+    }
+    qsort(v, (size_t)P, sizeof(orc_pool), orc_cmp_pool);
+    int32_t n = K < P ? K : P;
+    for (int32_t i = 0; i < n; ++i)
+        out[i] = v[i].j;
+    free(v);
+    qsort(out, (size_t)n, sizeof(int32_t), orc_cmp_int);
+    return n;
+}
+
+/* Expansion of a row's kept pools (ascending) into tokens, plus the trailing
+ * incomplete pool; -1 padding to width W. Returns the number of tokens, or -1 if
+ * they do not fit in W. */
+int orc_expand(int64_t ctx, int32_t topk, int32_t kpool, const int32_t *pools,
+               int32_t npools, int32_t W, int32_t *tokens)
+{
+    int32_t n = 0;
+    if (ctx > 0 && ctx <= topk) {
+        if (ctx > W)
+            return -1;
+        for (int64_t t = 0; t < ctx; ++t)
+            tokens[n++] = (int32_t)t;
+    } else if (ctx > topk) {
+        int64_t P = ctx / kpool;
+        for (int32_t i = 0; i < npools; ++i)
+            for (int32_t t = 0; t < kpool; ++t) {
+                if (n >= W)
+                    return -1;
+                tokens[n++] = (int32_t)((int64_t)pools[i] * kpool + t);
+            }
+        for (int64_t t = P * kpool; t < ctx; ++t) {
+            if (n >= W)
+                return -1;
+            tokens[n++] = (int32_t)t;
+        }
+    }
+    for (int32_t c = n; c < W; ++c)
+        tokens[c] = -1;
+    return n;
+}
+
+/* One token index through one request's block-table row. */
+int64_t orc_remap_token(int32_t t, const int32_t *bt_row, int32_t max_blocks,
+                        int32_t num_kv_blocks, int32_t block_size, int64_t block_stride_rows)
+{
+    if (t < 0)
+        return -1;
+    int32_t b = t / block_size;
+    if (b >= max_blocks)
+        return -1;
+    int32_t ph = bt_row[b];
+    if (ph < 0 || ph >= num_kv_blocks)
+        return -1;
+    return (int64_t)ph * block_stride_rows + (t % block_size);
+}
+
+/* Remap of whole rows: token_idx [rows, width] -> slots [rows, width], counts [rows].
+ * req_id[r] outside [0, num_reqs) gives an all -1 row. */
+void orc_remap_rows(const int32_t *req_id, int32_t num_reqs, const int32_t *block_table,
+                    int64_t bt_ld, int32_t max_blocks, int32_t num_kv_blocks,
+                    const int32_t *token_idx, int32_t rows, int32_t width,
+                    int32_t block_size, int64_t block_stride_rows, int64_t *slots,
+                    int32_t *counts)
+{
+    for (int32_t r = 0; r < rows; ++r) {
+        int32_t req = req_id[r];
+        int32_t cnt = 0;
+        for (int32_t c = 0; c < width; ++c) {
+            int64_t s = -1;
+            if (req >= 0 && req < num_reqs)
+                s = orc_remap_token(token_idx[(int64_t)r * width + c],
+                                    block_table + (int64_t)req * bt_ld, max_blocks,
+                                    num_kv_blocks, block_size, block_stride_rows);
+            slots[(int64_t)r * width + c] = s;
+            cnt += (s != -1);
+        }
+        if (counts)
+            counts[r] = cnt;
+    }
+}
+
+typedef struct {
+    int32_t num_reqs, num_rows;
+    const int32_t *qsl, *positions;
+    const uint16_t *q;            /* [num_rows, heads, dim] fp16 bits */
+    int64_t q_row_stride;         /* elements */
+    const uint16_t *key_cache;    /* fp16 bits */
+    int64_t key_page_stride;      /* elements */
+    int32_t num_key_pages;
+    const int32_t *key_page_table;
+    int64_t kpt_ld;
+    int32_t max_key_pages_per_req;
+    const int32_t *block_table;
+    int64_t bt_ld;
+    int32_t max_blocks_per_req, num_kv_blocks, block_size;
+    int64_t block_stride_rows;
+    int32_t heads, dim, key_page_size, index_topk, kpool, out_width;
+    int64_t max_context;
+} orc_problem;
+
+typedef struct {
+    const orc_problem *p;
+    const int32_t *rows;          /* rows to compute (indices into the batch) */
+    int32_t nrows;
+    int32_t tid, nthreads;
+    int64_t *slots;               /* [nrows, out_width] */
+    int32_t *counts;              /* [nrows] */
+    int32_t *token_idx;           /* [nrows, out_width] or NULL */
+    float *scores;                /* [nrows, scores_ld] or NULL */
+    double *abs_terms;            /* [nrows, scores_ld] or NULL */
+    int64_t scores_ld;
+    int32_t status;
+    int32_t error;
+} orc_job;
+
+static int orc_qsl_ok(const orc_problem *p)
+{
+    if (p->qsl[0] < 0 || p->qsl[p->num_reqs] > p->num_rows)
+        return 0;
+    for (int32_t i = 0; i < p->num_reqs; ++i)
+        if (p->qsl[i] > p->qsl[i + 1])
+            return 0;
+    return 1;
+}
+
+static int32_t orc_request_of(const orc_problem *p, int32_t r)
+{
+    for (int32_t i = 0; i < p->num_reqs; ++i)
+        if (p->qsl[i] <= r && r < p->qsl[i + 1])
+            return i;
+    return -1;
+}
+
+static void orc_one_row(orc_job *jb, int32_t k)
+{
+    const orc_problem *p = jb->p;
+    const int32_t W = p->out_width;
+    int32_t r = jb->rows[k];
+    int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)W);
+    int64_t *slot = jb->slots + (int64_t)k * W;
+    for (int32_t c = 0; c < W; ++c)
+        tok[c] = -1;
+
+    int32_t req = orc_qsl_ok(p) ? orc_request_of(p, r) : -1;
+    if (!orc_qsl_ok(p))
+        jb->status |= ORC_ST_BAD_QSL;
+    int64_t ctx = (int64_t)p->positions[r] + 1;
+    if (req >= 0 && ctx > p->max_context) {
+        jb->status |= ORC_ST_CTX_OVER_BOUND;
+        req = -1;
+    }
+    if (req >= 0 && ctx > p->index_topk) {
+        int32_t P = (int32_t)(ctx / p->kpool);
+        int32_t K = p->index_topk / p->kpool;
+        float *s = (float *)malloc(sizeof(float) * (size_t)P);
+        const uint16_t *qr = p->q + (int64_t)r * p->q_row_stride;
+        for (int32_t j = 0; j < P; ++j) {
+            int32_t lp = j / p->key_page_size;
+            int32_t pg = lp < p->max_key_pages_per_req
+                             ? p->key_page_table[(int64_t)req * p->kpt_ld + lp] : -1;
+            double a = 0.0;
+            if (pg < 0 || pg >= p->num_key_pages) {
+                s[j] = -INFINITY;
+                jb->status |= ORC_ST_KEYPAGE_OOB;
+            } else {
+                const uint16_t *key = p->key_cache + (int64_t)pg * p->key_page_stride +
+                                      (int64_t)(j % p->key_page_size) * p->dim;
+                s[j] = orc_pool_score(qr, key, p->heads, p->dim, &a);
+            }
+            if (jb->scores && j < jb->scores_ld)
+                jb->scores[(int64_t)k * jb->scores_ld + j] = s[j];
+            if (jb->abs_terms && j < jb->scores_ld)
+                jb->abs_terms[(int64_t)k * jb->scores_ld + j] = a;
+        }
+        int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+        int32_t n = orc_topk_pools(s, P, K, sel);
+        if (orc_expand(ctx, p->index_topk, p->kpool, sel, n, W, tok) < 0)
+            jb->error = 1;
+        free(sel);
+        free(s);
+    } else if (req >= 0) {
+        if (orc_expand(ctx, p->index_topk, p->kpool, NULL, 0, W, tok) < 0)
+            jb->error = 1;
+    }
+    int32_t cnt = 0;
+    for (int32_t c = 0; c < W; ++c) {
+        int64_t sl = -1;
+        if (req >= 0)
+            sl = orc_remap_token(tok[c], p->block_table + (int64_t)req * p->bt_ld,
+                                 p->max_blocks_per_req, p->num_kv_blocks, p->block_size,
+                                 p->block_stride_rows);
+        slot[c] = sl;
+        cnt += (sl != -1);
+    }
+    jb->counts[k] = cnt;
+    if (jb->token_idx)
+        memcpy(jb->token_idx + (int64_t)k * W, tok, sizeof(int32_t) * (size_t)W);
+    free(tok);
+}
+
+static void *orc_worker(void *arg)
+{
+    orc_job *jb = (orc_job *)arg;
+    for (int32_t k = jb->tid; k < jb->nrows; k += jb->nthreads)
+        orc_one_row(jb, k);
+    return NULL;
+}
+
+/* The whole selection for the listed rows, on nthreads POSIX threads (rows are
+ * independent). Returns the OR of the status bits, or -1 on an internal error
+ * (output width too small). */
+int32_t orc_select(const orc_problem *p, const int32_t *rows, int32_t nrows,
+                   int32_t nthreads, int64_t *slots, int32_t *counts, int32_t *token_idx,
+                   float *scores, double *abs_terms, int64_t scores_ld)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    orc_job jobs[256];
+    pthread_t th[256];
+    for (int32_t t = 0; t < nthreads; ++t) {
+        jobs[t] = (orc_job){p, rows, nrows, t, nthreads, slots, counts, token_idx,
+                            scores, abs_terms, scores_ld, 0, 0};
+    }
+    for (int32_t t = 1; t < nthreads; ++t)
+        pthread_create(&th[t], NULL, orc_worker, &jobs[t]);
+    orc_worker(&jobs[0]);
+    for (int32_t t = 1; t < nthreads; ++t)
+        pthread_join(th[t], NULL);
+    int32_t st = 0;
+    for (int32_t t = 0; t < nthreads; ++t) {
+        if (jobs[t].error)
+            return -1;
+        st |= jobs[t].status;
+    }
+    return st;
+}
+
+/* The scoring step alone (step 3) for the listed rows, over the row's complete pools:
+ * scores[k, j] for j < ctx / kpool, -inf on out-of-range key pages; entries at
+ * higher j are left untouched. Rows whose request cannot be found are skipped. */
+int32_t orc_score_rows(const orc_problem *p, const int32_t *rows, int32_t nrows,
+                       float *scores, double *abs_terms, int64_t scores_ld)
+{
+    int32_t st = 0;
+    for (int32_t k = 0; k < nrows; ++k) {
+        int32_t r = rows[k];
+        int32_t req = orc_request_of(p, r);
+        if (req < 0)
+            continue;
+        int64_t ctx = (int64_t)p->positions[r] + 1;
+        int64_t P = ctx > 0 ? ctx / p->kpool : 0;
+        if (P > scores_ld)
+            P = scores_ld;
+        const uint16_t *qr = p->q + (int64_t)r * p->q_row_stride;
+        for (int64_t j = 0; j < P; ++j) {
+            int32_t lp = (int32_t)(j / p->key_page_size);
+            int32_t pg = lp < p->max_key_pages_per_req
+                             ? p->key_page_table[(int64_t)req * p->kpt_ld + lp] : -1;
+            double a = 0.0;
+            float s;
+            if (pg < 0 || pg >= p->num_key_pages) {
+                s = -INFINITY;
+                st |= ORC_ST_KEYPAGE_OOB;
+            } else {
+                const uint16_t *key = p->key_cache + (int64_t)pg * p->key_page_stride +
+                                      (j % p->key_page_size) * p->dim;
+                s = orc_pool_score(qr, key, p->heads, p->dim, &a);
+            }
+            scores[(int64_t)k * scores_ld + j] = s;
+            if (abs_terms)
+                abs_terms[(int64_t)k * scores_ld + j] = a;
+        }
+    }
+    return st;
+}
+
+/* Top-k + expansion alone (steps 2, 4, 5) on given score rows: row k has context
+ * ctx[k] and scores[k, 0 .. ctx/kpool). token_idx [nrows, W]; counts = tokens. */
+int32_t orc_topk_expand_rows(const float *scores, int64_t scores_ld, const int64_t *ctx,
+                             int32_t nrows, int32_t topk, int32_t kpool, int32_t W,
+                             int32_t *token_idx, int32_t *counts)
+{
+    int32_t K = topk / kpool;
+    int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
+    for (int32_t k = 0; k < nrows; ++k) {
+        int32_t *tok = token_idx + (int64_t)k * W;
+        int32_t n;
+        if (ctx[k] > topk) {
+            int64_t P = ctx[k] / kpool;
+            int32_t ns = orc_topk_pools(scores + (int64_t)k * scores_ld, (int32_t)P, K, sel);
+            n = orc_expand(ctx[k], topk, kpool, sel, ns, W, tok);
+        } else {
+            n = orc_expand(ctx[k], topk, kpool, NULL, 0, W, tok);
+        }
+        if (n < 0) {
+            free(sel);
+            return -1;
+        }
+        counts[k] = n;
+    }
+    free(sel);
+    return 0;
+}

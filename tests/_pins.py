@@ -1,0 +1,254 @@
+"""Pins for the CPU oracle: checks against facts the pages and the mathematics fix.
+
+Each function takes the oracle module (or a stand-in loaded from a mutated build)
+and raises AssertionError when the oracle disagrees with an independent fact:
+an exact integer computation, an IEEE decoding done by numpy, a library sort, a
+closed form from the pages, or an invariant of the remap.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+import workloads
+
+
+def pin_half_decode(orc):
+    """fp16 decoding of all 65,536 bit patterns equals numpy's binary16 conversion."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = orc.half_to_float(bits)
+    ref = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def pin_score_integer_exact(orc, seed=7, n=64):
+    """Integer-valued q, k: the fp32 score equals the exact int64 dot product
+    sum_h sum_d q[h,d] k[d] (|score| <= 4*128*9 < 2^24, so fp32 is exact)."""
+    rng = np.random.default_rng(seed)
+    for i in range(n):
+        qi = rng.integers(-3, 4, size=(4, 128))
+        ki = rng.integers(-3, 4, size=128)
+        if i == 0:   # extreme: every term +9
+            qi = np.full((4, 128), 3)
+            ki = np.full(128, 3)
+        if i == 1:   # head-dependent signs: a dropped or repeated head shows
+            qi = np.stack([np.full(128, 3), np.full(128, -1), np.full(128, 2), np.full(128, 1)])
+            ki = rng.integers(1, 4, size=128)
+        exact = int((qi.astype(np.int64) * ki.astype(np.int64)[None, :]).sum())
+        s, a = orc.pool_score(qi.astype(np.float16), ki.astype(np.float16))
+        assert s == float(exact), (i, s, exact)
+        assert a == float(np.abs(qi * ki[None, :]).sum())
+
+
+def pin_score_normal_bound(orc, seed=11, n=32):
+    """Normal values: |s32 - exact| <= (n-1) u sum|terms| (sequential fp32 bound,
+    u = 2^-24, n = 512 terms), well inside the 1e-4 sum|terms| tolerance; and the
+    reported sum |q*k| equals the fp64 value."""
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        q = (rng.standard_normal((4, 128)) / np.sqrt(128)).astype(np.float16)
+        k = (rng.standard_normal(128) / np.sqrt(128)).astype(np.float16)
+        terms = q.astype(np.float64) * k.astype(np.float64)[None, :]
+        exact = terms.sum()
+        absum = np.abs(terms).sum()
+        s, a = orc.pool_score(q, k)
+        assert abs(s - exact) <= 511 * 2.0 ** -24 * absum + 1e-30
+        assert abs(a - absum) <= 1e-12 * absum
+
+
+def _check_topk_characterisation(scores, K, got):
+    P = scores.size
+    got = np.asarray(got)
+    assert got.size == min(K, P)
+    assert np.all(np.diff(got) > 0), "ascending, distinct"
+    assert got.size == 0 or (got[0] >= 0 and got[-1] < P)
+    chosen = np.zeros(P, dtype=bool)
+    chosen[got] = True
+    s_in = scores[chosen]
+    i_in = np.nonzero(chosen)[0]
+    s_out = scores[~chosen]
+    i_out = np.nonzero(~chosen)[0]
+    if s_in.size and s_out.size:
+        # every kept pool beats every dropped one: higher score, or equal and lower index
+        better = (s_in[:, None] > s_out[None, :]) | (
+            (s_in[:, None] == s_out[None, :]) & (i_in[:, None] < i_out[None, :]))
+        assert better.all()
+
+
+def pin_topk_bruteforce(orc, seed=3, trials=300):
+    """Tiny inputs: the kept set beats every dropped pool under (score desc, index asc)."""
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        P = int(rng.integers(1, 48))
+        K = int(rng.integers(1, P + 1))
+        mode = t % 4
+        if mode == 0:
+            s = rng.standard_normal(P).astype(np.float32)
+        elif mode == 1:
+            s = rng.integers(-2, 3, size=P).astype(np.float32)      # many exact ties
+        elif mode == 2:
+            s = rng.standard_normal(P).astype(np.float32)
+            s[rng.random(P) < 0.3] = -np.inf
+        else:
+            s = np.where(rng.random(P) < 0.5, 0.0, -0.0).astype(np.float32)
+        _check_topk_characterisation(s, K, orc.topk_pools(s, K))
+
+
+def pin_topk_all_zero(orc):
+    """All scores zero (with -0.0 mixed in): the K lowest pool indices win."""
+    s = np.zeros(1000, dtype=np.float32)
+    s[::3] = -0.0
+    assert np.array_equal(orc.topk_pools(s, 64), np.arange(64, dtype=np.int32))
+
+
+def pin_topk_stable_argsort(orc, seed=5):
+    """A plain top-k equals numpy's stable argsort of -score (ties: lower index first)."""
+    rng = np.random.default_rng(seed)
+    for ties in ("none", "coarse", "inf"):
+        s = workloads.random_scores(1, 4099, seed=seed, ties=ties)[0]
+        for K in (1, 7, 512, 4099):
+            ref = np.sort(np.argsort(-s, kind="stable")[:K])
+            assert np.array_equal(orc.topk_pools(s, K), ref), (ties, K)
+
+
+def pin_expand_closed_form(orc, seed=9):
+    """Expansion: valid count == ctx if ctx <= topk else topk + ctx % kpool (the
+    closed form of _kv_lens_host), strictly increasing tokens below ctx, kpool
+    consecutive tokens per kept pool, the trailing tokens present, identity below topk."""
+    rng = np.random.default_rng(seed)
+    for topk, kpool in ((256, 4), (2048, 4), (60, 3), (16, 1), (64, 8)):
+        W = topk + kpool
+        K = topk // kpool
+        for ctx in list(range(1, topk + 2 * kpool + 2)) + list(rng.integers(topk, 50 * topk, 40)):
+            ctx = int(ctx)
+            P = ctx // kpool
+            pools = np.sort(rng.choice(P, size=min(K, P), replace=False)).astype(np.int32) \
+                if ctx > topk else np.zeros(0, np.int32)
+            tok, n = orc.expand(ctx, topk, kpool, pools, W)
+            want = ctx if ctx <= topk else topk + ctx % kpool
+            assert n == want, (topk, kpool, ctx, n, want)
+            v = tok[:n]
+            assert np.all(tok[n:] == -1)
+            assert np.all(np.diff(v) > 0) and (n == 0 or (v[0] >= 0 and v[-1] < ctx))
+            if ctx <= topk:
+                assert np.array_equal(v, np.arange(ctx))
+            else:
+                body = v[:K * kpool].reshape(K, kpool)
+                assert np.array_equal(body[:, 0] // kpool, pools)
+                assert np.array_equal(body - body[:, :1], np.tile(np.arange(kpool), (K, 1)))
+                assert np.array_equal(v[K * kpool:], np.arange(P * kpool, ctx))
+
+
+def pin_remap_identity(orc):
+    """Identity block table with stride == block size: slot == token; -1 stays -1."""
+    bs = 64
+    bt = np.arange(100, dtype=np.int32)
+    for t in list(range(-1, 300)) + [100 * bs - 1]:
+        s = orc.remap_token(t, bt, 100, 100, bs, bs)
+        assert s == (t if t >= 0 else -1)
+    assert orc.remap_token(100 * bs, bt, 100, 100, bs, bs) == -1   # block 100 out of bounds
+
+
+def pin_remap_inverse(orc, seed=13):
+    """Shuffled table and a row stride above the block size (other layers' pages in
+    between): the slot decodes back to its token through the inverse permutation,
+    and never lands in the rows between blocks."""
+    rng = np.random.default_rng(seed)
+    bs, stride, nb = 64, 192, 500
+    perm = rng.permutation(nb).astype(np.int32)
+    inv = np.argsort(perm)
+    toks = rng.integers(0, nb * bs, size=2000).astype(np.int32)
+    toks[::17] = -1
+    req = np.zeros(toks.size, dtype=np.int32)
+    slots, counts = orc.remap_rows(req, 1, perm[None, :], nb, nb, toks[:, None], bs, stride)
+    slots = slots[:, 0]
+    assert np.array_equal(slots == -1, toks == -1)
+    ok = toks != -1
+    assert np.all(slots[ok] % stride < bs)
+    assert np.array_equal(inv[slots[ok] // stride] * bs + slots[ok] % stride, toks[ok])
+    assert np.array_equal(counts, (toks != -1).astype(np.int32))
+
+
+def pin_remap_guards(orc):
+    """-1 for t == -1, a logical block past max_blocks, and a physical id outside
+    [0, num_kv_blocks); in range, the formula block*stride + offset."""
+    bt = np.array([5, -2, 7, 9, 3], dtype=np.int32)
+    nkv = 8
+    assert orc.remap_token(-1, bt, 5, nkv, 4, 4) == -1
+    assert orc.remap_token(0, bt, 5, nkv, 4, 4) == 5 * 4 + 0
+    assert orc.remap_token(3, bt, 5, nkv, 4, 10) == 5 * 10 + 3
+    assert orc.remap_token(4, bt, 5, nkv, 4, 4) == -1      # physical -2
+    assert orc.remap_token(9, bt, 5, nkv, 4, 4) == 7 * 4 + 1
+    assert orc.remap_token(13, bt, 5, nkv, 4, 4) == -1     # physical 9 >= 8
+    assert orc.remap_token(17, bt, 5, nkv, 4, 4) == 3 * 4 + 1
+    assert orc.remap_token(17, bt, 4, nkv, 4, 4) == -1     # block 4 >= max_blocks 4
+    assert orc.remap_token(20, bt, 5, nkv, 4, 4) == -1     # block 5 past the row
+
+
+def pin_planted_winners(orc, seed=21):
+    """Keys equal to 3*sign(sum_h q_h) reach the largest score any key in {-3..3}
+    can reach, so K planted pools are exactly the kept set of their row."""
+    w = workloads.build_workload([[2000]], name="planted", seed=seed, integer_mode=True,
+                                 index_topk=256, kpool=4)
+    K = 64
+    P = 2000 // 4
+    rng = np.random.default_rng(seed)
+    planted = np.sort(rng.choice(P, size=K, replace=False))
+    Q = w.q[0].astype(np.int64).sum(axis=0)
+    best = (3 * np.sign(Q)).astype(np.float16)
+    kc = w.key_cache.reshape(w.num_key_pages, -1, 64, 128)
+    for j in planted:
+        kc[w.key_page_table[0, j // 64], 0, j % 64] = best
+    out = orc.select(w)
+    tok = out["token_idx"][0]
+    want = np.concatenate([(planted[:, None] * 4 + np.arange(4)[None, :]).ravel(),
+                           np.arange(P * 4, 2000)])
+    assert np.array_equal(tok[:want.size], want)
+    assert np.all(tok[want.size:] == -1)
+
+
+def pin_pipeline_counts(orc):
+    """Whole selection on the tiny and 32K workloads: valid counts follow the closed
+    form, token rows are ascending, and every slot lies inside its request's blocks."""
+    for name in ("tiny", "decode32k"):
+        w = workloads.make_workload(name)
+        out = orc.select(w)
+        ctx = w.row_contexts()
+        want = np.where(ctx <= w.index_topk, ctx, w.index_topk + ctx % w.kpool)
+        assert np.array_equal(out["counts"], want.astype(np.int32))
+        for r in range(w.num_rows):
+            req = int(np.searchsorted(w.qsl, r, side="right") - 1)
+            n = out["counts"][r]
+            tok = out["token_idx"][r]
+            assert np.all(np.diff(tok[:n]) > 0) and np.all(tok[n:] == -1)
+            allowed = set()
+            nblk = -(-int(ctx[r]) // 64)
+            for b in range(nblk):
+                base = int(w.block_table[req, b]) * w.block_stride_rows
+                allowed.update(range(base, base + 64))
+            sl = out["slots"][r][:n]
+            assert all(int(s) in allowed for s in sl)
+            assert np.all(out["slots"][r][n:] == -1)
+
+
+def pin_integer_scores_match_exact(orc):
+    """Scores of the tiny workload equal exact int64 dot products through the tables."""
+    w = workloads.make_workload("tiny")
+    sc, ab, st = orc.score_rows(w)
+    assert st == 0
+    qi = w.q.astype(np.int64)
+    kc = w.key_cache.reshape(w.num_key_pages, -1, 64, 128)[:, 0]
+    for r in range(w.num_rows):
+        req = int(np.searchsorted(w.qsl, r, side="right") - 1)
+        P = int(w.positions[r] + 1) // w.kpool
+        keys = kc[w.key_page_table[req, :(P + 63) // 64]].reshape(-1, 128)[:P].astype(np.int64)
+        exact = keys @ qi[r].sum(axis=0)
+        assert np.array_equal(sc[r, :P], exact.astype(np.float32))
+
+
+ALL_PINS = [pin_half_decode, pin_score_integer_exact, pin_score_normal_bound,
+            pin_topk_bruteforce, pin_topk_all_zero, pin_topk_stable_argsort,
+            pin_expand_closed_form, pin_remap_identity, pin_remap_inverse, pin_remap_guards,
+            pin_planted_winners, pin_pipeline_counts, pin_integer_scores_match_exact]

@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each.
+
+Each mutant is compiled from the oracle's C source with one textual change; the
+pins must then fail. This shows the pins constrain every step of the oracle (fp16
+decoding, score terms, order, tie-break, expansion, trailing pool, remap, guards,
+row context) rather than only re-stating it.
+"""
+
+import pytest
+
+import oracle
+from _pins import ALL_PINS
+
+MUTANTS = {
+    "dropped_head": [("for (int h = 0; h < heads; ++h)", "for (int h = 1; h < heads; ++h)")],
+    "transposed_q": [("q_row[h * dim + d]", "q_row[d * heads + h]")],
+    "wrong_sign_decode": [("return (float)(sign ? -v : v);", "return (float)(v);")],
+    "subnormal_scale": [("ldexp((double)frac, -24)", "ldexp((double)frac, -25)")],
+    "ties_to_higher_index": [("return a->j < b->j;", "return a->j > b->j;")],
+    "ascending_scores": [("return a->s > b->s;", "return a->s < b->s;")],
+    "one_pool_short": [("int32_t n = K < P ? K : P;", "int32_t n = K < P ? K - 1 : P;")],
+    "no_trailing_pool": [("for (int64_t t = P * kpool; t < ctx; ++t)",
+                          "for (int64_t t = P * kpool; t < P * kpool; ++t)")],
+    "remap_offset": [("return (int64_t)ph * block_stride_rows + (t % block_size);",
+                      "return (int64_t)ph * block_stride_rows + (t / block_size);")],
+    "remap_stride_is_block": [("return (int64_t)ph * block_stride_rows + (t % block_size);",
+                               "return (int64_t)ph * block_size + (t % block_size);")],
+    "missing_block_guard": [("if (b >= max_blocks)", "if (b > max_blocks)")],
+    "missing_physical_guard": [("if (ph < 0 || ph >= num_kv_blocks)", "if (ph < 0)")],
+    "context_is_position": [("int64_t ctx = (int64_t)p->positions[r] + 1;",
+                             "int64_t ctx = (int64_t)p->positions[r];")],
+    "key_row_from_page": [("(int64_t)(j % p->key_page_size) * p->dim",
+                           "(int64_t)(j / p->key_page_size) * p->dim"),
+                          ("(j % p->key_page_size) * p->dim", "(j / p->key_page_size) * p->dim")],
+    "kept_pools_not_sorted": [("    qsort(out, (size_t)n, sizeof(int32_t), orc_cmp_int);\n", "")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    so = oracle.build_variant(MUTANTS[name], name)
+    failed = []
+    with oracle.using_library(so):
+        for pin in ALL_PINS:
+            try:
+                pin(oracle)
+            except AssertionError:
+                failed.append(pin.__name__)
+                break
+    assert failed, f"no pin caught the planted mistake {name}"
