@@ -1,0 +1,408 @@
+"""Benchmark of the fused sparse-attention token selection (sel_select) on GB300.
+
+One step = one pass of the whole selection (segment builder, scorer, top-k with
+expansion and remap) over one batch of the 128K-context decode workload: 8 requests
+x 5 rows at contexts 131,068..131,072, 4 heads x 128 dims fp16 queries and
+compressed keys drawn from N(0,1)/sqrt(128), kpool 4, index_topk 2048, shuffled 64-token
+blocks and key pages interleaved with other layers' pages. Inputs are synthetic and
+seeded (workloads.make_workload("decode128k")).
+
+Timing: the step is captured once in a CUDA graph and replayed; before every timed
+replay a 2 x L2-sized buffer is written (outside the timed events) so the 64 MiB of
+keys come from HBM. Each replay is bracketed by CUDA events on the replay stream.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle on the host
+cores instead (the same workload, a bounded sample of rows per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "selected rows/s and achieved HBM GB/s (% of GB300 peak) at 128K context"
+UNIT = "rows/s"
+WORKLOAD_DESC = ("decode 8 requests x 5 rows at 128K context (ctx 131,068..131,072), H=4, D=128 fp16 "
+                 "N(0,1)/sqrt(128), kpool 4, index_topk 2048, 64-token blocks (stride 128 rows), "
+                 "key pages interleaved (stride 2 pages)")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode128k", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local, world
+
+
+# ---------------------------------------------------------------- byte accounting
+def algorithmic_bytes(w):
+    """Per-step algorithmic bytes of the selection (and of the scorer alone).
+
+    Key-cache bytes each request's complete visible pools need, read once per request
+    (only requests with a row whose context exceeds index_topk; 256 B per pool), the
+    query rows that are scored (1 KiB each), the key-page-table and block-table rows
+    (once per request), positions and query_start_loc, and the int32 slots [rows, W]
+    plus valid counts written."""
+    ctx = w.positions.astype(np.int64) + 1
+    keys = q = kpt = bt = 0
+    for i in range(w.num_reqs):
+        lo, hi = int(w.qsl[i]), int(w.qsl[i + 1])
+        c = ctx[lo:hi]
+        big = c[c > w.index_topk]
+        if big.size:
+            pools = int(big.max()) // w.kpool
+            keys += pools * 128 * 2
+            q += big.size * 4 * 128 * 2
+            kpt += -(-pools // 64) * 4
+        if hi > lo:
+            bt += -(-int(c.max()) // w.block_size) * 4
+    meta = w.num_rows * 4 + (w.num_reqs + 1) * 4
+    out = w.num_rows * w.out_width * 4 + w.num_rows * 4
+    return dict(step=keys + q + kpt + bt + meta + out, scorer=keys + q + kpt, keys=keys, topk_out=out + bt)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel_file, workload):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, valid only while
+    the kernel source still has the hash recorded with it."""
+    src = os.path.join(ROOT, "sparse_attention_kv_device_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", f"{kernel_file[:-3]}_{workload}.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        txt = open(prof).read()
+        m_sha = re.search(r"source sha256\[:16\]:\s*([0-9a-f]{16})", txt)
+        m_b = re.search(r"dram bytes per launch:\s*([0-9]+)", txt)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return int(m_b.group(1))
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/sel_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+def time_oracle(w, rows_per_step, steps, warmup, threads):
+    import oracle
+    n = w.num_rows
+    times = []
+    cursor = 0
+    for s in range(warmup + steps):
+        rows = (np.arange(rows_per_step) + cursor) % n
+        cursor = (cursor + rows_per_step) % n
+        t0 = time.perf_counter()
+        oracle.select(w, rows=rows.astype(np.int32), nthreads=threads)
+        dt = time.perf_counter() - t0
+        if s >= warmup:
+            times.append(dt)
+    return float(np.sum(times)), times
+
+
+def cpu_baseline(w, budget_s=12.0):
+    import oracle
+    threads = os.cpu_count() or 1
+    rows = np.arange(w.num_rows, dtype=np.int32)
+    done, t_total = 0, 0.0
+    while t_total < budget_s and done < 50:
+        t0 = time.perf_counter()
+        oracle.select(w, rows=rows, nthreads=threads)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return {"value": done * w.num_rows / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} full steps ({w.num_rows} rows each) of the {w.name} workload, "
+                      f"{threads} threads, {t_total:.1f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    w = workloads.make_workload(args.config)
+    threads = os.cpu_count() or 1
+    rows_per_step = min(threads, w.num_rows)
+    total, times = time_oracle(w, rows_per_step, args.steps, args.warmup, threads)
+    value = rows_per_step * args.steps / total
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD_DESC if args.config == "decode128k" else args.config,
+                       "rows_per_step": rows_per_step, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{rows_per_step} rows of the {w.name} workload per step "
+                                       f"(rotating over its {w.num_rows} rows), {threads} threads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_kv_device_gb300 as sel
+
+    rank, local, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = workloads.make_workload(args.config)
+    prob = sel.problem_from_workload(w, dev)
+    rows = w.num_rows
+    slots = torch.empty((rows, w.out_width), dtype=torch.int32, device=dev)
+    counts = torch.empty(rows, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(sel.sel_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        sel.sel_select(prob, slots, counts, status=status, ws=ws)
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} on the warm-up step")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sel.sel_select(prob, slots, counts, status=status, ws=ws)
+
+    def flush():
+        if not args.no_flush:
+            flush_buf.zero_()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush()
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region: K graph replays, each between its own events, L2 flushed before each
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush()
+            ev_s[i].record(stream)
+            graph.replay()
+            ev_e[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in zip(ev_s, ev_e)])
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * rows * args.steps / (total_ms / 1e3)
+    ok_status = int(status.item())
+
+    # ---- per-kernel times from trace events captured into a second graph
+    trace = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    sel.sel_set_trace_events(trace)
+    try:
+        tgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tgraph, stream=stream):
+            sel.sel_select(prob, slots, counts, status=status, ws=ws)
+    finally:
+        sel.sel_set_trace_events(None)
+    n_tr = min(args.steps, 100)
+    parts = np.zeros((n_tr, 3))
+    with torch.cuda.stream(stream):
+        for i in range(n_tr):
+            flush()
+            tgraph.replay()
+            stream.synchronize()
+            parts[i] = [trace[j].elapsed_time(trace[j + 1]) for j in range(3)]
+    kern_ms = parts.mean(axis=0)   # builder, scorer, top-k+remap
+
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    names = ["k_build_segments", "k_score_segments", "k_topk_expand"]
+    dom = int(np.argmax(kern_ms))
+    dom_bytes = [w.num_rows * 8 + (w.num_reqs + 1) * 4, ab["scorer"], ab["topk_out"]][dom]
+    achieved = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic("k_score.cu", args.config) if dom == 1 else None
+    step_gbs = ab["step"] / (total_ms / args.steps * 1e-3) / 1e9
+
+    # ---- end to end through the host-buffer entry point (pinned host inputs and outputs)
+    e2e = None
+    if not args.no_e2e:
+        hp = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hprob = sel.Problem(query_start_loc=hp(w.qsl), positions=hp(w.positions), q=hp(w.q),
+                            key_cache=prob.tensors[3], key_page_table=hp(w.key_page_table),
+                            block_table=hp(w.block_table), index_topk=w.index_topk, kpool=w.kpool,
+                            max_context=w.max_context, key_page_stride=w.key_page_stride,
+                            num_key_pages=w.num_key_pages, num_kv_blocks=w.num_kv_blocks,
+                            block_stride_rows=w.block_stride_rows, max_q_len=w.max_q_len,
+                            max_key_pages_per_req=w.max_key_pages_per_req,
+                            max_blocks_per_req=w.max_blocks_per_req, host_inputs=True)
+        slots_h = torch.empty((rows, w.out_width), dtype=torch.int32).pin_memory()
+        counts_h = torch.empty(rows, dtype=torch.int32).pin_memory()
+        stage = torch.empty(sel.sel_host_stage_bytes(hprob, w.out_width), dtype=torch.uint8, device=dev)
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                sel.sel_select_host(hprob, slots_h, counts_h, stage, ws, stream=stream)
+            for i in range(args.steps):
+                flush()
+                e_s[i].record(stream)
+                sel.sel_select_host(hprob, slots_h, counts_h, stage, ws, stream=stream)
+                e_e[i].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = float(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)))
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = (w.qsl.nbytes + w.positions.nbytes + w.q.nbytes + w.key_page_table.nbytes
+               + w.block_table.nbytes)
+        d2h = rows * w.out_width * 4 + rows * 4
+        e2e = {"value": world * rows * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC if args.config == "decode128k" else args.config,
+                       "rows": rows, "requests": w.num_reqs, "out_width": w.out_width,
+                       "l2": "flushed before every step (2x L2 buffer written outside the timed events)"
+                             if not args.no_flush else "not flushed",
+                       "timing": "CUDA-graph replay of sel_select, CUDA events per step on the replay stream",
+                       "parallelism": f"replicas x{world}"},
+            "step_ms": {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
+                        "p90": float(np.percentile(step_ms, 90))},
+            "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
+            "algorithmic_bytes_per_step": ab["step"],
+            "kernel_ms": {n: float(v) for n, v in zip(names, kern_ms)},
+            "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes": dom_bytes, "peak_source": f"{peak_kind} (hbm_gbs)"},
+            "gpu_launches": sel.sel_select_launch_count(prob) * args.steps,
+            "status": ok_status,
+            "wall_s_timed_region": t_wall,
+        }
+        if clk:
+            line["clocks"] = clk
+        if e2e:
+            line["e2e"] = e2e
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,380 @@
+// K-b: request-segmented paged scorer on the 5th-generation tensor cores.
+//
+// What it computes (ReVolta PR #59, "Change"; the score definition is the plain one,
+// sum over the 4 heads of q_h . k, accumulated in fp32):
+//     scores[r][j] = sum_{h<4} sum_{d<128} q[r][h][d] * key(j)[d]
+// for every row r of a segment and every pool j the row may score. The PR's idea is
+// kept: the rows of one request share its key page table, so each 64-key page is
+// loaded once per segment of rows and multiplied against all of the segment's
+// rows x 4 heads at once. The design is GB300's own:
+//   * each tile is two key pages (128 pools = the MMA's M); TMA copies the pages
+//     (128-byte swizzle, evict-first) into a ring of shared-memory stages;
+//   * one thread issues tcgen05.mma (M=128, N = rows*4 padded to 16, K=16, fp16 in,
+//     fp32 accumulate) with the keys as A and the segment's queries as B, into one
+//     of two TMEM accumulators;
+//   * four epilogue warps read the accumulator (one TMEM lane = one pool per thread),
+//     add each row's 4 head columns, and store the row scores coalesced;
+//   * every CTA takes an even share of all segments' tiles (segments may change
+//     inside a CTA's share, so the queries are double-buffered too).
+// Pools on key pages whose id is out of range score -inf and raise SEL_ST_KEYPAGE_OOB.
+#include "sel_device.cuh"
+#include "sel_kernels.h"
+
+namespace sel {
+
+SEL_PHASE_TABLE(score)
+
+namespace {
+
+constexpr int kRecBatch = 128;  // tile records staged in shared memory per producer batch
+
+struct ScoreSmem {
+    uint8_t* a;        // stages x kTileBytes (keys)
+    uint8_t* q;        // 2 x npad_max x 256 B (queries, two K halves each)
+    int4* rec;         // [kRecBatch] tile records of the producer's current batch
+    uint64_t* full;    // [stages]
+    uint64_t* empty;   // [stages]
+    uint64_t* tfull;   // [2]
+    uint64_t* tempty;  // [2]
+    uint64_t* qfull;   // [2]
+    uint64_t* qempty;  // [2]
+    uint64_t* done;    // [1]
+    uint32_t* tmem_base;
+    int* abort_flag;
+    int* oob_flag;
+};
+
+__device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_max) {
+    ScoreSmem s;
+    const uint32_t base = smem_u32(raw);
+    uint8_t* p = raw + (((base + 1023u) & ~1023u) - base);
+    s.a = p;
+    p += static_cast<size_t>(stages) * kTileBytes;
+    s.q = p;
+    p += 2u * static_cast<size_t>(npad_max) * 256u;
+    s.rec = reinterpret_cast<int4*>(p);
+    p += kRecBatch * sizeof(int4);
+    uint64_t* b = reinterpret_cast<uint64_t*>(p);
+    s.full = b;
+    s.empty = b + stages;
+    s.tfull = b + 2 * stages;
+    s.tempty = s.tfull + 2;
+    s.qfull = s.tempty + 2;
+    s.qempty = s.qfull + 2;
+    s.done = s.qempty + 2;
+    uint32_t* w = reinterpret_cast<uint32_t*>(s.done + 1);
+    s.tmem_base = w;
+    s.abort_flag = reinterpret_cast<int*>(w + 1);
+    s.oob_flag = reinterpret_cast<int*>(w + 2);
+    return s;
+}
+
+// Pools a row may score: its complete pools, when the row needs scoring.
+__device__ __forceinline__ int row_pool_limit(const ScoreArgs& a, int row) {
+    const int32_t c = __ldg(a.row_ctx + row - a.row_begin);
+    return (c > 0 && (a.score_all || c > a.topk)) ? min(c / a.kpool, a.pool_cap) : 0;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    k_score_segments(const ScoreArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_q) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ScoreSmem sm = carve(smem_raw, a.stages, a.npad_max);
+    const uint32_t qhalf_bytes = static_cast<uint32_t>(a.npad_max) * 128u;
+    // diagnostics: CTA 0 and CTA gridDim/2 stamp their phases (slot bases 0 and 256)
+    const int trace_base = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x / 2 ? 256 : -1);
+    (void)trace_base;
+    if (trace_base >= 0 && threadIdx.x == 0) SEL_PHASE(trace_base + 0);
+
+    // ---- prologue (overlaps the segment builder when launched as a dependent grid)
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 4 * 32);
+            mbar_init(&sm.qfull[i], 1);
+            mbar_init(&sm.qempty[i], 1);
+        }
+        mbar_init(sm.done, 1);
+        *sm.abort_flag = 0;
+        *sm.oob_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_base, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    volatile int* abort_flag = sm.abort_flag;
+
+    if (trace_base >= 0 && threadIdx.x == 0) SEL_PHASE(trace_base + 1);
+    pdl_wait();               // the builder's outputs are visible from here on
+    pdl_launch_dependents();  // the top-k grid may be scheduled as CTAs retire
+    if (trace_base >= 0 && threadIdx.x == 0) SEL_PHASE(trace_base + 2);
+
+    const int total = a.hdr[1];
+    const int t0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+    const int t1 = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+
+    if (t0 < t1 && warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        const uint64_t pol_k = l2_policy_evict_first();
+        const uint64_t pol_q = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        int qb = 1, cur = -1;
+        int q_uses0 = 0, q_uses1 = 0;          // segments loaded into query buffer 0 / 1
+        uint32_t qe_phase = 0;                 // bit b: parity to wait on query buffer b's release
+        uint32_t loaded = 0, last_parity = 0;  // stages holding a load, parity of their last load
+        bool ok = true;
+        for (int tb = t0; tb < t1 && ok; tb += kRecBatch) {
+            const int te = min(t1, tb + kRecBatch);
+            for (int t = tb + lane; t < te; t += 32) sm.rec[t - tb] = a.tiles[t];
+            __syncwarp();
+            if (lane == 0) {
+                for (int t = tb; t < te && ok; ++t) {
+                    const int4 rec = sm.rec[t - tb];
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    const int npages = rec.w == -2 ? 1 : 2;
+                    mbar_expect_tx(&sm.full[stage], static_cast<uint32_t>(npages) * kPageBytes);
+                    uint8_t* adst = sm.a + static_cast<size_t>(stage) * kTileBytes;
+                    loaded |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    for (int h = 0; h < npages; ++h) {
+                        const int pg = max(h == 0 ? rec.z : rec.w, 0);  // out-of-range pages: the epilogue writes -inf
+                        tma_load_3d(adst + h * kBoxBytes, &tmap_k, &sm.full[stage], 0, 0, pg, pol_k);
+                        tma_load_3d(adst + kPageBytes + h * kBoxBytes, &tmap_k, &sm.full[stage], 64, 0, pg, pol_k);
+                    }
+                    if (trace_base >= 0 && t == t0) SEL_PHASE(trace_base + 3);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                    if (rec.x != cur) {
+                        // the segment's queries, after its first key tile is on its way
+                        const int4 sd = a.seg[rec.x];
+                        qb ^= 1;
+                        if ((qb ? q_uses1 : q_uses0) > 0) {
+                            if (!mbar_wait(&sm.qempty[qb], (qe_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
+                            qe_phase ^= 1u << qb;
+                        }
+                        if (qb) ++q_uses1; else ++q_uses0;
+                        const int nbox = (sd.z + 3) / 4;
+                        mbar_expect_tx(&sm.qfull[qb], static_cast<uint32_t>(nbox) * 2u * kQBoxBytes);
+                        uint8_t* qdst = sm.q + qb * 2 * qhalf_bytes;
+                        for (int i = 0; i < nbox; ++i) {
+                            tma_load_3d(qdst + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 0, 0, sd.y + 4 * i, pol_q);
+                            tma_load_3d(qdst + qhalf_bytes + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 64, 0,
+                                        sd.y + 4 * i, pol_q);
+                        }
+                        cur = rec.x;
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0) {
+            if (ok) {
+                // drain: every stage's last load consumed, every query buffer released
+                for (int i = 0; i < a.stages && ok; ++i) {
+                    ok = mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok && q_uses0 > 0) ok = mbar_wait(&sm.qempty[0], qe_phase & 1u, abort_flag);
+                if (ok && q_uses1 > 0) ok = mbar_wait(&sm.qempty[1], (qe_phase >> 1) & 1u, abort_flag);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, kStTimeout);
+                // let every copy already issued land before the CTA leaves (bounded)
+                for (int i = 0; i < a.stages; ++i)
+                    if (loaded & (1u << i)) mbar_wait(&sm.full[i], (last_parity >> i) & 1u, nullptr);
+                if (q_uses0 > 0) mbar_wait(&sm.qfull[0], static_cast<uint32_t>(q_uses0 - 1) & 1u, nullptr);
+                if (q_uses1 > 0) mbar_wait(&sm.qfull[1], static_cast<uint32_t>(q_uses1 - 1) & 1u, nullptr);
+            }
+        }
+    } else if (t0 < t1 && warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            int qb = 1, cur = -1;
+            uint32_t qf_phase = 0;  // bit b: parity of query buffer b's next fill
+            uint32_t idesc = 0;
+            const uint32_t a_base = smem_u32(sm.a);
+            const uint32_t q_base = smem_u32(sm.q);
+            int4 next = a.tiles[t0];
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                const int4 rec = next;
+                if (t + 1 < t1) next = a.tiles[t + 1];  // in flight while this tile waits
+                if (rec.x != cur) {
+                    const int4 sd = a.seg[rec.x];
+                    qb ^= 1;
+                    if (!mbar_wait(&sm.qfull[qb], (qf_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
+                    qf_phase ^= 1u << qb;
+                    const uint32_t npad = static_cast<uint32_t>(((sd.z + 3) / 4) * 16);
+                    idesc = umma_idesc_f16_f32(kTilePools, npad);
+                    cur = rec.x;
+                }
+                if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
+                if (trace_base >= 0 && t - t0 < 48) SEL_PHASE(trace_base + 8 + (t - t0));
+                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc) * a.acc_cols;
+                const uint32_t abase = a_base + static_cast<uint32_t>(stage) * kTileBytes;
+                const uint32_t bbase = q_base + static_cast<uint32_t>(qb) * 2u * qhalf_bytes;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t koff = static_cast<uint32_t>(kk & 3) * 32u;
+                    const uint64_t ad = umma_desc_sw128(abase + static_cast<uint32_t>(kk >> 2) * kPageBytes + koff);
+                    const uint64_t bd = umma_desc_sw128(bbase + static_cast<uint32_t>(kk >> 2) * qhalf_bytes + koff);
+                    umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&sm.empty[stage]);
+                umma_commit(&sm.tfull[acc]);
+                if (t + 1 == t1 || next.x != rec.x) umma_commit(&sm.qempty[qb]);
+                if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, kStTimeout);
+            }
+            // all issued MMAs finished before teardown
+            umma_commit(sm.done);
+            mbar_wait(sm.done, 0, nullptr);
+        }
+    } else if (t0 < t1) {
+        // ------------------------------------------------------------ epilogue (warps 2-5)
+        // Warp-local only: each warp waits on its own, holds the segment's per-row
+        // pool limits in its lanes, and never waits for the other epilogue warps.
+        const int quarter = warp & 3;             // TMEM lanes this warp may access
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int cur = -1;
+        int4 sd = make_int4(0, 0, 0, 0);
+        int lim_lo = 0, lim_hi = 0;               // pools row `lane` / `lane + 32` may score
+        int oob = 0;
+        int4 next = a.tiles[t0];
+        for (int t = t0; t < t1; ++t) {
+            const int4 rec = next;
+            if (t + 1 < t1) next = a.tiles[t + 1];
+            if (rec.x != cur) {
+                sd = a.seg[rec.x];
+                lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
+                lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
+                cur = rec.x;
+            }
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&sm.tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report(a.status, kStTimeout);
+                }
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            if (trace_base >= 0 && warp == 2 && lane == 0 && t - t0 < 48) SEL_PHASE(trace_base + 64 + (t - t0));
+            const int p_in_tile = quarter * 32 + lane;
+            const int j = rec.y * kTilePools + p_in_tile;
+            const bool page_ok = (p_in_tile < kPagePools ? rec.z : rec.w) >= 0;
+            if (!page_ok && j < sd.w) oob = 1;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc) * a.acc_cols;
+            float* out = a.scores + static_cast<int64_t>(sd.y - a.row_begin) * a.scores_ld + j;
+            for (int rg = 0; rg * 8 < sd.z; ++rg) {
+                uint32_t v[32];
+                __syncwarp();
+                tmem_ld32(taddr + static_cast<uint32_t>(rg * 32), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int r = rg * 8 + rr;
+                    if (r >= sd.z) break;  // uniform over the warp
+                    const int lim = __shfl_sync(0xffffffffu, r < 32 ? lim_lo : lim_hi, r & 31);
+                    const bool ok = j < lim;
+                    const float h0 = __uint_as_float(v[4 * rr + 0]);
+                    const float h1 = __uint_as_float(v[4 * rr + 1]);
+                    const float h2 = __uint_as_float(v[4 * rr + 2]);
+                    const float h3 = __uint_as_float(v[4 * rr + 3]);
+                    const float sc = page_ok ? ((h0 + h1) + h2) + h3 : -__int_as_float(0x7f800000);
+                    if (ok) out[static_cast<int64_t>(r) * a.scores_ld] = sc;
+                    if (a.hist) {
+                        // level-1 histogram of the row (top 11 key bits), one add per distinct bin of the warp
+                        const uint32_t bin = ok ? (ordered_key(sc) >> 21) : 0xffffffffu;
+                        const uint32_t same = __match_any_sync(0xffffffffu, bin);
+                        if (ok && lane == __ffs(same) - 1)
+                            atomicAdd(a.hist + static_cast<int64_t>(sd.y - a.row_begin + r) * kTopkBins + bin,
+                                      static_cast<uint32_t>(__popc(same)));
+                    }
+                }
+            }
+            tc_fence_before();
+            if (trace_base >= 0 && warp == 2 && lane == 0 && t - t0 < 48) SEL_PHASE(trace_base + 128 + (t - t0));
+            mbar_arrive(&sm.tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (__any_sync(0xffffffffu, oob) && lane == 0) *sm.oob_flag = 1;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+    if (threadIdx.x == 0 && *sm.oob_flag) report(a.status, kStKeyPageOob);
+    if (trace_base >= 0 && threadIdx.x == 0) {
+        SEL_PHASE(trace_base + 200);
+        SEL_PHASE_VALUE(trace_base + 201, t1 - t0);
+    }
+    if (threadIdx.x == 0 && blockIdx.x < 200) SEL_PHASE(300 + blockIdx.x);  // every CTA's end
+}
+
+size_t score_smem_bytes(int stages, int npad_max) {
+    return 1024 + static_cast<size_t>(stages) * kTileBytes + 2u * static_cast<size_t>(npad_max) * 256u +
+           kRecBatch * sizeof(int4) + 512;
+}
+
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
+                         size_t smem, bool pdl, cudaStream_t s) {
+    static size_t configured[kMaxDevicesTracked] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_score_segments, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured[dev] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kScoreThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_score_segments, a, tmap_k, tmap_q);
+}
+
+}  // namespace sel

@@ -1,0 +1,589 @@
+// Host side of libsel: argument checks, workspace planning, TMA descriptor encoding
+// and the launch sequence behind every entry point of include/sel.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "sel.h"
+#include "sel_device.cuh"
+#include "sel_kernels.h"
+
+using namespace sel;
+
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kTopkSliceTarget = 8192;   // keys per CTA the top-k cluster aims for
+constexpr int kTopkMaxCluster = 8;       // portable cluster size
+constexpr int kMaxSegRows = 64;          // rows x 4 heads <= 256 = the MMA's largest N
+constexpr int kMaxChunkRows = 32768;
+constexpr int kTopkMaxBtCap = 8192;      // block-table entries a top-k CTA stages at most
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+uint32_t next_pow2(uint32_t x) {
+    uint32_t p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    int sms = 0;
+    int max_smem_optin = 0;
+};
+
+int current_device_info(DeviceInfo* out) {
+    static DeviceInfo cache[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SEL_ECUDA;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev].sms == 0) {
+        int sms = 0, smem = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SEL_ECUDA;
+        cache[dev].sms = sms;
+        cache[dev].max_smem_optin = smem;
+    }
+    *out = cache[dev];
+    return SEL_OK;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// fp16 [pages][64 rows][128] with page stride `page_stride` elements; box = one 64-row x
+// 64-dim half page in the 128-byte swizzle layout the tensor-core descriptors expect.
+int encode_key_map(CUtensorMap* m, const void* base, int64_t num_pages, int64_t page_stride) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return SEL_ECUDA;
+    cuuint64_t dims[3] = {128, 64, static_cast<cuuint64_t>(num_pages)};
+    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(page_stride) * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SEL_OK : SEL_ECUDA;
+}
+
+// fp16 [rows][4 heads][128] with row stride `row_stride` elements; box = 4 rows x 4
+// heads x 64 dims (16 query lines), same swizzle.
+int encode_q_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_stride) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return SEL_ECUDA;
+    cuuint64_t dims[3] = {128, 4, static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(row_stride) * 2};
+    cuuint32_t box[3] = {64, 4, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SEL_OK : SEL_ECUDA;
+}
+
+// ------------------------------------------------------------------ planning
+struct TopkPlan {
+    int cluster = 1;
+    int slice_cap = 4;
+    int bt_cap = 0;
+    size_t smem = 0;
+};
+
+// Cluster size and shared-memory plan of the top-k for rows of up to max_pools pools:
+// at least one CTA per kTopkSliceTarget keys, and as many CTAs (up to the portable
+// cluster size) as fill one wave of two CTAs per SM for `rows` rows. With remap, each CTA
+// also stages the block-table entries its slice's tokens need.
+int plan_topk(int64_t max_pools, int rows, int sms, int kpool, int block_size, bool remap, int max_smem,
+              TopkPlan* t) {
+    const int64_t mp = std::max<int64_t>(max_pools, 1);
+    const int64_t need = ceil_div(mp, kTopkSliceTarget);
+    const int64_t fill = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / std::max(rows, 1));
+    t->cluster = static_cast<int>(std::min<int64_t>(kTopkMaxCluster, std::max(need, std::min(fill, mp / 512 + 1))));
+    // per-CTA slice length L (multiple of 4); per-thread run R (multiple of 4); capacity T*R
+    const int64_t L = (ceil_div(mp, t->cluster) + 3) & ~int64_t(3);
+    const int64_t R = (ceil_div(L, kTopkThreads) + 3) & ~int64_t(3);
+    t->slice_cap = static_cast<int>(R * kTopkThreads);
+    t->bt_cap = remap ? static_cast<int>(std::min<int64_t>(kTopkMaxBtCap,
+                                                            ceil_div(L * kpool, block_size) + 2))
+                      : 0;
+    t->smem = topk_smem_bytes(t->slice_cap, t->bt_cap);
+    if (t->smem > static_cast<size_t>(max_smem)) return SEL_EUNSUPPORTED;
+    return SEL_OK;
+}
+
+struct Plan {
+    int chunk_rows = 1, seg_rows = 1, max_segs = 1, max_tiles = 1;
+    int64_t max_pools = 0, scores_ld = 4;
+    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0, off_tiles = 0,
+           off_scores = 0, off_hist = 0;
+    int64_t hist_words = 0;
+    size_t ws_score = 0, ws_select = 0;
+    int npad_max = 16, stages = 2;
+    uint32_t acc_cols = 32, tmem_cols = 64;
+    size_t score_smem = 0;
+    TopkPlan topk;
+    int sms = 0;
+};
+
+int check_problem(const sel_problem* p) {
+    if (!p) return SEL_EINVAL;
+    if (p->num_reqs < 0 || p->num_rows < 0 || p->max_context < 0 || p->max_q_len < 0) return SEL_EINVAL;
+    if (p->num_heads != 4 || p->head_dim != 128 || p->key_page_size != 64) return SEL_EUNSUPPORTED;
+    if (p->kpool < 1 || p->index_topk < 1 || p->index_topk % p->kpool != 0) return SEL_EINVAL;
+    if (p->block_size < 1 || p->block_stride_rows < p->block_size) return SEL_EINVAL;
+    if (p->key_page_stride < 64 * 128 || p->q_row_stride < 4 * 128) return SEL_EINVAL;
+    if (p->key_page_stride % 8 != 0 || p->q_row_stride % 8 != 0) return SEL_EUNSUPPORTED;
+    if (p->num_key_pages < 1 || p->num_kv_blocks < 0) return SEL_EINVAL;
+    if (p->max_key_pages_per_req < 0 || p->max_key_pages_per_req > p->kpt_ld) return SEL_EINVAL;
+    if (p->max_blocks_per_req < 0 || p->max_blocks_per_req > p->bt_ld) return SEL_EINVAL;
+    if (p->segment_rows < 0 || p->segment_rows > kMaxSegRows || p->chunk_rows < 0) return SEL_EINVAL;
+    // the key page table must be wide enough for the longest allowed context
+    if (ceil_div(p->max_context / p->kpool, 64) > p->max_key_pages_per_req) return SEL_EINVAL;
+    // slots are int32
+    if (p->num_kv_blocks > 0 &&
+        static_cast<int64_t>(p->num_kv_blocks - 1) * p->block_stride_rows + p->block_size > INT32_MAX)
+        return SEL_EINVAL;
+    if (p->num_rows > 0) {
+        if (!p->query_start_loc || !p->positions || !p->q || !p->key_cache || !p->key_page_table ||
+            !p->block_table)
+            return SEL_EINVAL;
+        if (!aligned16(p->q) || !aligned16(p->key_cache)) return SEL_EUNSUPPORTED;
+    }
+    return SEL_OK;
+}
+
+int make_plan(const sel_problem* p, Plan* pl) {
+    int rc = check_problem(p);
+    if (rc != SEL_OK) return rc;
+    DeviceInfo di;
+    if ((rc = current_device_info(&di)) != SEL_OK) return rc;
+    pl->sms = di.sms;
+    const int rows = std::max(1, p->num_rows);
+    pl->chunk_rows = std::min(std::min(rows, kMaxChunkRows), p->chunk_rows > 0 ? p->chunk_rows : 256);
+    int sr = p->segment_rows;
+    if (sr == 0) sr = p->max_q_len > 0 ? p->max_q_len : rows;
+    pl->seg_rows = std::max(1, std::min(sr, kMaxSegRows));
+    pl->max_segs = std::min(std::max(p->num_reqs, 1), pl->chunk_rows) +
+                   static_cast<int>(ceil_div(pl->chunk_rows, pl->seg_rows)) + 1;
+    pl->max_pools = p->max_context / p->kpool;
+    pl->scores_ld = (std::max<int64_t>(pl->max_pools, 1) + 3) & ~int64_t(3);
+    const int64_t tiles = static_cast<int64_t>(pl->max_segs) * std::max<int64_t>(1, ceil_div(pl->max_pools, 128));
+    if (tiles > INT32_MAX / 16) return SEL_EUNSUPPORTED;
+    pl->max_tiles = static_cast<int>(tiles);
+
+    size_t off = 0;
+    pl->off_hdr = off;
+    off = align256(off + 16 * sizeof(int32_t));
+    pl->off_row_req = off;
+    off = align256(off + sizeof(int32_t) * pl->chunk_rows);
+    pl->off_row_ctx = off;
+    off = align256(off + sizeof(int32_t) * pl->chunk_rows);
+    pl->off_seg = off;
+    off = align256(off + sizeof(int4) * pl->max_segs);
+    pl->off_prefix = off;
+    off = align256(off + sizeof(int32_t) * (pl->max_segs + 1));
+    pl->off_tiles = off;
+    off = align256(off + sizeof(int4) * static_cast<size_t>(pl->max_tiles));
+    pl->ws_score = off;
+    pl->off_scores = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
+    pl->off_hist = off;
+    pl->hist_words = static_cast<int64_t>(pl->chunk_rows) * kTopkBins;
+    off = align256(off + sizeof(uint32_t) * static_cast<size_t>(pl->hist_words));
+    pl->ws_select = off;
+
+    pl->npad_max = ((4 * pl->seg_rows + 15) / 16) * 16;
+    pl->acc_cols = std::max<uint32_t>(32, next_pow2(static_cast<uint32_t>(pl->npad_max)));
+    pl->tmem_cols = 2 * pl->acc_cols;
+    const size_t fixed = score_smem_bytes(0, pl->npad_max);
+    if (fixed + 2 * 32768 > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    pl->stages = static_cast<int>(std::min<size_t>(8, (di.max_smem_optin - fixed) / 32768));
+    pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max);
+    return plan_topk(pl->max_pools, pl->chunk_rows, di.sms, p->kpool, p->block_size, true, di.max_smem_optin,
+                     &pl->topk);
+}
+
+// ------------------------------------------------------------------ tracing
+std::mutex g_trace_mu;
+cudaEvent_t g_trace[4] = {nullptr, nullptr, nullptr, nullptr};
+int g_trace_n = 0;
+
+void trace_record(int i, cudaStream_t s) {
+    if (g_trace_n < 4 || !g_trace[i]) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(g_trace[i], s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(g_trace[i], s);
+}
+
+// ------------------------------------------------------------------ shared launch path
+struct Ws {
+    int32_t* hdr;
+    int32_t* row_req;
+    int32_t* row_ctx;
+    int4* seg;
+    int32_t* prefix;
+    int4* tiles;
+    float* scores;
+    uint32_t* hist;
+};
+
+Ws carve_ws(void* ws, const Plan& pl) {
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    Ws w;
+    w.hdr = reinterpret_cast<int32_t*>(b + pl.off_hdr);
+    w.row_req = reinterpret_cast<int32_t*>(b + pl.off_row_req);
+    w.row_ctx = reinterpret_cast<int32_t*>(b + pl.off_row_ctx);
+    w.seg = reinterpret_cast<int4*>(b + pl.off_seg);
+    w.prefix = reinterpret_cast<int32_t*>(b + pl.off_prefix);
+    w.tiles = reinterpret_cast<int4*>(b + pl.off_tiles);
+    w.scores = reinterpret_cast<float*>(b + pl.off_scores);
+    w.hist = reinterpret_cast<uint32_t*>(b + pl.off_hist);
+    return w;
+}
+
+// Builder + scorer for rows [c0, c1); scores row k of the chunk at scores + k*ld.
+int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int c1, int score_all,
+                         float* scores, int64_t ld, int64_t pool_cap, uint32_t* hist, int32_t* status,
+                         const CUtensorMap& tk, const CUtensorMap& tq, cudaStream_t s) {
+    BuildArgs b{};
+    b.qsl = p->query_start_loc;
+    b.positions = p->positions;
+    b.key_page_table = p->key_page_table;
+    b.kpt_ld = p->kpt_ld;
+    b.max_key_pages = p->max_key_pages_per_req;
+    b.num_key_pages = p->num_key_pages;
+    b.num_reqs = p->num_reqs;
+    b.num_rows = p->num_rows;
+    b.row_begin = c0;
+    b.row_end = c1;
+    b.seg_rows = pl.seg_rows;
+    b.topk = p->index_topk;
+    b.kpool = p->kpool;
+    b.max_context = p->max_context;
+    b.score_all = score_all;
+    b.pool_cap = static_cast<int32_t>(std::min<int64_t>(pool_cap, INT32_MAX));
+    b.max_segs = pl.max_segs;
+    b.max_tiles = pl.max_tiles;
+    b.tiles = w.tiles;
+    b.row_req = w.row_req;
+    b.row_ctx = w.row_ctx;
+    b.seg = w.seg;
+    b.seg_tile_prefix = w.prefix;
+    b.hdr = w.hdr;
+    b.status = status;
+    b.hist = hist;
+    b.hist_words = static_cast<int64_t>(c1 - c0) * kTopkBins;
+    b.zero_ctas = static_cast<int32_t>(std::min<int64_t>(32, std::max<int64_t>(1, b.hist_words / 16384)));
+    if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
+    if (c0 == 0 && !score_all) trace_record(1, s);
+
+    ScoreArgs a{};
+    a.seg = w.seg;
+    a.hdr = w.hdr;
+    a.tiles = w.tiles;
+    a.row_ctx = w.row_ctx;
+    a.row_begin = c0;
+    a.topk = p->index_topk;
+    a.kpool = p->kpool;
+    a.score_all = score_all;
+    a.pool_cap = b.pool_cap;
+    a.scores = scores;
+    a.scores_ld = ld;
+    a.hist = hist;
+    a.npad_max = pl.npad_max;
+    a.stages = pl.stages;
+    a.tmem_cols = pl.tmem_cols;
+    a.acc_cols = pl.acc_cols;
+    a.status = status;
+    if (launch_score(a, tk, tq, pl.sms, pl.score_smem, true, s) != cudaSuccess) return SEL_ECUDA;
+    return SEL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sel_error_string(int code) {
+    switch (code) {
+        case SEL_OK: return "ok";
+        case SEL_EINVAL: return "invalid argument (null pointer, negative or inconsistent size)";
+        case SEL_EUNSUPPORTED: return "unsupported shape or alignment (needs 4 heads, 128 dims, 64-key pages, 16-B aligned buffers)";
+        case SEL_ECUDA: return "a CUDA call failed";
+        case SEL_EWORKSPACE: return "workspace smaller than the size query returned";
+        default: return "unknown error";
+    }
+}
+
+int sel_version(void) { return 100; }
+
+size_t sel_workspace_bytes(const sel_problem* p) {
+    Plan pl;
+    return make_plan(p, &pl) == SEL_OK ? pl.ws_select : 0;
+}
+
+size_t sel_score_workspace_bytes(const sel_problem* p) {
+    Plan pl;
+    return make_plan(p, &pl) == SEL_OK ? pl.ws_score : 0;
+}
+
+int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int32_t* status, void* ws,
+                    size_t ws_bytes, sel_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(p, &pl);
+    if (rc != SEL_OK) return rc;
+    if (p->num_rows == 0) return SEL_OK;
+    if (!scores || scores_ld < 1 || !ws) return SEL_EINVAL;
+    if (ws_bytes < pl.ws_score) return SEL_EWORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap tk, tq;
+    if ((rc = encode_key_map(&tk, p->key_cache, p->num_key_pages, p->key_page_stride)) != SEL_OK) return rc;
+    if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
+    Ws w = carve_ws(ws, pl);
+    int32_t* st = status ? status : w.hdr + 8;
+    for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
+        const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
+        rc = launch_chunk_scoring(p, pl, w, c0, c1, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
+                                  scores_ld, nullptr, st, tk, tq, s);
+        if (rc != SEL_OK) return rc;
+    }
+    return SEL_OK;
+}
+
+int sel_topk_expand(const float* scores, int64_t scores_ld, const int32_t* positions, int32_t num_rows,
+                    int32_t index_topk, int32_t kpool, int32_t* token_idx, int32_t out_width,
+                    int32_t* valid_counts, int32_t* status, sel_stream_t stream) {
+    if (num_rows < 0 || kpool < 1 || index_topk < 1 || index_topk % kpool != 0) return SEL_EINVAL;
+    if (num_rows == 0) return SEL_OK;
+    if (!scores || !positions || !token_idx || scores_ld < 1) return SEL_EINVAL;
+    if (out_width < index_topk + kpool - 1 || out_width % 4 != 0 || scores_ld % 4 != 0) return SEL_EINVAL;
+    if (!aligned16(scores) || !aligned16(token_idx)) return SEL_EUNSUPPORTED;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != SEL_OK) return rc;
+    TopkPlan tp;
+    if ((rc = plan_topk(scores_ld, std::min(num_rows, 65535), di.sms, kpool, 1, false, di.max_smem_optin, &tp)) !=
+        SEL_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int c0 = 0; c0 < num_rows; c0 += 65535) {
+        const int rows = std::min(65535, num_rows - c0);
+        TopkArgs a{};
+        a.scores = scores + static_cast<int64_t>(c0) * scores_ld;
+        a.scores_ld = scores_ld;
+        a.positions = positions;
+        a.row_begin = c0;
+        a.topk = index_topk;
+        a.kpool = kpool;
+        a.out_width = out_width;
+        a.max_pools = scores_ld;
+        a.slice_cap = tp.slice_cap;
+        a.bt_cap = 0;
+        a.token_idx = token_idx;
+        a.counts = valid_counts;
+        a.status = status;
+        a.block_size = 1;
+        if (launch_topk(a, false, tp.cluster, rows, tp.smem, false, s) != cudaSuccess) return SEL_ECUDA;
+    }
+    return SEL_OK;
+}
+
+int sel_remap_global(const int32_t* req_id, int32_t num_reqs, const int32_t* block_table, int64_t bt_ld,
+                     int32_t max_blocks_per_req, int32_t num_kv_blocks, const int32_t* token_idx,
+                     int32_t num_rows, int32_t width, int32_t block_size, int64_t block_stride_rows,
+                     int32_t* slots, int32_t* valid_counts, sel_stream_t stream) {
+    if (num_rows < 0 || width < 0 || num_reqs < 0 || block_size < 1 || block_stride_rows < block_size)
+        return SEL_EINVAL;
+    if (max_blocks_per_req < 0 || max_blocks_per_req > bt_ld || num_kv_blocks < 0) return SEL_EINVAL;
+    if (num_kv_blocks > 0 && static_cast<int64_t>(num_kv_blocks - 1) * block_stride_rows + block_size > INT32_MAX)
+        return SEL_EINVAL;
+    if (num_rows == 0) return SEL_OK;
+    if (!req_id || !block_table || !token_idx || !slots) return SEL_EINVAL;
+    if (width % 4 != 0) return SEL_EINVAL;
+    if (!aligned16(token_idx) || !aligned16(slots)) return SEL_EUNSUPPORTED;
+    RemapArgs a{};
+    a.req_id = req_id;
+    a.num_reqs = num_reqs;
+    a.block_table = block_table;
+    a.bt_ld = bt_ld;
+    a.max_blocks = max_blocks_per_req;
+    a.num_kv_blocks = num_kv_blocks;
+    a.block_size = block_size;
+    a.block_stride_rows = block_stride_rows;
+    a.token_idx = token_idx;
+    a.width = width;
+    a.slots = slots;
+    a.counts = valid_counts;
+    return launch_remap(a, num_rows, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,
+               int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {
+    Plan pl;
+    int rc = make_plan(p, &pl);
+    if (rc != SEL_OK) return rc;
+    if (p->num_rows == 0) return SEL_OK;
+    if (!slots || !ws) return SEL_EINVAL;
+    if (out_width < p->index_topk + p->kpool - 1 || out_width % 4 != 0) return SEL_EINVAL;
+    if (!aligned16(slots) || (token_idx && !aligned16(token_idx))) return SEL_EUNSUPPORTED;
+    if (ws_bytes < pl.ws_select) return SEL_EWORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUtensorMap tk, tq;
+    if ((rc = encode_key_map(&tk, p->key_cache, p->num_key_pages, p->key_page_stride)) != SEL_OK) return rc;
+    if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
+    Ws w = carve_ws(ws, pl);
+    int32_t* st = status ? status : w.hdr + 8;
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
+        const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
+        const bool last = c1 == p->num_rows;
+        if (c0 == 0) trace_record(0, s);
+        rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, w.hist, st, tk, tq, s);
+        if (rc != SEL_OK) return rc;
+        if (last) trace_record(2, s);
+        TopkArgs a{};
+        a.scores = w.scores;
+        a.scores_ld = pl.scores_ld;
+        a.positions = p->positions;
+        a.row_ctx = w.row_ctx;
+        a.row_req = w.row_req;
+        a.hist = w.hist;
+        a.row_begin = c0;
+        a.topk = p->index_topk;
+        a.kpool = p->kpool;
+        a.out_width = out_width;
+        a.max_pools = pl.max_pools;
+        a.slice_cap = pl.topk.slice_cap;
+        a.bt_cap = pl.topk.bt_cap;
+        a.token_idx = token_idx;
+        a.slots = slots;
+        a.counts = valid_counts;
+        a.block_table = p->block_table;
+        a.bt_ld = p->bt_ld;
+        a.max_blocks = p->max_blocks_per_req;
+        a.num_kv_blocks = p->num_kv_blocks;
+        a.block_size = p->block_size;
+        a.block_stride_rows = p->block_stride_rows;
+        a.status = st;
+        if (launch_topk(a, true, pl.topk.cluster, c1 - c0, pl.topk.smem, true, s) != cudaSuccess) return SEL_ECUDA;
+        if (last) trace_record(3, s);
+    }
+    return SEL_OK;
+}
+
+int32_t sel_select_launch_count(const sel_problem* p) {
+    Plan pl;
+    if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
+    return static_cast<int32_t>(3 * ceil_div(p->num_rows, pl.chunk_rows));
+}
+
+size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {
+    if (check_problem(p) != SEL_OK || out_width < 0) return 0;
+    size_t off = 0;
+    off = align256(off + sizeof(int32_t) * (p->num_reqs + 1));
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(p->num_rows));
+    off = align256(off + 2 * static_cast<size_t>(p->num_rows) * p->q_row_stride);
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(p->num_reqs) * p->kpt_ld);
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(p->num_reqs) * p->bt_ld);
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width);
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(p->num_rows));
+    return off;
+}
+
+int sel_select_host(const sel_problem* p, int32_t* slots_host, int32_t out_width, int32_t* counts_host,
+                    int32_t* status, void* stage, size_t stage_bytes, void* ws, size_t ws_bytes,
+                    sel_stream_t stream) {
+    int rc = check_problem(p);
+    if (rc != SEL_OK) return rc;
+    if (p->num_rows == 0) return SEL_OK;
+    if (!slots_host || !counts_host || !stage) return SEL_EINVAL;
+    if (stage_bytes < sel_host_stage_bytes(p, out_width)) return SEL_EWORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* b = static_cast<uint8_t*>(stage);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* q = b + off;
+        off = align256(off + bytes);
+        return q;
+    };
+    const size_t n_qsl = sizeof(int32_t) * (p->num_reqs + 1);
+    const size_t n_pos = sizeof(int32_t) * static_cast<size_t>(p->num_rows);
+    const size_t n_q = 2 * (static_cast<size_t>(p->num_rows - 1) * p->q_row_stride + 512);
+    const size_t n_kpt = p->num_reqs ? sizeof(int32_t) * (static_cast<size_t>(p->num_reqs - 1) * p->kpt_ld +
+                                                          p->max_key_pages_per_req)
+                                     : 0;
+    const size_t n_bt = p->num_reqs ? sizeof(int32_t) * (static_cast<size_t>(p->num_reqs - 1) * p->bt_ld +
+                                                         p->max_blocks_per_req)
+                                    : 0;
+    uint8_t* d_qsl = take(n_qsl);
+    uint8_t* d_pos = take(n_pos);
+    uint8_t* d_q = take(2 * static_cast<size_t>(p->num_rows) * p->q_row_stride);
+    uint8_t* d_kpt = take(sizeof(int32_t) * static_cast<size_t>(p->num_reqs) * p->kpt_ld);
+    uint8_t* d_bt = take(sizeof(int32_t) * static_cast<size_t>(p->num_reqs) * p->bt_ld);
+    uint8_t* d_slots = take(sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width);
+    uint8_t* d_counts = take(n_pos);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    if (cudaMemcpyAsync(d_qsl, p->query_start_loc, n_qsl, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(d_pos, p->positions, n_pos, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(d_q, p->q, n_q, h2d, s) != cudaSuccess ||
+        (n_kpt && cudaMemcpyAsync(d_kpt, p->key_page_table, n_kpt, h2d, s) != cudaSuccess) ||
+        (n_bt && cudaMemcpyAsync(d_bt, p->block_table, n_bt, h2d, s) != cudaSuccess))
+        return SEL_ECUDA;
+    sel_problem d = *p;
+    d.query_start_loc = reinterpret_cast<const int32_t*>(d_qsl);
+    d.positions = reinterpret_cast<const int32_t*>(d_pos);
+    d.q = d_q;
+    d.key_page_table = reinterpret_cast<const int32_t*>(d_kpt);
+    d.block_table = reinterpret_cast<const int32_t*>(d_bt);
+    rc = sel_select(&d, reinterpret_cast<int32_t*>(d_slots), out_width, reinterpret_cast<int32_t*>(d_counts),
+                    nullptr, status, ws, ws_bytes, stream);
+    if (rc != SEL_OK) return rc;
+    const cudaMemcpyKind d2h = cudaMemcpyDeviceToHost;
+    if (cudaMemcpyAsync(slots_host, d_slots, sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width, d2h,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(counts_host, d_counts, n_pos, d2h, s) != cudaSuccess)
+        return SEL_ECUDA;
+    return SEL_OK;
+}
+
+int sel_set_trace_events(void* const* events, int32_t n) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (n == 0) {
+        g_trace_n = 0;
+        for (int i = 0; i < 4; ++i) g_trace[i] = nullptr;
+        return SEL_OK;
+    }
+    if (n < 4 || !events) return SEL_EINVAL;
+    for (int i = 0; i < 4; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    g_trace_n = 4;
+    return SEL_OK;
+}
+
+}  // extern "C"

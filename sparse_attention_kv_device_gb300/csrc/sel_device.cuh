@@ -1,0 +1,297 @@
+// Device-side building blocks shared by the selection kernels (sm_103a only):
+// mbarrier waits with a time limit, TMA tensor loads, tcgen05 MMA / TMEM access,
+// block scans, and the ordered-key mapping used by the radix top-k.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libsel targets sm_103a (tcgen05, TMA); compile with -gencode arch=compute_103a,code=sm_103a"
+#endif
+
+namespace sel {
+
+// Shape constants of the path (4 heads x 128 dims fp16, 64 keys per key page).
+constexpr int kHeads = 4;
+constexpr int kHeadDim = 128;
+constexpr int kPagePools = 64;                    // compressed keys per key page
+constexpr int kTilePools = 128;                   // pools per MMA tile (two key pages) = UMMA M
+constexpr uint32_t kBoxBytes = 64 * 128;          // 64 rows x 64 fp16 (one 128-B swizzle column)
+constexpr uint32_t kPageBytes = 2 * kBoxBytes;    // one key page, 16 KiB
+constexpr uint32_t kTileBytes = 2 * kPageBytes;   // one MMA tile of keys, 32 KiB
+constexpr uint32_t kQBoxBytes = 16 * 128;         // 4 query rows x 4 heads x 64 dims
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // every wait gives up after 1 s
+
+// status bits (the same values as SEL_ST_* in include/sel.h)
+constexpr int kStKeyPageOob = 1;
+constexpr int kStCtxOverBound = 2;
+constexpr int kStTimeout = 4;
+constexpr int kStBadQsl = 8;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits until the phase with the given parity has completed. Gives up (returns
+// false) once another role has raised *abort or after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 3-D tiled load into shared memory, completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle
+// layout: 8-row x 128-B swizzle atoms stacked along M/N every 1024 B (stride byte
+// offset), start address in 16-B units, descriptor version 1 (bits 46-48 = 0b001),
+// layout type 2 = SWIZZLE_128B (bits 61-63). The leading byte offset is unused for
+// swizzled K-major operands whose K extent per instruction stays inside one atom.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;             // LBO (ignored): 16 B
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;     // SBO: 1024 B between 8-row groups
+    d |= static_cast<uint64_t>(1u) << 46;             // fixed constant 0b001
+    d |= static_cast<uint64_t>(2u) << 61;             // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D = fp32 (bits 4-5 = 1), A = B = fp16 (bits 7-9,
+// 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t umma_idesc_f16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- phase tracing (diagnostics)
+// Built with -DSEL_PHASE_TRACE, each kernel file declares SEL_PHASE_TABLE(tag): a table
+// of kPhaseSlots global-timer stamps (ns) and an exported reader sel_debug_phases_<tag>.
+// SEL_PHASE(slot) stores the timer into the file's table. Without the define both
+// compile to nothing.
+constexpr int kPhaseSlots = 512;
+#ifdef SEL_PHASE_TRACE
+#define SEL_PHASE_TABLE(tag)                                                              \
+    static __device__ unsigned long long g_sel_phase[::sel::kPhaseSlots];                 \
+    extern "C" int sel_debug_phases_##tag(void* dst, size_t bytes) {                      \
+        if (bytes > sizeof(g_sel_phase)) bytes = sizeof(g_sel_phase);                     \
+        return cudaMemcpyFromSymbol(dst, g_sel_phase, bytes) == cudaSuccess ? 0 : -3;     \
+    }
+#define SEL_PHASE(slot) (g_sel_phase[(slot)] = ::sel::global_timer_ns())
+#define SEL_PHASE_VALUE(slot, v) (g_sel_phase[(slot)] = static_cast<unsigned long long>(v))
+#else
+#define SEL_PHASE_TABLE(tag)
+#define SEL_PHASE(slot) ((void)0)
+#define SEL_PHASE_VALUE(slot, v) ((void)0)
+#endif
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Blocks until the grids this one depends on have completed and their writes are
+// visible (a no-op when the kernel was launched without the dependency attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allows the dependent grid to be scheduled before this one finishes.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------- named barriers
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- scans
+// Inclusive warp scan.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// Exclusive scan over the whole block (blockDim.x a multiple of 32, <= 1024).
+// `scratch` holds >= 33 words of shared memory. Returns the exclusive prefix and
+// writes the block total to *total. Contains two __syncthreads.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    uint32_t incl = warp_incl_scan(v);
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < nwarps ? scratch[lane] : 0u;
+        uint32_t wi = warp_incl_scan(w);
+        if (lane < nwarps) scratch[lane] = wi - w;
+        if (lane == nwarps - 1) scratch[32] = wi;
+    }
+    __syncthreads();
+    uint32_t r = scratch[warp] + incl - v;
+    *total = scratch[32];
+    return r;
+}
+
+// Sum over the block; every thread receives the total. Two __syncthreads.
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* scratch) {
+    uint32_t total;
+    block_excl_scan(v, scratch, &total);
+    return total;
+}
+
+// ---------------------------------------------------------------- keys
+// Maps an fp32 score to an unsigned key with the same order: larger score -> larger
+// key; -0.0 and +0.0 share a key; NaN (outside the input contract) maps to 0, below -inf.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One token through a request's block-table row (the sparse_utils remap):
+// -1 for t < 0, a logical block past max_blocks, or a physical id outside [0, nkv).
+__device__ __forceinline__ int32_t remap_token(int32_t t, const int32_t* __restrict__ bt_row, int32_t max_blocks,
+                                               int32_t nkv, int32_t block_size, int64_t stride) {
+    if (t < 0) return -1;
+    const int32_t b = t / block_size;
+    if (b >= max_blocks) return -1;
+    const int32_t ph = __ldg(bt_row + b);
+    if (ph < 0 || ph >= nkv) return -1;
+    return static_cast<int32_t>(static_cast<int64_t>(ph) * stride + (t - b * block_size));
+}
+
+}  // namespace sel

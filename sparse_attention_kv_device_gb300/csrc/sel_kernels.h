@@ -1,0 +1,119 @@
+// Argument blocks and launchers of the selection kernels. Host and device code both
+// include this file; it holds no device code.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sel {
+
+// Segment builder: one CTA turns query_start_loc / positions into per-row request
+// ids and contexts and a list of request segments (<= seg_rows rows of one request)
+// with the number of 128-pool tiles each must score.
+struct BuildArgs {
+    const int32_t* qsl;        // [num_reqs + 1]
+    const int32_t* positions;  // [num_rows]
+    const int32_t* key_page_table;
+    int64_t kpt_ld;
+    int32_t max_key_pages, num_key_pages;
+    int32_t num_reqs, num_rows;
+    int32_t row_begin, row_end;  // the chunk of rows handled by this launch
+    int32_t seg_rows;
+    int32_t topk, kpool, max_context;
+    int32_t score_all;  // 1: score every row's complete pools; 0: only rows with ctx > topk
+    int32_t pool_cap;   // no row scores more pools than this (the score row length)
+    int32_t max_segs, max_tiles;
+    int32_t* row_req;          // [row_end - row_begin]
+    int32_t* row_ctx;          // [row_end - row_begin]; -1 = no output (padding, bad row)
+    int4* seg;                 // [max_segs] {req, first row, rows, pools to score}
+    int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
+    int4* tiles;               // [max_tiles] {segment, tile in segment, page 0, page 1}
+    int32_t* hdr;              // [0] segments, [1] tiles
+    int32_t* status;
+    uint32_t* hist;            // per-row level-1 histograms the scorer fills; zeroed here (nullable)
+    int64_t hist_words;
+    int32_t zero_ctas;         // extra CTAs that zero `hist` while CTA 0 builds
+    // shared-memory staging plan (filled by launch_build)
+    int32_t smem_qsl, smem_rows, smem_segs;
+    int32_t smem_rows_off, smem_segs_off, smem_prefix_off;
+};
+
+// Segmented scorer (TMA + tcgen05): every CTA scores an even share of all tiles.
+struct ScoreArgs {
+    const int4* seg;
+    const int32_t* hdr;
+    const int4* tiles;
+    const int32_t* row_ctx;  // chunk-local
+    int32_t row_begin;
+    int32_t topk, kpool, score_all, pool_cap;
+    float* scores;           // chunk-local rows
+    int64_t scores_ld;
+    uint32_t* hist;          // chunk-local rows x kTopkBins: counts of the top 11 key bits (nullable)
+    int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
+    int32_t stages;
+    uint32_t tmem_cols;      // TMEM columns allocated (power of two)
+    uint32_t acc_cols;       // columns per accumulator buffer
+    int32_t* status;
+};
+
+// Top-k pools + expansion (+ remap), one thread-block cluster per row.
+struct TopkArgs {
+    const float* scores;       // chunk-local rows
+    int64_t scores_ld;
+    const int32_t* positions;  // global rows; used when row_ctx is null
+    const int32_t* row_ctx;    // chunk-local (builder output) or null
+    const int32_t* row_req;    // chunk-local (builder output), needed with remap
+    const uint32_t* hist;      // chunk-local rows x kTopkBins level-1 histograms (scorer output) or null
+    int32_t row_begin;
+    int32_t topk, kpool, out_width;
+    int64_t max_pools;         // rows with ctx / kpool beyond this are out of bound
+    int32_t slice_cap;         // keys staged in shared memory per CTA
+    int32_t bt_cap;            // block-table entries staged in shared memory per CTA
+    int32_t* token_idx;        // [rows][out_width] global rows, nullable
+    int32_t* slots;            // [rows][out_width] global rows, with remap
+    int32_t* counts;           // [rows] global rows, nullable
+    const int32_t* block_table;
+    int64_t bt_ld;
+    int32_t max_blocks, num_kv_blocks, block_size;
+    int64_t block_stride_rows;
+    int32_t* status;
+};
+
+// Stand-alone block-table remap.
+struct RemapArgs {
+    const int32_t* req_id;
+    int32_t num_reqs;
+    const int32_t* block_table;
+    int64_t bt_ld;
+    int32_t max_blocks, num_kv_blocks, block_size;
+    int64_t block_stride_rows;
+    const int32_t* token_idx;
+    int32_t width;
+    int32_t* slots;
+    int32_t* counts;
+};
+
+constexpr int kBuildThreads = 1024;
+constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kTopkThreads = 512;
+constexpr int kTopkBins = 2048;
+constexpr int kTopkCandCap = 2048;   // threshold-bin keys gathered per row for the local select
+constexpr int kMaxDevicesTracked = 64;
+constexpr int kRemapThreads = 128;
+
+size_t score_smem_bytes(int stages, int npad_max);
+size_t topk_smem_bytes(int slice_cap, int bt_cap);
+
+// Launchers. With `pdl` the kernel is a programmatic dependent of the previous kernel
+// on the stream: its prologue may overlap that kernel, and it waits (griddepcontrol)
+// before reading what that kernel wrote.
+cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
+                         size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs& a, bool remap, int cluster, int rows, size_t smem, bool pdl,
+                        cudaStream_t s);
+cudaError_t launch_remap(const RemapArgs& a, int rows, cudaStream_t s);
+
+}  // namespace sel

@@ -1,0 +1,326 @@
+"""Python binding of libsel (include/sel.h): argument marshalling only.
+
+Every function here has the name of a C entry point, checks that the tensors it is
+given are on the right device with the right dtype and layout, turns them into raw
+pointers and calls the library. All computation happens in the library's CUDA
+kernels; there is no fallback of any kind: if libsel.so is missing or fails to load,
+importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+# SEL_LIBRARY selects another build of the same library (e.g. a diagnostics build)
+_LIB_PATH = os.environ.get("SEL_LIBRARY", _build.LIB)
+
+SEL_OK = 0
+SEL_EINVAL = -1
+SEL_EUNSUPPORTED = -2
+SEL_ECUDA = -3
+SEL_EWORKSPACE = -4
+
+ST_KEYPAGE_OOB = 1
+ST_CTX_OVER_BOUND = 2
+ST_TIMEOUT = 4
+ST_BAD_QSL = 8
+
+
+class SelError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {sel_error_string(code)} (code {code})")
+
+
+class sel_problem(C.Structure):
+    _fields_ = [
+        ("num_reqs", C.c_int32), ("num_rows", C.c_int32), ("max_context", C.c_int32),
+        ("max_q_len", C.c_int32), ("num_heads", C.c_int32), ("head_dim", C.c_int32),
+        ("index_topk", C.c_int32), ("kpool", C.c_int32), ("key_page_size", C.c_int32),
+        ("block_size", C.c_int32), ("block_stride_rows", C.c_int64),
+        ("key_page_stride", C.c_int64), ("num_key_pages", C.c_int32),
+        ("num_kv_blocks", C.c_int32), ("max_key_pages_per_req", C.c_int32),
+        ("max_blocks_per_req", C.c_int32), ("kpt_ld", C.c_int64), ("bt_ld", C.c_int64),
+        ("q_row_stride", C.c_int64), ("segment_rows", C.c_int32), ("chunk_rows", C.c_int32),
+        ("query_start_loc", C.c_void_p), ("positions", C.c_void_p), ("q", C.c_void_p),
+        ("key_cache", C.c_void_p), ("key_page_table", C.c_void_p), ("block_table", C.c_void_p),
+    ]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libsel.so is not built ({_LIB_PATH}); run "
+                          "sparse_attention_kv_device_gb300.build.build() or __graft_entry__.build()")
+    lib = C.CDLL(_LIB_PATH)
+    P, I32, I64, SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+    PP = C.POINTER(sel_problem)
+    lib.sel_error_string.argtypes = [C.c_int]
+    lib.sel_error_string.restype = C.c_char_p
+    lib.sel_version.restype = C.c_int
+    lib.sel_workspace_bytes.argtypes = [PP]
+    lib.sel_workspace_bytes.restype = SZ
+    lib.sel_score_workspace_bytes.argtypes = [PP]
+    lib.sel_score_workspace_bytes.restype = SZ
+    lib.sel_score_paged.argtypes = [PP, P, I64, P, P, SZ, P]
+    lib.sel_topk_expand.argtypes = [P, I64, P, I32, I32, I32, P, I32, P, P, P]
+    lib.sel_remap_global.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I64, P, P, P]
+    lib.sel_select.argtypes = [PP, P, I32, P, P, P, P, SZ, P]
+    lib.sel_host_stage_bytes.argtypes = [PP, I32]
+    lib.sel_host_stage_bytes.restype = SZ
+    lib.sel_select_host.argtypes = [PP, P, I32, P, P, P, SZ, P, SZ, P]
+    lib.sel_set_trace_events.argtypes = [C.POINTER(C.c_void_p), I32]
+    lib.sel_select_launch_count.argtypes = [PP]
+    lib.sel_select_launch_count.restype = I32
+    for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
+              "sel_select_host", "sel_set_trace_events"):
+        getattr(lib, f).restype = C.c_int
+    return lib
+
+
+_lib = _load()
+
+EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_workspace_bytes",
+           "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
+           "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
+           "sel_select_launch_count"]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def sel_error_string(code: int) -> str:
+    return _lib.sel_error_string(int(code)).decode()
+
+
+def sel_version() -> int:
+    return int(_lib.sel_version())
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != SEL_OK:
+        raise SelError(rc, where)
+
+
+def _dev(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class Problem:
+    """A sel_problem plus the device tensors it points into (kept alive here).
+
+    Tensors: query_start_loc int32 [num_reqs+1], positions int32 [num_rows],
+    q fp16 [num_rows, 4, 128] (row stride may exceed 512), key_cache fp16 (any shape,
+    contiguous, physical page p at element p * key_page_stride), key_page_table int32
+    [num_reqs, kpt_ld], block_table int32 [num_reqs, bt_ld].
+    """
+
+    def __init__(self, *, query_start_loc, positions, q, key_cache, key_page_table, block_table,
+                 index_topk, kpool, max_context, key_page_stride, num_key_pages, num_kv_blocks,
+                 block_size=64, block_stride_rows=None, max_key_pages_per_req=None,
+                 max_blocks_per_req=None, max_q_len=0, segment_rows=0, chunk_rows=0,
+                 num_rows=None, host_inputs=False):
+        # host_inputs: the per-step inputs (everything but key_cache) are host tensors,
+        # for sel_select_host; the key cache always lives on the device.
+        _dev(key_cache, torch.float16, "key_cache")
+        for t, dt, n in ((query_start_loc, torch.int32, "query_start_loc"),
+                         (positions, torch.int32, "positions"), (q, torch.float16, "q"),
+                         (key_page_table, torch.int32, "key_page_table"),
+                         (block_table, torch.int32, "block_table")):
+            if host_inputs:
+                if t.is_cuda or t.dtype != dt:
+                    raise ValueError(f"{n} must be a host {dt} tensor")
+            else:
+                _dev(t, dt, n)
+        if q.dim() != 3 or q.shape[1] != 4 or q.shape[2] != 128 or q.stride(2) != 1 or q.stride(1) != 128:
+            raise ValueError("q must be [rows, 4, 128] with contiguous heads")
+        if not (key_cache.is_contiguous() and key_page_table.is_contiguous() and block_table.is_contiguous()
+                and positions.is_contiguous() and query_start_loc.is_contiguous()):
+            raise ValueError("tables, positions and the key cache must be contiguous")
+        self.tensors = (query_start_loc, positions, q, key_cache, key_page_table, block_table)
+        p = sel_problem()
+        p.num_reqs = int(query_start_loc.numel() - 1)
+        p.num_rows = int(positions.numel() if num_rows is None else num_rows)
+        p.max_context = int(max_context)
+        p.max_q_len = int(max_q_len)
+        p.num_heads, p.head_dim = 4, 128
+        p.index_topk, p.kpool = int(index_topk), int(kpool)
+        p.key_page_size = 64
+        p.block_size = int(block_size)
+        p.block_stride_rows = int(block_size if block_stride_rows is None else block_stride_rows)
+        p.key_page_stride = int(key_page_stride)
+        p.num_key_pages = int(num_key_pages)
+        p.num_kv_blocks = int(num_kv_blocks)
+        p.kpt_ld = int(key_page_table.shape[1])
+        p.bt_ld = int(block_table.shape[1])
+        p.max_key_pages_per_req = int(p.kpt_ld if max_key_pages_per_req is None else max_key_pages_per_req)
+        p.max_blocks_per_req = int(p.bt_ld if max_blocks_per_req is None else max_blocks_per_req)
+        p.q_row_stride = int(q.stride(0))
+        p.segment_rows = int(segment_rows)
+        p.chunk_rows = int(chunk_rows)
+        p.query_start_loc = query_start_loc.data_ptr()
+        p.positions = positions.data_ptr()
+        p.q = q.data_ptr()
+        p.key_cache = key_cache.data_ptr()
+        p.key_page_table = key_page_table.data_ptr()
+        p.block_table = block_table.data_ptr()
+        self.c = p
+
+    @property
+    def num_rows(self):
+        return int(self.c.num_rows)
+
+    def byref(self):
+        return C.byref(self.c)
+
+
+def problem_from_workload(w, device="cuda", **overrides) -> Problem:
+    """Copy a workload (any object with the workload fields) to the device as a Problem."""
+    dev = torch.device(device)
+    kw = dict(
+        query_start_loc=torch.from_numpy(w.qsl).to(dev),
+        positions=torch.from_numpy(w.positions).to(dev),
+        q=torch.from_numpy(w.q).to(dev),
+        key_cache=torch.from_numpy(w.key_cache).to(dev),
+        key_page_table=torch.from_numpy(w.key_page_table).to(dev),
+        block_table=torch.from_numpy(w.block_table).to(dev),
+        index_topk=w.index_topk, kpool=w.kpool, max_context=w.max_context,
+        key_page_stride=w.key_page_stride, num_key_pages=w.num_key_pages,
+        num_kv_blocks=w.num_kv_blocks, block_size=w.block_size,
+        block_stride_rows=w.block_stride_rows, max_key_pages_per_req=w.max_key_pages_per_req,
+        max_blocks_per_req=w.max_blocks_per_req, max_q_len=w.max_q_len, chunk_rows=w.chunk_rows)
+    kw.update(overrides)
+    return Problem(**kw)
+
+
+def sel_workspace_bytes(problem: Problem) -> int:
+    n = int(_lib.sel_workspace_bytes(problem.byref()))
+    if n == 0:
+        raise SelError(SEL_EINVAL, "sel_workspace_bytes")
+    return n
+
+
+def sel_score_workspace_bytes(problem: Problem) -> int:
+    n = int(_lib.sel_score_workspace_bytes(problem.byref()))
+    if n == 0:
+        raise SelError(SEL_EINVAL, "sel_score_workspace_bytes")
+    return n
+
+
+def _workspace(ws, nbytes, device):
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    elif ws.numel() * ws.element_size() < nbytes:
+        raise SelError(SEL_EWORKSPACE, "workspace")
+    return ws
+
+
+def sel_score_paged(problem: Problem, scores, status=None, ws=None, stream=None):
+    """scores: fp32 [num_rows, scores_ld] on the device (row stride = scores.stride(0))."""
+    _dev(scores, torch.float32, "scores")
+    _dev(status, torch.int32, "status")
+    if scores.stride(1) != 1:
+        raise ValueError("scores rows must be contiguous")
+    ws = _workspace(ws, sel_score_workspace_bytes(problem), scores.device)
+    _check(_lib.sel_score_paged(problem.byref(), _ptr(scores), scores.stride(0), _ptr(status), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)), "sel_score_paged")
+    return scores
+
+
+def sel_topk_expand(scores, positions, index_topk, kpool, token_idx, valid_counts=None, status=None,
+                    stream=None):
+    """scores fp32 [rows, ld]; positions int32 [rows]; token_idx int32 [rows, out_width]."""
+    _dev(scores, torch.float32, "scores")
+    _dev(positions, torch.int32, "positions")
+    _dev(token_idx, torch.int32, "token_idx")
+    _dev(valid_counts, torch.int32, "valid_counts")
+    _dev(status, torch.int32, "status")
+    if scores.stride(1) != 1 or not token_idx.is_contiguous():
+        raise ValueError("scores rows and token_idx must be contiguous")
+    rows = int(positions.numel())
+    _check(_lib.sel_topk_expand(_ptr(scores), scores.stride(0), _ptr(positions), rows, int(index_topk),
+                                int(kpool), _ptr(token_idx), int(token_idx.shape[1]), _ptr(valid_counts),
+                                _ptr(status), _stream(stream)), "sel_topk_expand")
+    return token_idx, valid_counts
+
+
+def sel_remap_global(req_id, block_table, token_idx, slots, *, num_kv_blocks, block_size=64,
+                     block_stride_rows=None, max_blocks_per_req=None, valid_counts=None, stream=None):
+    """req_id int32 [rows]; block_table int32 [num_reqs, bt_ld]; token_idx, slots int32 [rows, width]."""
+    for t, n in ((req_id, "req_id"), (block_table, "block_table"), (token_idx, "token_idx"),
+                 (slots, "slots"), (valid_counts, "valid_counts")):
+        _dev(t, torch.int32, n)
+    if not (token_idx.is_contiguous() and slots.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("token_idx, slots and block_table must be contiguous")
+    rows, width = token_idx.shape
+    mb = block_table.shape[1] if max_blocks_per_req is None else max_blocks_per_req
+    stride = block_size if block_stride_rows is None else block_stride_rows
+    _check(_lib.sel_remap_global(_ptr(req_id), int(block_table.shape[0]), _ptr(block_table),
+                                 int(block_table.shape[1]), int(mb), int(num_kv_blocks), _ptr(token_idx),
+                                 int(rows), int(width), int(block_size), int(stride), _ptr(slots),
+                                 _ptr(valid_counts), _stream(stream)), "sel_remap_global")
+    return slots, valid_counts
+
+
+def sel_select(problem: Problem, slots, valid_counts, token_idx=None, status=None, ws=None, stream=None):
+    """slots int32 [num_rows, out_width]; valid_counts int32 [num_rows]."""
+    for t, n in ((slots, "slots"), (valid_counts, "valid_counts"), (token_idx, "token_idx"),
+                 (status, "status")):
+        _dev(t, torch.int32, n)
+    if not slots.is_contiguous() or (token_idx is not None and not token_idx.is_contiguous()):
+        raise ValueError("slots and token_idx must be contiguous")
+    ws = _workspace(ws, sel_workspace_bytes(problem), slots.device)
+    _check(_lib.sel_select(problem.byref(), _ptr(slots), int(slots.shape[1]), _ptr(valid_counts),
+                           _ptr(token_idx), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
+                           _stream(stream)), "sel_select")
+    return slots, valid_counts
+
+
+def sel_host_stage_bytes(problem: Problem, out_width: int) -> int:
+    return int(_lib.sel_host_stage_bytes(problem.byref(), int(out_width)))
+
+
+def sel_select_host(problem: Problem, slots_host, counts_host, stage, ws, status=None, stream=None):
+    """problem's per-step inputs are HOST tensors (pinned); key_cache is on the device."""
+    _dev(stage, torch.uint8, "stage")
+    _dev(ws, torch.uint8, "ws")
+    _check(_lib.sel_select_host(problem.byref(), _ptr(slots_host), int(slots_host.shape[1]),
+                                _ptr(counts_host), _ptr(status), _ptr(stage), stage.numel(), _ptr(ws),
+                                ws.numel(), _stream(stream)), "sel_select_host")
+    return slots_host, counts_host
+
+
+def sel_set_trace_events(events) -> None:
+    """events: four torch.cuda.Event(enable_timing=True), or None to switch tracing off."""
+    if not events:
+        _check(_lib.sel_set_trace_events(None, 0), "sel_set_trace_events")
+        return
+    for e in events:
+        if not e.cuda_event:   # torch creates the CUDA event on its first record
+            e.record()
+    arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(_lib.sel_set_trace_events(arr, len(events)), "sel_set_trace_events")
+
+
+def sel_select_launch_count(problem: Problem) -> int:
+    return int(_lib.sel_select_launch_count(problem.byref()))

@@ -1,0 +1,315 @@
+"""GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Integer-valued workloads and every integer/index step are compared bit for bit;
+normal-valued workloads follow the tolerance rule of the selection (scores within
+1e-4 * sum|q*k| of the oracle, kept sets equal up to swaps of near-tied pools)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _golden import ints, load
+from _gpu import (DEV, TOL, assert_select_bitexact, assert_select_parity, lib, oracle_select, run_scores,
+                  run_select, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------- remap (K-d)
+@pytest.mark.parametrize("rows,width,stride", [(1, 4, 64), (37, 2052, 128), (300, 260, 64), (5, 8, 192)])
+def test_remap_matches_oracle(rows, width, stride):
+    sel = lib()
+    rng = np.random.default_rng(rows * 7 + width)
+    nreq, nb = 6, 40
+    nkv = 300
+    bt = rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)
+    bt[0, 3] = -2
+    bt[1, 5] = nkv + 7
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)   # includes invalid ids
+    tok = workloads.random_token_indices(rows, width, (nb + 2) * 64, seed=rows + width)
+    mb = nb - 1
+    ref_slots, ref_counts = oracle.remap_rows(req, nreq, bt, mb, nkv, tok, 64, stride)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    sel.sel_remap_global(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, block_size=64,
+                         block_stride_rows=stride, max_blocks_per_req=mb, valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
+def test_remap_golden_worked_example():
+    sel = lib()
+    g = load("remap_worked_example.txt")
+    bt = np.stack([ints(g, "block_table_row0"), ints(g, "block_table_row1")]).astype(np.int32)
+    tok = np.stack([ints(g, "tokens_row0"), ints(g, "tokens_row1")]).astype(np.int32)
+    tok = np.concatenate([tok, np.full((2, 3), -1, np.int32)], axis=1)   # width 8 (multiple of 4)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    for key, stride in (("slots", int(g["stride"][0])), ("slots_b", int(g["stride_b"][0]))):
+        slots = torch.empty((2, 8), dtype=torch.int32, device=DEV)
+        counts = torch.empty(2, dtype=torch.int32, device=DEV)
+        sel.sel_remap_global(t(ints(g, "req_id").astype(np.int32)), t(bt), t(tok), slots,
+                             num_kv_blocks=int(g["num_kv_blocks"][0]), block_size=int(g["block_size"][0]),
+                             block_stride_rows=stride, max_blocks_per_req=int(g["max_blocks"][0]),
+                             valid_counts=counts)
+        torch.cuda.synchronize()
+        got = slots.cpu().numpy()
+        np.testing.assert_array_equal(got[0, :5], ints(g, f"{key}_row0"))
+        np.testing.assert_array_equal(got[1, :5], ints(g, f"{key}_row1"))
+        np.testing.assert_array_equal(counts.cpu().numpy(), ints(g, "counts"))
+
+
+# ---------------------------------------------------------------- top-k + expansion (K-c)
+TOPK_CASES = [
+    # (topk, kpool, contexts)                          exercises
+    (256, 4, [1, 7, 255, 256, 257, 258, 259, 1000, 3001]),        # short rows, trailing pools
+    (2048, 4, [2049, 4096, 32765, 32768, 32769]),                 # one CTA per row
+    (2048, 4, [131068, 131069, 131070, 131071, 131072]),         # 4-CTA clusters (128K)
+    (2048, 4, [262144, 200001, 4000, 2000, 0]),                   # 8-CTA clusters, ragged
+    (2048, 4, [400003]),                                          # 8 CTAs x 12.5K keys
+    (60, 3, [59, 60, 61, 62, 1000, 5000]),                        # kpool 3 (scalar stores)
+    (16, 1, [16, 17, 50, 20000]),                                 # kpool 1: a plain top-k
+]
+
+
+@pytest.mark.parametrize("ties", ["none", "coarse", "zeros", "inf"])
+@pytest.mark.parametrize("case", range(len(TOPK_CASES)))
+def test_topk_expand_matches_oracle(case, ties):
+    sel = lib()
+    topk, kpool, ctxs = TOPK_CASES[case]
+    ctx = np.array(ctxs, dtype=np.int64)
+    W = ((topk + kpool - 1) + 3) // 4 * 4
+    ld = max(4, (int(ctx.max()) // kpool + 3) // 4 * 4)
+    scores = workloads.random_scores(len(ctx), ld, seed=100 * case + len(ties), ties=ties)
+    ref_tok, ref_cnt = oracle.topk_expand_rows(scores, ctx, topk, kpool, W)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    tok = torch.full((len(ctx), W), -7, dtype=torch.int32, device=DEV)
+    cnt = torch.full((len(ctx),), -7, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sel.sel_topk_expand(t(scores), t((ctx - 1).astype(np.int32)), topk, kpool, tok, cnt, status=status)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+    assert int(status.item()) == 0
+
+
+def test_topk_rows_beyond_scores_are_out_of_bound():
+    sel = lib()
+    scores = workloads.random_scores(2, 1024, seed=3)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    tok = torch.full((2, 260), -7, dtype=torch.int32, device=DEV)
+    cnt = torch.full((2,), -7, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # ctx 4,101 has 1,025 complete pools: one more than the 1,024 score columns
+    sel.sel_topk_expand(t(scores), t(np.array([4095, 4100], np.int32)), 256, 4, tok, cnt, status=status)
+    torch.cuda.synchronize()
+    got = tok.cpu().numpy()
+    assert (got[1] == -1).all() and int(cnt[1].item()) == 0
+    assert int(status.item()) & 2
+    ref, _ = oracle.topk_expand_rows(scores[:1], np.array([4096]), 256, 4, 260)
+    np.testing.assert_array_equal(got[0], ref[0])
+
+
+# ---------------------------------------------------------------- scorer (K-b)
+@pytest.mark.parametrize("name", ["tiny", "decode32k"])
+def test_scores_integer_exact(name):
+    w = workloads.make_workload(name)
+    gs, st = run_scores(w)
+    os_, _, ost = oracle.score_rows(w, scores_ld=gs.shape[1])
+    assert st == ost == 0
+    for r in range(w.num_rows):
+        P = (int(w.positions[r]) + 1) // w.kpool
+        np.testing.assert_array_equal(gs[r, :P], os_[r, :P])
+
+
+@pytest.mark.parametrize("name", ["decode128k", "ragged", "mixed"])
+def test_scores_normal_within_tolerance(name):
+    w = workloads.make_workload(name)
+    rows = sample_rows(w, per_request=1)
+    gs, st = run_scores(w)
+    os_, ab, _ = oracle.score_rows(w, rows=rows, scores_ld=gs.shape[1])
+    for k, r in enumerate(rows):
+        P = (int(w.positions[r]) + 1) // w.kpool
+        err = np.abs(gs[r, :P].astype(np.float64) - os_[k, :P].astype(np.float64))
+        assert (err <= TOL * ab[k, :P]).all(), (name, r, float((err / np.maximum(ab[k, :P], 1e-30)).max()))
+
+
+# ---------------------------------------------------------------- the fused path
+@pytest.mark.parametrize("name", ["tiny", "decode32k"])
+def test_select_integer_bitexact(name):
+    w = workloads.make_workload(name)
+    out = run_select(w)
+    ref = oracle_select(w)
+    assert out["status"] == ref["status"] == 0
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
+@pytest.mark.parametrize("name", ["decode128k", "ragged", "ragged_b", "mixed"])
+def test_select_normal_parity(name):
+    w = workloads.make_workload(name)
+    out = run_select(w)
+    rows = np.arange(w.num_rows, dtype=np.int32) if w.num_rows <= 64 else sample_rows(w)
+    ref = oracle_select(w, rows=rows, want_scores=True)
+    assert out["status"] == ref["status"]
+    differing = assert_select_parity(w, out, ref, rows)
+    assert differing <= max(1, len(rows) // 4), differing
+    if name == "ragged":
+        # the guarded blocks are -1 in place; counts follow the non -1 slots
+        assert (out["counts"] <= w.index_topk + w.kpool - 1).all()
+
+
+@pytest.mark.parametrize("seg_rows,chunk_rows", [(1, 0), (2, 0), (3, 5), (4, 1), (64, 3), (0, 7)])
+def test_segmentation_invariance(seg_rows, chunk_rows):
+    """Integer mode: outputs do not depend on how rows are cut into segments or chunks."""
+    w = workloads.make_workload("decode32k")
+    ref = oracle_select(w)
+    out = run_select(w, segment_rows=seg_rows, chunk_rows=chunk_rows)
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
+def test_batching_invariance():
+    """A request selected alone or inside a batch gives the same rows."""
+    full = workloads.build_workload([list(range(5000, 5005)), [9000, 9001], [300]], name="b", seed=8,
+                                    integer_mode=True, index_topk=256)
+    out = run_select(full)
+    for i in range(full.num_reqs):
+        lo, hi = int(full.qsl[i]), int(full.qsl[i + 1])
+        ref = oracle_select(full, rows=np.arange(lo, hi, dtype=np.int32))
+        np.testing.assert_array_equal(out["token_idx"][lo:hi], ref["token_idx"])
+        np.testing.assert_array_equal(out["slots"][lo:hi].astype(np.int64), ref["slots"])
+
+
+def test_padding_rows_and_empty_batch():
+    w = workloads.build_workload([[3000], [100, 101]], name="pad", seed=5, integer_mode=True,
+                                 index_topk=256, pad_rows=3)
+    out = run_select(w)
+    ref = oracle_select(w)
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+    assert (out["slots"][3:] == -1).all() and (out["counts"][3:] == 0).all()
+    sel = lib()
+    prob = sel.problem_from_workload(w, DEV, num_rows=0)
+    e = torch.empty((0, w.out_width), dtype=torch.int32, device=DEV)
+    sel.sel_select(prob, e, torch.empty(0, dtype=torch.int32, device=DEV))
+
+
+def test_status_bits_and_guards():
+    w = workloads.build_workload([[3000, 3001], [2500]], name="st", seed=4, integer_mode=True,
+                                 index_topk=256, kpool=4, max_context=3000)
+    w.key_page_table[0, 5] = w.num_key_pages + 3
+    out = run_select(w)
+    ref = oracle_select(w)
+    assert out["status"] == ref["status"] == 3
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+    gs, st = run_scores(w)
+    assert st & 1 and np.isneginf(gs[0, 5 * 64:6 * 64]).all()
+    w.qsl[1] = 5
+    out2 = run_select(w)
+    assert out2["status"] & 8
+    assert (out2["slots"] == -1).all() and (out2["counts"] == 0).all()
+
+
+def test_output_guard_canaries():
+    """Outputs embedded in larger buffers: nothing is written outside them."""
+    sel = lib()
+    w = workloads.make_workload("tiny")
+    prob = sel.problem_from_workload(w, DEV)
+    G = 1024
+    canary = 0x5A5A5A5A
+    n = w.num_rows * w.out_width
+    big = torch.full((n + 2 * G,), canary, dtype=torch.int32, device=DEV)
+    bigc = torch.full((w.num_rows + 2 * G,), canary, dtype=torch.int32, device=DEV)
+    bigt = torch.full((n + 2 * G,), canary, dtype=torch.int32, device=DEV)
+    ws_n = sel.sel_workspace_bytes(prob)
+    ws = torch.full((ws_n + 2 * 4096,), 0x3C, dtype=torch.uint8, device=DEV)
+    slots = big[G:G + n].view(w.num_rows, w.out_width)
+    tok = bigt[G:G + n].view(w.num_rows, w.out_width)
+    sel.sel_select(prob, slots, bigc[G:G + w.num_rows], token_idx=tok, ws=ws[4096:4096 + ws_n])
+    torch.cuda.synchronize()
+    for b in (big, bigc, bigt):
+        h = b.cpu().numpy()
+        assert (h[:G] == canary).all() and (h[-G:] == canary).all()
+    wsh = ws.cpu().numpy()
+    assert (wsh[:4096] == 0x3C).all() and (wsh[-4096:] == 0x3C).all()
+    ref = oracle_select(w)
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref["slots"])
+
+
+def test_graph_replay_after_inplace_changes():
+    """Capture once, change queries, keys, positions and tables in place, replay."""
+    sel = lib()
+    w = workloads.make_workload("decode32k")
+    prob = sel.problem_from_workload(w, DEV)
+    qsl_d, pos_d, q_d, kc_d, kpt_d, bt_d = prob.tensors
+    slots = torch.empty((w.num_rows, w.out_width), dtype=torch.int32, device=DEV)
+    counts = torch.empty(w.num_rows, dtype=torch.int32, device=DEV)
+    tok = torch.empty_like(slots)
+    ws = torch.empty(sel.sel_workspace_bytes(prob), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        sel.sel_select(prob, slots, counts, token_idx=tok, ws=ws)   # warm-up outside capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sel.sel_select(prob, slots, counts, token_idx=tok, ws=ws)
+    rng = np.random.default_rng(99)
+    for step in range(3):
+        w.q[:] = rng.integers(-3, 4, size=w.q.shape).astype(np.float16)
+        kcv = w.key_cache.reshape(w.num_key_pages, 64, 128)
+        live = np.unique(w.key_page_table[w.key_page_table >= 0])
+        kcv[live[: len(live) // 2]] = rng.integers(-3, 4, size=(len(live) // 2, 64, 128)).astype(np.float16)
+        w.positions[:] = w.positions - step   # contexts shrink: 32,766-step ..
+        perm = rng.permutation(w.num_kv_blocks).astype(np.int32)
+        valid = w.block_table >= 0
+        w.block_table[valid] = perm[w.block_table[valid]]
+        q_d.copy_(torch.from_numpy(w.q))
+        kc_d.copy_(torch.from_numpy(w.key_cache))
+        pos_d.copy_(torch.from_numpy(w.positions))
+        bt_d.copy_(torch.from_numpy(w.block_table))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle_select(w)
+        out = dict(slots=slots.cpu().numpy(), counts=counts.cpu().numpy(), token_idx=tok.cpu().numpy())
+        assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
+def test_select_host_path_matches_device():
+    sel = lib()
+    w = workloads.make_workload("tiny")
+    dprob = sel.problem_from_workload(w, DEV)
+    hp = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hprob = sel.Problem(query_start_loc=hp(w.qsl), positions=hp(w.positions), q=hp(w.q),
+                        key_cache=dprob.tensors[3], key_page_table=hp(w.key_page_table),
+                        block_table=hp(w.block_table), index_topk=w.index_topk, kpool=w.kpool,
+                        max_context=w.max_context, key_page_stride=w.key_page_stride,
+                        num_key_pages=w.num_key_pages, num_kv_blocks=w.num_kv_blocks,
+                        block_stride_rows=w.block_stride_rows, max_q_len=w.max_q_len,
+                        host_inputs=True)
+    slots_h = torch.empty((w.num_rows, w.out_width), dtype=torch.int32).pin_memory()
+    counts_h = torch.empty(w.num_rows, dtype=torch.int32).pin_memory()
+    stage = torch.empty(sel.sel_host_stage_bytes(hprob, w.out_width), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(sel.sel_workspace_bytes(dprob), dtype=torch.uint8, device=DEV)
+    sel.sel_select_host(hprob, slots_h, counts_h, stage, ws)
+    torch.cuda.synchronize()
+    ref = oracle_select(w)
+    np.testing.assert_array_equal(slots_h.numpy().astype(np.int64), ref["slots"])
+    np.testing.assert_array_equal(counts_h.numpy(), ref["counts"])
+
+
+def test_trace_events_time_the_kernels():
+    sel = lib()
+    w = workloads.make_workload("decode32k")
+    prob = sel.problem_from_workload(w, DEV)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    slots = torch.empty((w.num_rows, w.out_width), dtype=torch.int32, device=DEV)
+    counts = torch.empty(w.num_rows, dtype=torch.int32, device=DEV)
+    sel.sel_set_trace_events(ev)
+    try:
+        sel.sel_select(prob, slots, counts)
+    finally:
+        sel.sel_set_trace_events(None)
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
+    assert sel.sel_select_launch_count(prob) == 3
