@@ -206,12 +206,14 @@ int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width
                     void *ws, size_t ws_bytes, sel_stream_t stream);
 
 /*
- * Tracing hook. With n >= 4 events (cudaEvent_t handles, created by the caller with
+ * Tracing hook. With n >= 6 events (cudaEvent_t handles, created by the caller with
  * timing enabled), every following sel_select records, on `stream`: events[0] before its
  * first segment-builder launch, events[1] after that builder (before the first scorer
- * launch), events[2] after the last scorer launch and events[3] after the last top-k
- * launch. Inside stream capture the records become external event nodes. n == 0
- * switches tracing off. Calls to sel_select are serialised while tracing state is read.
+ * launch), events[2] after the last scorer launch, events[3] after the last row-histogram
+ * launch, events[4] after the last candidate-collect launch and events[5] after the last
+ * finalize (exact select, expansion, remap) launch. Inside stream capture the records
+ * become external event nodes. n == 0 switches tracing off. Calls to sel_select are
+ * serialised while tracing state is read.
  */
 int sel_set_trace_events(void *const *events, int32_t n);
 

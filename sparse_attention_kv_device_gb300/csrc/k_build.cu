@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
             h[i] = make_uint4(0, 0, 0, 0);
         return;
     }
-    if (tid == 0) SEL_PHASE(0);
+    if (tid == 0) { SEL_PHASE(0); SEL_PHASE_CLK(32); }
     const int nchunk = a.row_end - a.row_begin;
 
     // shared-memory staging (host decided what fits); generic pointers either way
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
     for (int i = tid; i < a.num_reqs; i += blockDim.x) bad |= qsl[i] > qsl[i + 1];
     if (tid == 0) bad |= (qsl[0] < 0) | (qsl[a.num_reqs] > a.num_rows);
     bad = __syncthreads_or(bad);
-    if (tid == 0) SEL_PHASE(1);
+    if (tid == 0) { SEL_PHASE(1); SEL_PHASE_CLK(33); }
     if (bad) {
         for (int r = tid; r < nchunk; r += blockDim.x) {
             a.row_req[r] = -1;
@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
             report(a.status, kStBadQsl);
             a.hdr[0] = 0;
             a.hdr[1] = 0;
+            a.hdr[2] = 0;
             a.seg_tile_prefix[0] = 0;
         }
         return;
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
         if (a.smem_rows) a.row_ctx[k] = c;
     }
     __syncthreads();
-    if (tid == 0) SEL_PHASE(2);
+    if (tid == 0) { SEL_PHASE(2); SEL_PHASE_CLK(34); }
 
     // 3. segments: request i's rows inside the chunk, cut every seg_rows rows.
     uint32_t carry = 0;
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
         __syncthreads();
     }
     const int nseg = min(static_cast<int>(carry), a.max_segs);
-    if (tid == 0) SEL_PHASE(3);
+    if (tid == 0) { SEL_PHASE(3); SEL_PHASE_CLK(35); }
 
     // 4. tiles of 128 pools per segment, exclusive prefix.
     uint32_t tcarry = 0;
@@ -171,7 +172,9 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
         if (a.smem_segs) a.seg_tile_prefix[nseg] = static_cast<int32_t>(tcarry);
         a.hdr[0] = nseg;
         a.hdr[1] = ntiles;
+        a.hdr[2] = 0;
         SEL_PHASE(4);
+        SEL_PHASE_CLK(36);
     }
     __syncthreads();
 
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
     }
 #ifdef SEL_PHASE_TRACE
     __syncthreads();
-    if (tid == 0) SEL_PHASE(5);
+    if (tid == 0) { SEL_PHASE(5); SEL_PHASE_CLK(37); }
 #endif
 }
 

@@ -26,19 +26,22 @@ SEL_PHASE_TABLE(score)
 
 namespace {
 
-constexpr int kRecBatch = 128;  // tile records staged in shared memory per producer batch
+constexpr int kSchedRing = 16;  // tiles published ahead by the producer (> stages + accumulators + 2)
 
 struct ScoreSmem {
-    uint8_t* a;        // stages x kTileBytes (keys)
-    uint8_t* q;        // 2 x npad_max x 256 B (queries, two K halves each)
-    int4* rec;         // [kRecBatch] tile records of the producer's current batch
-    uint64_t* full;    // [stages]
-    uint64_t* empty;   // [stages]
-    uint64_t* tfull;   // [2]
-    uint64_t* tempty;  // [2]
-    uint64_t* qfull;   // [2]
-    uint64_t* qempty;  // [2]
-    uint64_t* done;    // [1]
+    uint8_t* a;          // stages x kTileBytes (keys)
+    uint8_t* q;          // 2 x npad_max x 256 B (queries, two K halves each)
+    int4* rec_ring;      // [kSchedRing] tile records in the order this CTA processes them
+    int* tile_ring;      // [kSchedRing] tile ids (-1: no more tiles)
+    uint64_t* full;      // [stages]
+    uint64_t* empty;     // [stages]
+    uint64_t* tfull;     // [2]
+    uint64_t* tempty;    // [2]
+    uint64_t* qfull;     // [2]
+    uint64_t* qempty;    // [2]
+    uint64_t* sfull;     // [kSchedRing] schedule slot published
+    uint64_t* sempty;    // [kSchedRing] schedule slot read by the MMA thread and the 4 epilogue warps
+    uint64_t* done;      // [1]
     uint32_t* tmem_base;
     int* abort_flag;
     int* oob_flag;
@@ -52,8 +55,10 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
     p += static_cast<size_t>(stages) * kTileBytes;
     s.q = p;
     p += 2u * static_cast<size_t>(npad_max) * 256u;
-    s.rec = reinterpret_cast<int4*>(p);
-    p += kRecBatch * sizeof(int4);
+    s.rec_ring = reinterpret_cast<int4*>(p);
+    p += kSchedRing * sizeof(int4);
+    s.tile_ring = reinterpret_cast<int*>(p);
+    p += kSchedRing * sizeof(int);
     uint64_t* b = reinterpret_cast<uint64_t*>(p);
     s.full = b;
     s.empty = b + stages;
@@ -61,7 +66,9 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
     s.tempty = s.tfull + 2;
     s.qfull = s.tempty + 2;
     s.qempty = s.qfull + 2;
-    s.done = s.qempty + 2;
+    s.sfull = s.qempty + 2;
+    s.sempty = s.sfull + kSchedRing;
+    s.done = s.sempty + kSchedRing;
     uint32_t* w = reinterpret_cast<uint32_t*>(s.done + 1);
     s.tmem_base = w;
     s.abort_flag = reinterpret_cast<int*>(w + 1);
@@ -77,6 +84,9 @@ __device__ __forceinline__ int row_pool_limit(const ScoreArgs& a, int row) {
 
 }  // namespace
 
+// Tile schedule: CTA g first takes the contiguous static share [g*S, g*S + S) with
+// S = floor(3/4 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
+// atomic counter, so CTAs that stream faster take more of the tail.
 __global__ void __launch_bounds__(kScoreThreads, 1)
     k_score_segments(const ScoreArgs a, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_q) {
@@ -84,8 +94,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ScoreSmem sm = carve(smem_raw, a.stages, a.npad_max);
     const uint32_t qhalf_bytes = static_cast<uint32_t>(a.npad_max) * 128u;
-    // diagnostics: CTA 0 and CTA gridDim/2 stamp their phases (slot bases 0 and 256)
-    const int trace_base = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x / 2 ? 256 : -1);
+    // diagnostics: CTA 0 and CTA gridDim/2 stamp their phases (slot bases 0 and 150)
+    const int trace_base = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x / 2 ? 150 : -1);
     (void)trace_base;
     if (trace_base >= 0 && threadIdx.x == 0) SEL_PHASE(trace_base + 0);
 
@@ -100,6 +110,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             mbar_init(&sm.tempty[i], 4 * 32);
             mbar_init(&sm.qfull[i], 1);
             mbar_init(&sm.qempty[i], 1);
+        }
+        for (int i = 0; i < kSchedRing; ++i) {
+            mbar_init(&sm.sfull[i], 1);
+            mbar_init(&sm.sempty[i], 1 + 4);
         }
         mbar_init(sm.done, 1);
         *sm.abort_flag = 0;
@@ -125,65 +139,86 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     pdl_launch_dependents();  // the top-k grid may be scheduled as CTAs retire
     if (trace_base >= 0 && threadIdx.x == 0) SEL_PHASE(trace_base + 2);
 
-    const int total = a.hdr[1];
-    const int t0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
-    const int t1 = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    if (warp == 0) {
+        // ------------------------------------------------------------ scheduler + TMA producer
+        if (lane == 0) {
+            const int total = a.hdr[1];
+            const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
+            const int dyn0 = share * static_cast<int>(gridDim.x);
+            int s_next = static_cast<int>(blockIdx.x) * share;
+            const int s_end = s_next + share;
+            auto grab = [&]() -> int {
+                if (s_next < s_end) return s_next++;
+                const int t = dyn0 + atomicAdd(a.hdr + 2, 1);
+                return t < total ? t : -1;
+            };
+            // two tiles ahead: their ids and records are in flight while the current one is issued
+            int t_a = grab();
+            int4 r_a = t_a >= 0 ? a.tiles[t_a] : make_int4(0, 0, 0, 0);
+            int t_b = t_a >= 0 ? grab() : -1;
+            int4 r_b = t_b >= 0 ? a.tiles[t_b] : make_int4(0, 0, 0, 0);
 
-    if (t0 < t1 && warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        const uint64_t pol_k = l2_policy_evict_first();
-        const uint64_t pol_q = l2_policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        int qb = 1, cur = -1;
-        int q_uses0 = 0, q_uses1 = 0;          // segments loaded into query buffer 0 / 1
-        uint32_t qe_phase = 0;                 // bit b: parity to wait on query buffer b's release
-        uint32_t loaded = 0, last_parity = 0;  // stages holding a load, parity of their last load
-        bool ok = true;
-        for (int tb = t0; tb < t1 && ok; tb += kRecBatch) {
-            const int te = min(t1, tb + kRecBatch);
-            for (int t = tb + lane; t < te; t += 32) sm.rec[t - tb] = a.tiles[t];
-            __syncwarp();
-            if (lane == 0) {
-                for (int t = tb; t < te && ok; ++t) {
-                    const int4 rec = sm.rec[t - tb];
-                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-                    const int npages = rec.w == -2 ? 1 : 2;
-                    mbar_expect_tx(&sm.full[stage], static_cast<uint32_t>(npages) * kPageBytes);
-                    uint8_t* adst = sm.a + static_cast<size_t>(stage) * kTileBytes;
-                    loaded |= 1u << stage;
-                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                    for (int h = 0; h < npages; ++h) {
-                        const int pg = max(h == 0 ? rec.z : rec.w, 0);  // out-of-range pages: the epilogue writes -inf
-                        tma_load_3d(adst + h * kBoxBytes, &tmap_k, &sm.full[stage], 0, 0, pg, pol_k);
-                        tma_load_3d(adst + kPageBytes + h * kBoxBytes, &tmap_k, &sm.full[stage], 64, 0, pg, pol_k);
+            const uint64_t pol_k = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            int qb = 1, cur = -1;
+            int q_uses0 = 0, q_uses1 = 0;          // segments loaded into query buffer 0 / 1
+            uint32_t qe_phase = 0;                 // bit b: parity to wait on query buffer b's release
+            uint32_t loaded = 0, last_parity = 0;  // stages holding a load, parity of their last load
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int t = t_a;
+                const int4 rec = r_a;
+                t_a = t_b;
+                r_a = r_b;
+                if (t_a >= 0) {
+                    t_b = grab();
+                    if (t_b >= 0) r_b = a.tiles[t_b];
+                } else {
+                    t_b = -1;
+                }
+                // publish the tile (or the end) to the MMA thread and the epilogue warps
+                const int slot = n & (kSchedRing - 1);
+                if (!mbar_wait(&sm.sempty[slot], ((n / kSchedRing) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                sm.tile_ring[slot] = t;
+                sm.rec_ring[slot] = rec;
+                mbar_arrive(&sm.sfull[slot]);
+                if (t < 0) break;
+
+                if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                const int npages = rec.w == -2 ? 1 : 2;
+                mbar_expect_tx(&sm.full[stage], static_cast<uint32_t>(npages) * kPageBytes);
+                uint8_t* adst = sm.a + static_cast<size_t>(stage) * kTileBytes;
+                loaded |= 1u << stage;
+                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                for (int h = 0; h < npages; ++h) {
+                    const int pg = max(h == 0 ? rec.z : rec.w, 0);  // out-of-range pages: the epilogue writes -inf
+                    tma_load_3d(adst + h * kBoxBytes, &tmap_k, &sm.full[stage], 0, 0, pg, pol_k);
+                    tma_load_3d(adst + kPageBytes + h * kBoxBytes, &tmap_k, &sm.full[stage], 64, 0, pg, pol_k);
+                }
+                if (trace_base >= 0 && n == 0) SEL_PHASE(trace_base + 3);
+                if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                if (rec.x != cur) {
+                    // the segment's queries, after its first key tile is on its way
+                    const int4 sd = a.seg[rec.x];
+                    qb ^= 1;
+                    if ((qb ? q_uses1 : q_uses0) > 0) {
+                        if (!mbar_wait(&sm.qempty[qb], (qe_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
+                        qe_phase ^= 1u << qb;
                     }
-                    if (trace_base >= 0 && t == t0) SEL_PHASE(trace_base + 3);
-                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
-                    if (rec.x != cur) {
-                        // the segment's queries, after its first key tile is on its way
-                        const int4 sd = a.seg[rec.x];
-                        qb ^= 1;
-                        if ((qb ? q_uses1 : q_uses0) > 0) {
-                            if (!mbar_wait(&sm.qempty[qb], (qe_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
-                            qe_phase ^= 1u << qb;
-                        }
-                        if (qb) ++q_uses1; else ++q_uses0;
-                        const int nbox = (sd.z + 3) / 4;
-                        mbar_expect_tx(&sm.qfull[qb], static_cast<uint32_t>(nbox) * 2u * kQBoxBytes);
-                        uint8_t* qdst = sm.q + qb * 2 * qhalf_bytes;
-                        for (int i = 0; i < nbox; ++i) {
-                            tma_load_3d(qdst + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 0, 0, sd.y + 4 * i, pol_q);
-                            tma_load_3d(qdst + qhalf_bytes + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 64, 0,
-                                        sd.y + 4 * i, pol_q);
-                        }
-                        cur = rec.x;
+                    if (qb) ++q_uses1; else ++q_uses0;
+                    const int nbox = (sd.z + 3) / 4;
+                    mbar_expect_tx(&sm.qfull[qb], static_cast<uint32_t>(nbox) * 2u * kQBoxBytes);
+                    uint8_t* qdst = sm.q + qb * 2 * qhalf_bytes;
+                    for (int i = 0; i < nbox; ++i) {
+                        tma_load_3d(qdst + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 0, 0, sd.y + 4 * i, pol_q);
+                        tma_load_3d(qdst + qhalf_bytes + i * kQBoxBytes, &tmap_q, &sm.qfull[qb], 64, 0,
+                                    sd.y + 4 * i, pol_q);
                     }
+                    cur = rec.x;
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        }
-        if (lane == 0) {
             if (ok) {
                 // drain: every stage's last load consumed, every query buffer released
                 for (int i = 0; i < a.stages && ok; ++i) {
@@ -203,7 +238,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (q_uses1 > 0) mbar_wait(&sm.qfull[1], static_cast<uint32_t>(q_uses1 - 1) & 1u, nullptr);
             }
         }
-    } else if (t0 < t1 && warp == 1) {
+    } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int stage = 0, acc = 0;
@@ -213,12 +248,17 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             uint32_t idesc = 0;
             const uint32_t a_base = smem_u32(sm.a);
             const uint32_t q_base = smem_u32(sm.q);
-            int4 next = a.tiles[t0];
             bool ok = true;
-            for (int t = t0; t < t1 && ok; ++t) {
-                const int4 rec = next;
-                if (t + 1 < t1) next = a.tiles[t + 1];  // in flight while this tile waits
+            for (int n = 0; ok; ++n) {
+                const int slot = n & (kSchedRing - 1);
+                if (!mbar_wait(&sm.sfull[slot], (n / kSchedRing) & 1, abort_flag)) { ok = false; break; }
+                const int t = sm.tile_ring[slot];
+                const int4 rec = sm.rec_ring[slot];
+                mbar_arrive(&sm.sempty[slot]);
+                if (t < 0) break;
                 if (rec.x != cur) {
+                    // the previous segment's queries are free once its MMAs complete
+                    if (cur >= 0) umma_commit(&sm.qempty[qb]);
                     const int4 sd = a.seg[rec.x];
                     qb ^= 1;
                     if (!mbar_wait(&sm.qfull[qb], (qf_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
@@ -228,7 +268,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     cur = rec.x;
                 }
                 if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
-                if (trace_base >= 0 && t - t0 < 48) SEL_PHASE(trace_base + 8 + (t - t0));
+                if (trace_base >= 0 && n < 60) SEL_PHASE(trace_base + 8 + n);
                 if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc) * a.acc_cols;
@@ -243,11 +283,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 }
                 umma_commit(&sm.empty[stage]);
                 umma_commit(&sm.tfull[acc]);
-                if (t + 1 == t1 || next.x != rec.x) umma_commit(&sm.qempty[qb]);
                 if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            if (ok && cur >= 0) umma_commit(&sm.qempty[qb]);  // the last segment's buffer
             if (!ok) {
                 *abort_flag = 1;
                 report(a.status, kStTimeout);
@@ -256,7 +296,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             umma_commit(sm.done);
             mbar_wait(sm.done, 0, nullptr);
         }
-    } else if (t0 < t1) {
+    } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         // Warp-local only: each warp waits on its own, holds the segment's per-row
         // pool limits in its lanes, and never waits for the other epilogue warps.
@@ -267,17 +307,29 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         int4 sd = make_int4(0, 0, 0, 0);
         int lim_lo = 0, lim_hi = 0;               // pools row `lane` / `lane + 32` may score
         int oob = 0;
-        int4 next = a.tiles[t0];
-        for (int t = t0; t < t1; ++t) {
-            const int4 rec = next;
-            if (t + 1 < t1) next = a.tiles[t + 1];
+        for (int n = 0;; ++n) {
+            const int slot = n & (kSchedRing - 1);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&sm.sfull[slot], (n / kSchedRing) & 1, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report(a.status, kStTimeout);
+                }
+                break;
+            }
+            const int t = sm.tile_ring[slot];
+            const int4 rec = sm.rec_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sempty[slot]);
+            if (t < 0) break;
             if (rec.x != cur) {
                 sd = a.seg[rec.x];
                 lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
                 lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
                 cur = rec.x;
             }
-            int ok = 1;
             if (lane == 0) ok = mbar_wait(&sm.tfull[acc], acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
@@ -289,7 +341,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             }
             __syncwarp();
             tc_fence_after();
-            if (trace_base >= 0 && warp == 2 && lane == 0 && t - t0 < 48) SEL_PHASE(trace_base + 64 + (t - t0));
+            if (trace_base >= 0 && warp == 2 && lane == 0 && n < 60) SEL_PHASE(trace_base + 70 + n);
             const int p_in_tile = quarter * 32 + lane;
             const int j = rec.y * kTilePools + p_in_tile;
             const bool page_ok = (p_in_tile < kPagePools ? rec.z : rec.w) >= 0;
@@ -307,25 +359,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     const int r = rg * 8 + rr;
                     if (r >= sd.z) break;  // uniform over the warp
                     const int lim = __shfl_sync(0xffffffffu, r < 32 ? lim_lo : lim_hi, r & 31);
-                    const bool ok = j < lim;
+                    const bool okp = j < lim;
                     const float h0 = __uint_as_float(v[4 * rr + 0]);
                     const float h1 = __uint_as_float(v[4 * rr + 1]);
                     const float h2 = __uint_as_float(v[4 * rr + 2]);
                     const float h3 = __uint_as_float(v[4 * rr + 3]);
                     const float sc = page_ok ? ((h0 + h1) + h2) + h3 : -__int_as_float(0x7f800000);
-                    if (ok) out[static_cast<int64_t>(r) * a.scores_ld] = sc;
-                    if (a.hist) {
-                        // level-1 histogram of the row (top 11 key bits), one add per distinct bin of the warp
-                        const uint32_t bin = ok ? (ordered_key(sc) >> 21) : 0xffffffffu;
-                        const uint32_t same = __match_any_sync(0xffffffffu, bin);
-                        if (ok && lane == __ffs(same) - 1)
-                            atomicAdd(a.hist + static_cast<int64_t>(sd.y - a.row_begin + r) * kTopkBins + bin,
-                                      static_cast<uint32_t>(__popc(same)));
-                    }
+                    if (okp) out[static_cast<int64_t>(r) * a.scores_ld] = sc;
                 }
             }
             tc_fence_before();
-            if (trace_base >= 0 && warp == 2 && lane == 0 && t - t0 < 48) SEL_PHASE(trace_base + 128 + (t - t0));
             mbar_arrive(&sm.tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
@@ -341,16 +384,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         tmem_dealloc(tmem, a.tmem_cols);
     }
     if (threadIdx.x == 0 && *sm.oob_flag) report(a.status, kStKeyPageOob);
-    if (trace_base >= 0 && threadIdx.x == 0) {
-        SEL_PHASE(trace_base + 200);
-        SEL_PHASE_VALUE(trace_base + 201, t1 - t0);
-    }
     if (threadIdx.x == 0 && blockIdx.x < 200) SEL_PHASE(300 + blockIdx.x);  // every CTA's end
 }
 
 size_t score_smem_bytes(int stages, int npad_max) {
     return 1024 + static_cast<size_t>(stages) * kTileBytes + 2u * static_cast<size_t>(npad_max) * 256u +
-           kRecBatch * sizeof(int4) + 512;
+           kSchedRing * (sizeof(int4) + sizeof(int)) + (2 * static_cast<size_t>(stages) + 9 + 2 * kSchedRing) * 8 + 64;
 }
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,

@@ -10,27 +10,22 @@
 // block_table[req, t / block_size] * block_stride_rows + t % block_size (-1 guarded), and
 // the valid count is the number of non -1 slots, reduced on chip without atomics.
 //
-// GB300 design: one thread-block cluster (1..8 CTAs) per row. Each CTA takes an even
-// slice of the row; thread t of a CTA owns a contiguous run of the slice, staged once
-// as order-preserving 32-bit keys in shared memory in a transposed layout (key i of
-// thread t at i * threads + t, so every pass is bank-conflict free) together with the
-// block-table entries the slice's tokens need. A first radix level over the top 11
-// key bits finds the bin b1 holding the K-th largest key: each CTA builds a local
-// histogram, the owner of every bin range sums it across the cluster through
-// distributed shared memory and pushes the totals to all CTAs, and every CTA scans
-// them. The keys of bin b1 (a few hundred for real scores) are then gathered from all
-// CTAs in index order and every CTA finishes the select on that small set alone (two
-// local radix levels over the remaining 21 bits). When the bin is too crowded
-// (massive ties), the two levels run cluster-wide instead. Keys equal to the threshold
-// are kept lowest index first across the cluster. The kept pools are placed by one
-// block scan over the per-thread counts, so each pass over the slice costs a few
-// instructions per key.
-#include <cooperative_groups.h>
-
+// GB300 design: one 1024-thread CTA per row; no cluster, no distributed shared memory.
+// Thread t owns a contiguous run of the row's pools and holds up to 32 of their
+// order-preserving 32-bit keys in registers at a time. An exact three-level radix
+// select (11 + 11 + 10 key bits) finds the K-th largest key:
+//   level 1: the bin b1 holding it, from the row's histogram of the top 11 bits (made by
+//            the histogram kernel, or counted here when there is none);
+//   list:    the row's keys with bin >= b1 (the keys above the threshold bin and the
+//            threshold bin itself: about K plus a few hundred for real scores) are
+//            compacted, in index order, into a shared-memory list by one block scan;
+//   levels 2, 3: on the list's bin-b1 keys only.
+// The kept pools are then the list entries above the threshold plus the first equal ones;
+// one packed block scan over the list gives each its output column. The block-table row
+// is staged in shared memory while the keys load. A crowded threshold bin (massive ties,
+// list overflow) takes a slower path that re-reads the row for levels 2, 3 and output.
 #include "sel_device.cuh"
 #include "sel_kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace sel {
 
@@ -38,48 +33,47 @@ SEL_PHASE_TABLE(topk)
 
 namespace {
 
+constexpr int T = kTopkThreads;
+constexpr int kChunk = 32;  // keys a thread holds in registers at a time
+
 struct TopkSmem {
-    uint32_t* keys;     // [slice_cap] key i of thread t at i * kTopkThreads + t
-    uint32_t* hist;     // [kTopkBins] local histogram
-    uint32_t* tot;      // [kTopkBins] cluster totals
-    uint2* cand;        // [kTopkCandCap] this CTA's keys of bin b1: (key, pool index), index order
-    uint2* merged;      // [kTopkCandCap] every CTA's candidates, index order
-    int32_t* btab;      // [bt_cap] block-table entries covering this CTA's tokens
+    uint32_t* cnt;      // [T] per (key slot, warp) counts of a chunk, then their prefix
+    uint32_t* hist;     // [kTopkBins]
+    uint2* list;        // [kTopkListCap] (key, pool) with bin >= b1, index order
+    int32_t* btab;      // [bt_cap] the row's block-table entries
     uint32_t* scratch;  // [64]
-    uint32_t* xch;      // [32]: 0..7 candidates, 8..15 keys above b1, 16..23 valid slots (per CTA)
-    uint32_t* cnt;      // [32]: 0..7 keys > thr, 8..15 keys == thr, 16..23 candidates, 24..31 above b1
     uint32_t* res;      // [8]
 };
 
-__device__ __forceinline__ TopkSmem carve(uint32_t* base, int slice_cap, int bt_cap) {
+__device__ __forceinline__ TopkSmem carve(uint32_t* base, int bt_cap) {
     TopkSmem s;
-    s.keys = base;
-    s.hist = base + slice_cap;
-    s.tot = s.hist + kTopkBins;
-    s.cand = reinterpret_cast<uint2*>(s.tot + kTopkBins);
-    s.merged = s.cand + kTopkCandCap;
-    s.btab = reinterpret_cast<int32_t*>(s.merged + kTopkCandCap);
+    s.cnt = base;
+    s.hist = base + T;
+    s.list = reinterpret_cast<uint2*>(s.hist + kTopkBins);
+    s.btab = reinterpret_cast<int32_t*>(s.list + kTopkListCap);
     s.scratch = reinterpret_cast<uint32_t*>(s.btab + ((bt_cap + 3) & ~3));
-    s.xch = s.scratch + 64;
-    s.cnt = s.xch + 32;
-    s.res = s.cnt + 32;
+    s.res = s.scratch + 64;
     return s;
 }
 
-// Local: the bin (of `nbins`, counted from the top) that holds the Kc-th largest key
-// counted in `hist`, and Kc minus the keys in the bins above it.
+// The bin (of `nbins`, counted from the top) that holds the Kc-th largest key counted in
+// `hist`, and Kc minus the keys in the bins above it.
 __device__ __forceinline__ void block_find_bin(const uint32_t* hist, const TopkSmem& sm, int nbins, uint32_t Kc,
                                                uint32_t& bin, uint32_t& krem) {
     const int tid = threadIdx.x;
-    const int per = nbins / kTopkThreads;
+    const int per = (nbins + T - 1) / T;
     uint32_t local = 0;
-    for (int i = 0; i < per; ++i) local += hist[nbins - 1 - (tid * per + i)];
+    for (int i = 0; i < per; ++i) {
+        const int b = nbins - 1 - (tid * per + i);
+        if (b >= 0) local += hist[b];
+    }
     uint32_t total;
     const uint32_t above = block_excl_scan(local, sm.scratch, &total);
     if (above < Kc && Kc <= above + local) {
         uint32_t acc = above;
         for (int i = 0; i < per; ++i) {
             const int b = nbins - 1 - (tid * per + i);
+            if (b < 0) break;
             if (acc + hist[b] >= Kc) {
                 sm.res[0] = static_cast<uint32_t>(b);
                 sm.res[1] = Kc - acc;
@@ -93,34 +87,9 @@ __device__ __forceinline__ void block_find_bin(const uint32_t* hist, const TopkS
     krem = sm.res[1];
 }
 
-// Cluster-wide: sums every CTA's local histogram into `tot` (each CTA owns a bin
-// range, adds it over the cluster and pushes the totals to every CTA), then finds the
-// bin of the Kc-th largest key locally.
-__device__ __forceinline__ void cluster_find_bin(cg::cluster_group& cluster, uint32_t C, uint32_t crank,
-                                                 const TopkSmem& sm, int nbins, uint32_t Kc, uint32_t& bin,
-                                                 uint32_t& krem) {
-    cluster.sync();  // every local histogram is complete
-    const int lo = static_cast<int>(crank) * nbins / static_cast<int>(C);
-    const int hi = static_cast<int>(crank + 1) * nbins / static_cast<int>(C);
-    for (int b = lo + static_cast<int>(threadIdx.x); b < hi; b += blockDim.x) {
-        uint32_t v[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) v[c] = c < static_cast<int>(C) ? cluster.map_shared_rank(sm.hist, c)[b] : 0u;
-        uint32_t s = 0;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) s += v[c];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            if (c < static_cast<int>(C)) cluster.map_shared_rank(sm.tot, c)[b] = s;
-    }
-    cluster.sync();  // every CTA holds the totals of all bins
-    block_find_bin(sm.tot, sm, nbins, Kc, bin, krem);
-}
-
 struct RowMap {  // how a token reaches its slot
     const int32_t* bt_row;  // global block-table row
-    const int32_t* btab;    // shared-memory copy of entries [blk0, blk0 + nblk), or null
-    int64_t blk0;
+    const int32_t* btab;    // shared-memory copy of entries [0, nblk), or null
     int32_t nblk;
 };
 
@@ -128,8 +97,8 @@ __device__ __forceinline__ int32_t slot_of(const TopkArgs& a, const RowMap& m, i
     if (t < 0) return -1;
     const int32_t b = t / a.block_size;
     int32_t ph;
-    if (m.btab && b >= m.blk0 && b < m.blk0 + m.nblk) {
-        ph = m.btab[b - m.blk0];  // entries past max_blocks were stored as -1
+    if (m.btab && b < m.nblk) {
+        ph = m.btab[b];  // entries past max_blocks were stored as -1
     } else {
         if (b >= a.max_blocks) return -1;
         ph = __ldg(m.bt_row + b);
@@ -189,29 +158,45 @@ __device__ __forceinline__ uint32_t emit_run(const TopkArgs& a, const RowMap& m,
     return valid;
 }
 
+// Chunk c of a row is pools [c*kChunkPools, (c+1)*kChunkPools); its key i held by thread
+// tid is pool c*kChunkPools + i*T + tid, so every warp load reads one contiguous 128-byte
+// line. Keys are loaded first, then converted in place to order-preserving keys; pools
+// past P become 0, below every real key.
+constexpr int kChunkPools = T * kChunk;
+
+__device__ __forceinline__ void load_chunk(const float* row, int64_t c, int64_t P, uint32_t (&k)[kChunk]) {
+    const int64_t base = c * kChunkPools + threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+        k[i] = base + static_cast<int64_t>(i) * T < P ? __float_as_uint(__ldcg(row + base + static_cast<int64_t>(i) * T)) : 0u;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+        k[i] = base + static_cast<int64_t>(i) * T < P ? ordered_key(__uint_as_float(k[i])) : 0u;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    return (1u << (threadIdx.x & 31)) - 1u;
+}
+
 }  // namespace
 
 template <bool REMAP>
-__global__ void __launch_bounds__(kTopkThreads, 2) k_topk_expand(const TopkArgs a) {
+__global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs a) {
     extern __shared__ __align__(16) uint32_t tk_smem[];
-    cg::cluster_group cluster = cg::this_cluster();
-    const uint32_t C = cluster.num_blocks();
-    const uint32_t crank = cluster.block_rank();
     const int tid = threadIdx.x;
-    constexpr int T = kTopkThreads;
-    const int rl = blockIdx.y;
+    const int rl = blockIdx.x;
     const int r = a.row_begin + rl;
-    TopkSmem sm = carve(tk_smem, a.slice_cap, a.bt_cap);
-    // diagnostics: CTA rank 0 of rows 0 and gridDim.y/2 stamp their phases (bases 0, 256)
-    const int tb = crank != 0 ? -1 : (rl == 0 ? 0 : (rl == static_cast<int>(gridDim.y) / 2 ? 256 : -1));
+    TopkSmem sm = carve(tk_smem, a.bt_cap);
+    // diagnostics: rows 0 and gridDim.x/2 stamp their phases (bases 0, 256)
+    const int tb = rl == 0 ? 0 : (rl == static_cast<int>(gridDim.x) / 2 ? 256 : -1);
     (void)tb;
-#define TK_PHASE(i) do { if (tb >= 0 && tid == 0) SEL_PHASE(tb + (i)); } while (0)
+#define TK_PHASE(i) do { if (tb >= 0 && tid == 0) { SEL_PHASE(tb + (i)); SEL_PHASE_CLK(tb + 32 + (i)); } } while (0)
     TK_PHASE(0);
 
-    pdl_wait();  // scores and row descriptors come from the preceding kernels
+    pdl_wait();  // scores, row descriptors and histograms come from the preceding kernels
     TK_PHASE(1);
 
-    // ---- the row: context, request, mode (identical in every CTA of the cluster)
+    // ---- the row: context, request, mode
     bool valid = true;
     int64_t ctx;
     if (a.row_ctx) {
@@ -226,26 +211,21 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k_topk_expand(const TopkArgs 
         req = a.row_req[rl];
         valid = valid && req >= 0;
     }
-    int64_t P = 0;
     const int K = a.topk / a.kpool;
-    int64_t L = 0;
-    int R = 0;  // keys per thread (multiple of 4)
+    int64_t P = 0;
     if (valid && ctx > a.topk) {
         P = ctx / a.kpool;
-        L = ((P + C - 1) / C + 3) & ~int64_t(3);
-        R = static_cast<int>(((L + T - 1) / T + 3) & ~int64_t(3));
-        if (P > a.max_pools || static_cast<int64_t>(R) * T > a.slice_cap) {
+        if (P > a.max_pools) {
             valid = false;
-            if (crank == 0 && tid == 0) report(a.status, kStCtxOverBound);
+            if (tid == 0) report(a.status, kStCtxOverBound);
         }
     }
     int32_t* tok_row = a.token_idx ? a.token_idx + static_cast<int64_t>(r) * a.out_width : nullptr;
     int32_t* slot_row = REMAP ? a.slots + static_cast<int64_t>(r) * a.out_width : nullptr;
-    RowMap map{(REMAP && valid) ? a.block_table + static_cast<int64_t>(req) * a.bt_ld : nullptr, nullptr, 0, 0};
+    RowMap map{(REMAP && valid) ? a.block_table + static_cast<int64_t>(req) * a.bt_ld : nullptr, nullptr, 0};
 
     if (!valid || ctx <= a.topk) {
-        // every token of a short row, or nothing: no selection, the first CTA writes the row
-        if (crank != 0) return;
+        // every token of a short row, or nothing: no selection
         const int64_t n = valid && ctx > 0 ? ctx : 0;
         const uint32_t v = emit_run<REMAP>(a, map, tok_row, slot_row, 0, 0, n);
         const uint32_t cnt = block_sum(v, sm.scratch);
@@ -253,236 +233,218 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k_topk_expand(const TopkArgs 
         return;
     }
 
-    // ---- this CTA's slice [beg, beg + n); thread t owns [t*R, t*R + R) of it
-    const int64_t beg = static_cast<int64_t>(crank) * L;
-    const int64_t rem = P - beg < L ? P - beg : L;
-    const int n = rem > 0 ? static_cast<int>(rem) : 0;
-    const int my0 = tid * R;                      // first slice index of this thread
-    const int my_n = max(0, min(R, n - my0));     // valid keys of this thread
-    if (REMAP && n > 0) {
-        const int64_t b0 = beg * a.kpool / a.block_size;
-        const int64_t b1e = ((beg + n) * a.kpool - 1) / a.block_size + 1;
-        if (b1e - b0 <= a.bt_cap) {
-            map.btab = sm.btab;
-            map.blk0 = b0;
-            map.nblk = static_cast<int32_t>(b1e - b0);
-            for (int i = tid; i < map.nblk; i += blockDim.x)
-                sm.btab[i] = b0 + i < a.max_blocks ? __ldg(map.bt_row + b0 + i) : -1;
-        }
-    }
-    for (int b = tid; b < kTopkBins; b += blockDim.x) sm.hist[b] = 0;
-    __syncthreads();
+    // ---- the row's scores, read chunk by chunk (see load_chunk)
+    const float* row = a.scores + static_cast<int64_t>(rl) * a.scores_ld;
+    const int64_t nchunks = (P + kChunkPools - 1) / kChunkPools;
+    const int warp = tid >> 5;
+    const bool have_hist = a.hist != nullptr;
 
-    // ---- stage the run as keys (loads issued 4 float4 at a time); level-1 histogram
-    //      locally unless the scorer already counted it
-    const bool local_hist = a.hist == nullptr;
-    {
-        const float4* src = reinterpret_cast<const float4*>(a.scores + static_cast<int64_t>(rl) * a.scores_ld +
-                                                            beg + my0);
-        for (int q0 = 0; q0 < R; q0 += 16) {
-            float4 v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (q0 + 4 * j < my_n) v[j] = __ldcg(src + (q0 >> 2) + j);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = q0 + 4 * j;
-                if (i < my_n) {
-                    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t k = i + u < my_n ? ordered_key(f[u]) : 0u;
-                        sm.keys[(i + u) * T + tid] = k;
-                        if (local_hist && i + u < my_n) atomicAdd(&sm.hist[k >> 21], 1u);
-                    }
-                }
-            }
-        }
-    }
-    TK_PHASE(2);
-    uint32_t b1, k1, b2, k2, b3, k3;
-    if (local_hist) {
-        cluster_find_bin(cluster, C, crank, sm, 2048, static_cast<uint32_t>(K), b1, k1);
-    } else {
+    // every load is issued before any is waited on: histogram and block table (copied
+    // asynchronously into shared memory), first keys (registers)
+    if (have_hist) {
         const uint32_t* hrow = a.hist + static_cast<int64_t>(rl) * kTopkBins;
-        for (int b = tid; b < kTopkBins; b += blockDim.x) sm.tot[b] = __ldcg(hrow + b);
+        for (int i = tid; i < kTopkBins / 4; i += T) cp_async_16(sm.hist + 4 * i, hrow + 4 * i);
+    }
+    int nblk = 0;
+    if (REMAP) {
+        int64_t need = (ctx + a.block_size - 1) / a.block_size;
+        if (need > a.max_blocks) need = a.max_blocks;
+        if (need <= a.bt_cap) nblk = static_cast<int>(need);
+        for (int i = tid; i < nblk; i += T) cp_async_4(sm.btab + i, map.bt_row + i);
+    }
+    uint32_t key[kChunk];
+    load_chunk(row, 0, P, key);
+
+    // ---- level 1: the bin b1 (top 11 key bits) of the K-th largest key
+    if (!have_hist) {
+        for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
         __syncthreads();
-        block_find_bin(sm.tot, sm, 2048, static_cast<uint32_t>(K), b1, k1);
+        for (int64_t c = 0; c < nchunks; ++c) {
+            if (c > 0) load_chunk(row, c, P, key);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+                if (c * kChunkPools + static_cast<int64_t>(i) * T + tid < P) atomicAdd(&sm.hist[key[i] >> 21], 1u);
+        }
+        if (nchunks > 1) load_chunk(row, 0, P, key);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    TK_PHASE(2);
+    uint32_t b1, k1;
+    block_find_bin(sm.hist, sm, kTopkBins, static_cast<uint32_t>(K), b1, k1);
+    const uint32_t m_list = static_cast<uint32_t>(K) - k1 + sm.hist[b1];  // keys with bin >= b1
+    if (nblk > 0) {
+        map.btab = sm.btab;
+        map.nblk = nblk;
     }
     TK_PHASE(3);
-    const uint32_t m_all = sm.tot[b1];  // keys of bin b1 in the whole row
-    uint32_t thr, need_eq;
 
-    if (m_all <= static_cast<uint32_t>(kTopkCandCap)) {
-        // ---- local candidates (keys of bin b1) in index order, and keys above bin b1
-        uint32_t nc = 0, na = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const uint32_t bk = sm.keys[i * T + tid] >> 21;
-            nc += bk == b1;
-            na += bk > b1;
-        }
-        uint32_t tot_packed;
-        const uint32_t pre = block_excl_scan(nc | (na << 16), sm.scratch, &tot_packed);
-        uint32_t pos = pre & 0xffffu;
-        if (nc) {
-            for (int i = 0; i < my_n; ++i) {
-                const uint32_t k = sm.keys[i * T + tid];
-                if ((k >> 21) == b1) sm.cand[pos++] = make_uint2(k, static_cast<uint32_t>(beg + my0 + i));
+    uint32_t vcount = 0;
+    if (m_list <= static_cast<uint32_t>(kTopkListCap)) {
+        // ---- ordered list of the keys with bin >= b1: per chunk, warp ballots counted per
+        //      (key slot, warp), one block scan over those counts, then the writes
+        uint32_t listed = 0;
+        for (int64_t c = 0; c < nchunks; ++c) {
+            if (c > 0) load_chunk(row, c, P, key);
+            const int64_t cbase = c * kChunkPools + tid;  // pool of key[0]; key[i] is pool cbase + i*T
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const uint32_t m = __ballot_sync(0xffffffffu, cbase + i * T < P && (key[i] >> 21) >= b1);
+                if ((tid & 31) == 0) sm.cnt[i * (T / 32) + warp] = __popc(m);
             }
+            __syncthreads();
+            uint32_t total;
+            const uint32_t ex = block_excl_scan(sm.cnt[tid], sm.scratch, &total);
+            sm.cnt[tid] = ex;  // slot (i, warp) at index i * (T/32) + warp: index order
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const bool sel = cbase + i * T < P && (key[i] >> 21) >= b1;
+                const uint32_t m = __ballot_sync(0xffffffffu, sel);
+                if (sel) {
+                    const uint32_t pos = listed + sm.cnt[i * (T / 32) + warp] + __popc(m & lanemask_lt());
+                    if (pos < static_cast<uint32_t>(kTopkListCap))
+                        sm.list[pos] = make_uint2(key[i], static_cast<uint32_t>(c * kChunkPools + i * T + tid));
+                }
+            }
+            listed += total;
+            __syncthreads();  // sm.cnt is reused by the next chunk
         }
-        if (tid == 0) {
-            sm.xch[crank] = tot_packed & 0xffffu;
-            sm.xch[8 + crank] = tot_packed >> 16;
-        }
+        for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
+        __syncthreads();
         TK_PHASE(4);
-        cluster.sync();  // every CTA's candidate list and counts are published
-        TK_PHASE(5);
+        const uint32_t n_list = min(listed, static_cast<uint32_t>(kTopkListCap));
 
-        // ---- gather all candidates in index order (CTA order, then each list's order)
-        if (tid < static_cast<int>(C)) {
-            const uint32_t* px = cluster.map_shared_rank(sm.xch, static_cast<unsigned>(tid));
-            sm.cnt[16 + tid] = px[tid];      // candidates of CTA tid
-            sm.cnt[24 + tid] = px[8 + tid];  // keys above bin b1 in CTA tid
-        }
-        if (tid < 16) sm.cnt[tid] = 0;  // per-CTA counts of keys > thr / == thr, filled below
-        __syncthreads();
-        for (uint32_t g = tid; g < m_all; g += blockDim.x) {  // all DSMEM loads in flight at once
-            uint32_t c = 0, base = 0;
-            while (g >= base + sm.cnt[16 + c]) base += sm.cnt[16 + c++];
-            sm.merged[g] = cluster.map_shared_rank(sm.cand, c)[g - base];
-        }
-        for (int b = tid; b < kTopkBins; b += blockDim.x) sm.hist[b] = 0;
-        __syncthreads();
-        TK_PHASE(6);
-
-        // ---- exact select of the k1-th largest among the candidates, locally
-        for (uint32_t i = tid; i < m_all; i += blockDim.x) atomicAdd(&sm.hist[(sm.merged[i].x >> 10) & 2047u], 1u);
-        __syncthreads();
-        block_find_bin(sm.hist, sm, 2048, k1, b2, k2);
-        const uint32_t pre22 = (b1 << 11) | b2;
-        for (int b = tid; b < 1024; b += blockDim.x) sm.tot[b] = 0;
-        __syncthreads();
-        for (uint32_t i = tid; i < m_all; i += blockDim.x) {
-            const uint32_t k = sm.merged[i].x;
-            if ((k >> 10) == pre22) atomicAdd(&sm.tot[k & 1023u], 1u);
-        }
-        __syncthreads();
-        block_find_bin(sm.tot, sm, 1024, k2, b3, k3);
-        thr = (pre22 << 10) | b3;
-        need_eq = k3;
-        TK_PHASE(7);
-
-        // ---- per-CTA counts of keys > thr and == thr (from the candidates + keys above b1)
-        for (uint32_t i = tid; i < m_all; i += blockDim.x) {
-            const uint32_t k = sm.merged[i].x;
-            uint32_t c = 0, end = sm.cnt[16];
-            while (i >= end) end += sm.cnt[16 + ++c];
-            if (k > thr) atomicAdd(&sm.cnt[c], 1u);
-            else if (k == thr) atomicAdd(&sm.cnt[8 + c], 1u);
-        }
-        __syncthreads();
-        if (tid < static_cast<int>(C)) sm.cnt[tid] += sm.cnt[24 + tid];
-        __syncthreads();
-    } else {
-        // ---- crowded bin (massive ties): levels 2 and 3 over the whole cluster
-        for (int b = tid; b < kTopkBins; b += blockDim.x) sm.hist[b] = 0;
-        __syncthreads();
-        for (int i = 0; i < my_n; ++i) {
-            const uint32_t k = sm.keys[i * T + tid];
+        // ---- levels 2 and 3 among the list's keys of bin b1
+        for (uint32_t g = tid; g < n_list; g += T) {
+            const uint32_t k = sm.list[g].x;
             if ((k >> 21) == b1) atomicAdd(&sm.hist[(k >> 10) & 2047u], 1u);
         }
-        cluster_find_bin(cluster, C, crank, sm, 2048, k1, b2, k2);
-        const uint32_t pre22 = (b1 << 11) | b2;
-        for (int b = tid; b < kTopkBins; b += blockDim.x) sm.hist[b] = 0;
         __syncthreads();
-        for (int i = 0; i < my_n; ++i) {
-            const uint32_t k = sm.keys[i * T + tid];
+        uint32_t b2, k2, b3, k3;
+        block_find_bin(sm.hist, sm, 2048, k1, b2, k2);
+        const uint32_t pre22 = (b1 << 11) | b2;
+        for (int b = tid; b < 1024; b += T) sm.hist[b] = 0;
+        __syncthreads();
+        for (uint32_t g = tid; g < n_list; g += T) {
+            const uint32_t k = sm.list[g].x;
             if ((k >> 10) == pre22) atomicAdd(&sm.hist[k & 1023u], 1u);
         }
-        cluster_find_bin(cluster, C, crank, sm, 1024, k2, b3, k3);
-        thr = (pre22 << 10) | b3;
-        need_eq = k3;
-        uint32_t g = 0, e = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const uint32_t k = sm.keys[i * T + tid];
-            g += k > thr;
-            e += k == thr;
-        }
-        uint32_t ge;
-        block_excl_scan(g | (e << 16), sm.scratch, &ge);
-        if (tid < static_cast<int>(C)) {
-            uint32_t* peer = cluster.map_shared_rank(sm.xch, static_cast<unsigned>(tid));
-            peer[crank] = ge & 0xffffu;
-            peer[8 + crank] = ge >> 16;
-        }
-        cluster.sync();
-        if (tid < static_cast<int>(C)) {
-            sm.cnt[tid] = sm.xch[tid];
-            sm.cnt[8 + tid] = sm.xch[8 + tid];
-        }
         __syncthreads();
-    }
-    TK_PHASE(8);
+        block_find_bin(sm.hist, sm, 1024, k2, b3, k3);
+        const uint32_t thr = (pre22 << 10) | b3;  // the K-th largest key of the row
+        const uint32_t need_eq = k3;              // keys equal to thr that are kept (lowest index first)
+        TK_PHASE(5);
 
-    // ---- this CTA's share of the kept pools: keys > thr, then the first equal ones
-    uint32_t sel_before = 0, my_take = 0, eq_seen = 0;
-    for (uint32_t c = 0; c < C; ++c) {
-        const uint32_t e = sm.cnt[8 + c];
-        const uint32_t take = need_eq > eq_seen ? min(e, need_eq - eq_seen) : 0u;
-        eq_seen += e;
-        if (c < crank) sel_before += sm.cnt[c] + take;
-        if (c == crank) my_take = take;
-    }
-
-    // ---- per-thread counts, one block scan, then each thread writes its kept pools in order
-    uint32_t gt = 0, eq = 0;
-    for (int i = 0; i < my_n; ++i) {
-        const uint32_t k = sm.keys[i * T + tid];
-        gt += k > thr;
-        eq += k == thr;
-    }
-    uint32_t unused;
-    const uint32_t pre2 = block_excl_scan(gt | (eq << 16), sm.scratch, &unused);
-    const uint32_t gt_pre = pre2 & 0xffffu, eq_pre = pre2 >> 16;
-    TK_PHASE(9);
-    uint32_t vcount = 0;
-    if (gt | eq) {
-        uint32_t pos = sel_before + gt_pre + min(eq_pre, my_take);
-        uint32_t eq_run = eq_pre;
-        for (int i = 0; i < my_n; ++i) {
-            const uint32_t k = sm.keys[i * T + tid];
-            bool keep = k > thr;
-            if (k == thr) keep = eq_run++ < my_take;
-            if (keep) {
-                const int32_t t0 = static_cast<int32_t>((beg + my0 + i) * a.kpool);
-                vcount += emit_pool<REMAP>(a, map, tok_row, slot_row, static_cast<int64_t>(pos) * a.kpool, t0);
-                ++pos;
+        // ---- kept entries: keys > thr and the first need_eq keys == thr; one packed scan
+        //      gives each its output column
+        const uint32_t per = (n_list + T - 1) / T;
+        const uint32_t g0 = tid * per, g1 = min(n_list, g0 + per);
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t g = g0; g < g1; ++g) {
+            const uint32_t k = sm.list[g].x;
+            gt += k > thr;
+            eq += k == thr;
+        }
+        uint32_t unused;
+        const uint32_t pre2 = block_excl_scan(gt | (eq << 16), sm.scratch, &unused);
+        uint32_t gt_run = pre2 & 0xffffu, eq_run = pre2 >> 16;
+        for (uint32_t g = g0; g < g1; ++g) {
+            const uint2 e = sm.list[g];
+            const uint32_t out = gt_run + min(eq_run, need_eq);
+            const bool keep = e.x > thr || (e.x == thr && eq_run < need_eq);
+            gt_run += e.x > thr;
+            eq_run += e.x == thr;
+            if (keep)
+                vcount += emit_pool<REMAP>(a, map, tok_row, slot_row, static_cast<int64_t>(out) * a.kpool,
+                                           static_cast<int32_t>(static_cast<int64_t>(e.y) * a.kpool));
+        }
+        TK_PHASE(6);
+    } else {
+        // ---- crowded threshold bin (massive ties): levels 2 and 3 and the output re-read the row
+        uint32_t pre = b1, shift = 21, krem = k1;
+        for (int lvl = 0; lvl < 2; ++lvl) {
+            const uint32_t nb = lvl == 0 ? 2048u : 1024u;
+            const uint32_t sh = lvl == 0 ? 10u : 0u;
+            for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
+            __syncthreads();
+            for (int64_t c = 0; c < nchunks; ++c) {
+                load_chunk(row, c, P, key);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i)
+                    if (c * kChunkPools + i * T + tid < P && (key[i] >> shift) == pre)
+                    atomicAdd(&sm.hist[(key[i] >> sh) & (nb - 1)], 1u);
             }
+            __syncthreads();
+            uint32_t bb, kk;
+            block_find_bin(sm.hist, sm, static_cast<int>(nb), krem, bb, kk);
+            pre = (pre << (lvl == 0 ? 11 : 10)) | bb;
+            shift = sh;
+            krem = kk;
+        }
+        const uint32_t thr = pre;
+        const uint32_t need_eq = krem;
+        // per chunk: counts of keys > thr and == thr per (key slot, warp), two block scans,
+        // then each kept key's column = (keys > thr before it) + min(keys == thr before it, need_eq)
+        uint32_t gt_base = 0, eq_base = 0;
+        uint32_t* gcnt = sm.hist;          // [T]
+        uint32_t* ecnt = sm.hist + T;      // [T]
+        for (int64_t c = 0; c < nchunks; ++c) {
+            load_chunk(row, c, P, key);
+            const int64_t cbase = c * kChunkPools + tid;
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const bool in = cbase + i * T < P;
+                const uint32_t mg = __ballot_sync(0xffffffffu, in && key[i] > thr);
+                const uint32_t me = __ballot_sync(0xffffffffu, in && key[i] == thr);
+                if ((tid & 31) == 0) {
+                    gcnt[i * (T / 32) + warp] = __popc(mg);
+                    ecnt[i * (T / 32) + warp] = __popc(me);
+                }
+            }
+            __syncthreads();
+            uint32_t gtot, etot;
+            const uint32_t gex = block_excl_scan(gcnt[tid], sm.scratch, &gtot);
+            __syncthreads();
+            const uint32_t eex = block_excl_scan(ecnt[tid], sm.scratch, &etot);
+            gcnt[tid] = gex;
+            ecnt[tid] = eex;
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const bool in = cbase + i * T < P;
+                const bool g = in && key[i] > thr;
+                const bool e = in && key[i] == thr;
+                const uint32_t mg = __ballot_sync(0xffffffffu, g);
+                const uint32_t me = __ballot_sync(0xffffffffu, e);
+                const uint32_t gb = gt_base + gcnt[i * (T / 32) + warp] + __popc(mg & lanemask_lt());
+                const uint32_t eb = eq_base + ecnt[i * (T / 32) + warp] + __popc(me & lanemask_lt());
+                if (g || (e && eb < need_eq))
+                    vcount += emit_pool<REMAP>(a, map, tok_row, slot_row,
+                                               static_cast<int64_t>(gb + min(eb, need_eq)) * a.kpool,
+                                               static_cast<int32_t>((c * kChunkPools + i * T + tid) * a.kpool));
+            }
+            gt_base += gtot;
+            eq_base += etot;
+            __syncthreads();
         }
     }
-    TK_PHASE(10);
 
-    // ---- trailing incomplete pool and -1 padding (first CTA), valid count
-    if (crank == 0) vcount += emit_run<REMAP>(a, map, tok_row, slot_row, K * a.kpool, P * a.kpool, ctx);
-    const uint32_t vcta = block_sum(vcount, sm.scratch);
-    if (tid == 0) cluster.map_shared_rank(sm.xch, 0u)[16 + crank] = vcta;
-    cluster.sync();  // also: no CTA leaves while a peer may still read its shared memory
-    if (crank == 0 && tid == 0 && a.counts) {
-        uint32_t total = 0;
-        for (uint32_t c = 0; c < C; ++c) total += sm.xch[16 + c];
-        a.counts[r] = static_cast<int32_t>(total);
-    }
-    TK_PHASE(11);
+    // ---- trailing incomplete pool and -1 padding, valid count
+    vcount += emit_run<REMAP>(a, map, tok_row, slot_row, K * a.kpool, P * a.kpool, ctx);
+    const uint32_t total_valid = block_sum(vcount, sm.scratch);
+    if (tid == 0 && a.counts) a.counts[r] = static_cast<int32_t>(total_valid);
+    TK_PHASE(7);
+    if (tid == 0 && rl < 200) SEL_PHASE(300 + rl);  // diagnostics: every row's end
 #undef TK_PHASE
 }
 
-size_t topk_smem_bytes(int slice_cap, int bt_cap) {
-    return static_cast<size_t>(slice_cap) * 4 + 2 * kTopkBins * 4 + 2 * kTopkCandCap * 8 +
-           static_cast<size_t>((bt_cap + 3) & ~3) * 4 + (64 + 32 + 32 + 8) * 4;
+size_t topk_smem_bytes(int bt_cap) {
+    return (static_cast<size_t>(T) + kTopkBins) * 4 + static_cast<size_t>(kTopkListCap) * 8 +
+           static_cast<size_t>((bt_cap + 3) & ~3) * 4 + (64 + 8) * 4;
 }
 
-cudaError_t launch_topk(const TopkArgs& a, bool remap, int cluster, int rows, size_t smem, bool pdl,
-                        cudaStream_t s) {
+cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s) {
     static size_t configured[2][kMaxDevicesTracked] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -494,19 +456,15 @@ cudaError_t launch_topk(const TopkArgs& a, bool remap, int cluster, int rows, si
         configured[remap ? 1 : 0][dev] = smem;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(cluster), static_cast<unsigned>(rows), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
     cfg.blockDim = dim3(kTopkThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     if (remap) return cudaLaunchKernelEx(&cfg, k_topk_expand<true>, a);
     return cudaLaunchKernelEx(&cfg, k_topk_expand<false>, a);
 }

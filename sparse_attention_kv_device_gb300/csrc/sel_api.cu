@@ -19,8 +19,6 @@ using namespace sel;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kTopkSliceTarget = 8192;   // keys per CTA the top-k cluster aims for
-constexpr int kTopkMaxCluster = 8;       // portable cluster size
 constexpr int kMaxSegRows = 64;          // rows x 4 heads <= 256 = the MMA's largest N
 constexpr int kMaxChunkRows = 32768;
 constexpr int kTopkMaxBtCap = 8192;      // block-table entries a top-k CTA stages at most
@@ -108,30 +106,17 @@ int encode_q_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_str
 
 // ------------------------------------------------------------------ planning
 struct TopkPlan {
-    int cluster = 1;
-    int slice_cap = 4;
     int bt_cap = 0;
     size_t smem = 0;
 };
 
-// Cluster size and shared-memory plan of the top-k for rows of up to max_pools pools:
-// at least one CTA per kTopkSliceTarget keys, and as many CTAs (up to the portable
-// cluster size) as fill one wave of two CTAs per SM for `rows` rows. With remap, each CTA
-// also stages the block-table entries its slice's tokens need.
-int plan_topk(int64_t max_pools, int rows, int sms, int kpool, int block_size, bool remap, int max_smem,
-              TopkPlan* t) {
-    const int64_t mp = std::max<int64_t>(max_pools, 1);
-    const int64_t need = ceil_div(mp, kTopkSliceTarget);
-    const int64_t fill = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / std::max(rows, 1));
-    t->cluster = static_cast<int>(std::min<int64_t>(kTopkMaxCluster, std::max(need, std::min(fill, mp / 512 + 1))));
-    // per-CTA slice length L (multiple of 4); per-thread run R (multiple of 4); capacity T*R
-    const int64_t L = (ceil_div(mp, t->cluster) + 3) & ~int64_t(3);
-    const int64_t R = (ceil_div(L, kTopkThreads) + 3) & ~int64_t(3);
-    t->slice_cap = static_cast<int>(R * kTopkThreads);
-    t->bt_cap = remap ? static_cast<int>(std::min<int64_t>(kTopkMaxBtCap,
-                                                            ceil_div(L * kpool, block_size) + 2))
+// Shared-memory plan of the top-k: with remap, a row stages up to kTopkMaxBtCap entries
+// of its block-table row (longer rows read the rest from global memory).
+int plan_topk(int64_t max_context, int block_size, bool remap, int max_smem, TopkPlan* t) {
+    t->bt_cap = remap ? static_cast<int>(std::min<int64_t>(kTopkMaxBtCap, ceil_div(std::max<int64_t>(max_context, 1),
+                                                                                   block_size)))
                       : 0;
-    t->smem = topk_smem_bytes(t->slice_cap, t->bt_cap);
+    t->smem = topk_smem_bytes(t->bt_cap);
     if (t->smem > static_cast<size_t>(max_smem)) return SEL_EUNSUPPORTED;
     return SEL_OK;
 }
@@ -140,7 +125,7 @@ struct Plan {
     int chunk_rows = 1, seg_rows = 1, max_segs = 1, max_tiles = 1;
     int64_t max_pools = 0, scores_ld = 4;
     size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0, off_tiles = 0,
-           off_scores = 0, off_hist = 0;
+           off_scores = 0, off_hist = 0, off_rowsel = 0, off_cand = 0;
     int64_t hist_words = 0;
     size_t ws_score = 0, ws_select = 0;
     int npad_max = 16, stages = 2;
@@ -148,6 +133,8 @@ struct Plan {
     size_t score_smem = 0;
     TopkPlan topk;
     int sms = 0;
+    int bm_words = 1;
+    size_t fin_smem = 0;
 };
 
 int check_problem(const sel_problem* p) {
@@ -212,9 +199,15 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->ws_score = off;
     pl->off_scores = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
+    // per-row histograms followed by per-row candidate counts: one region the builder zeroes
     pl->off_hist = off;
-    pl->hist_words = static_cast<int64_t>(pl->chunk_rows) * kTopkBins;
+    pl->hist_words = (static_cast<int64_t>(pl->chunk_rows) * (kTopkBins + 1) + 3) & ~int64_t(3);
     off = align256(off + sizeof(uint32_t) * static_cast<size_t>(pl->hist_words));
+    pl->off_rowsel = off;
+    off = align256(off + sizeof(int2) * static_cast<size_t>(pl->chunk_rows));
+    pl->off_cand = off;
+    off = align256(off + sizeof(uint2) * static_cast<size_t>(pl->chunk_rows) * kSelCandCap);
+    pl->bm_words = static_cast<int>((pl->max_pools + 31) / 32);
     pl->ws_select = off;
 
     pl->npad_max = ((4 * pl->seg_rows + 15) / 16) * 16;
@@ -223,18 +216,23 @@ int make_plan(const sel_problem* p, Plan* pl) {
     const size_t fixed = score_smem_bytes(0, pl->npad_max);
     if (fixed + 2 * 32768 > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
     pl->stages = static_cast<int>(std::min<size_t>(8, (di.max_smem_optin - fixed) / 32768));
+    while (pl->stages > 2 && score_smem_bytes(pl->stages, pl->npad_max) > static_cast<size_t>(di.max_smem_optin))
+        --pl->stages;
     pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max);
-    return plan_topk(pl->max_pools, pl->chunk_rows, di.sms, p->kpool, p->block_size, true, di.max_smem_optin,
-                     &pl->topk);
+    if ((rc = plan_topk(p->max_context, p->block_size, true, di.max_smem_optin, &pl->topk)) != SEL_OK) return rc;
+    pl->fin_smem = finalize_smem_bytes(kSelCandCap, pl->bm_words, pl->topk.bt_cap);
+    if (pl->fin_smem > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    return SEL_OK;
 }
 
 // ------------------------------------------------------------------ tracing
 std::mutex g_trace_mu;
-cudaEvent_t g_trace[4] = {nullptr, nullptr, nullptr, nullptr};
+constexpr int kTraceEvents = 6;
+cudaEvent_t g_trace[kTraceEvents] = {};
 int g_trace_n = 0;
 
 void trace_record(int i, cudaStream_t s) {
-    if (g_trace_n < 4 || !g_trace[i]) return;
+    if (g_trace_n < kTraceEvents || !g_trace[i]) return;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaStreamIsCapturing(s, &cs);
     if (cs == cudaStreamCaptureStatusActive)
@@ -253,6 +251,9 @@ struct Ws {
     int4* tiles;
     float* scores;
     uint32_t* hist;
+    uint32_t* row_count;
+    int2* row_sel;
+    uint2* cand;
 };
 
 Ws carve_ws(void* ws, const Plan& pl) {
@@ -266,6 +267,9 @@ Ws carve_ws(void* ws, const Plan& pl) {
     w.tiles = reinterpret_cast<int4*>(b + pl.off_tiles);
     w.scores = reinterpret_cast<float*>(b + pl.off_scores);
     w.hist = reinterpret_cast<uint32_t*>(b + pl.off_hist);
+    w.row_count = w.hist + static_cast<int64_t>(pl.chunk_rows) * kTopkBins;
+    w.row_sel = reinterpret_cast<int2*>(b + pl.off_rowsel);
+    w.cand = reinterpret_cast<uint2*>(b + pl.off_cand);
     return w;
 }
 
@@ -300,7 +304,7 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     b.hdr = w.hdr;
     b.status = status;
     b.hist = hist;
-    b.hist_words = static_cast<int64_t>(c1 - c0) * kTopkBins;
+    b.hist_words = pl.hist_words;
     b.zero_ctas = static_cast<int32_t>(std::min<int64_t>(32, std::max<int64_t>(1, b.hist_words / 16384)));
     if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
     if (c0 == 0 && !score_all) trace_record(1, s);
@@ -317,7 +321,6 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     a.pool_cap = b.pool_cap;
     a.scores = scores;
     a.scores_ld = ld;
-    a.hist = hist;
     a.npad_max = pl.npad_max;
     a.stages = pl.stages;
     a.tmem_cols = pl.tmem_cols;
@@ -389,12 +392,10 @@ int sel_topk_expand(const float* scores, int64_t scores_ld, const int32_t* posit
     int rc = current_device_info(&di);
     if (rc != SEL_OK) return rc;
     TopkPlan tp;
-    if ((rc = plan_topk(scores_ld, std::min(num_rows, 65535), di.sms, kpool, 1, false, di.max_smem_optin, &tp)) !=
-        SEL_OK)
-        return rc;
+    if ((rc = plan_topk(0, 1, false, di.max_smem_optin, &tp)) != SEL_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (int c0 = 0; c0 < num_rows; c0 += 65535) {
-        const int rows = std::min(65535, num_rows - c0);
+    for (int c0 = 0; c0 < num_rows; c0 += kMaxChunkRows) {
+        const int rows = std::min(kMaxChunkRows, num_rows - c0);
         TopkArgs a{};
         a.scores = scores + static_cast<int64_t>(c0) * scores_ld;
         a.scores_ld = scores_ld;
@@ -404,13 +405,12 @@ int sel_topk_expand(const float* scores, int64_t scores_ld, const int32_t* posit
         a.kpool = kpool;
         a.out_width = out_width;
         a.max_pools = scores_ld;
-        a.slice_cap = tp.slice_cap;
         a.bt_cap = 0;
         a.token_idx = token_idx;
         a.counts = valid_counts;
         a.status = status;
         a.block_size = 1;
-        if (launch_topk(a, false, tp.cluster, rows, tp.smem, false, s) != cudaSuccess) return SEL_ECUDA;
+        if (launch_topk(a, false, rows, tp.smem, false, s) != cudaSuccess) return SEL_ECUDA;
     }
     return SEL_OK;
 }
@@ -468,32 +468,54 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, w.hist, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
-        TopkArgs a{};
-        a.scores = w.scores;
-        a.scores_ld = pl.scores_ld;
-        a.positions = p->positions;
-        a.row_ctx = w.row_ctx;
-        a.row_req = w.row_req;
-        a.hist = w.hist;
-        a.row_begin = c0;
-        a.topk = p->index_topk;
-        a.kpool = p->kpool;
-        a.out_width = out_width;
-        a.max_pools = pl.max_pools;
-        a.slice_cap = pl.topk.slice_cap;
-        a.bt_cap = pl.topk.bt_cap;
-        a.token_idx = token_idx;
-        a.slots = slots;
-        a.counts = valid_counts;
-        a.block_table = p->block_table;
-        a.bt_ld = p->bt_ld;
-        a.max_blocks = p->max_blocks_per_req;
-        a.num_kv_blocks = p->num_kv_blocks;
-        a.block_size = p->block_size;
-        a.block_stride_rows = p->block_stride_rows;
-        a.status = st;
-        if (launch_topk(a, true, pl.topk.cluster, c1 - c0, pl.topk.smem, true, s) != cudaSuccess) return SEL_ECUDA;
+        HistArgs h{};
+        h.scores = w.scores;
+        h.scores_ld = pl.scores_ld;
+        h.row_ctx = w.row_ctx;
+        h.topk = p->index_topk;
+        h.kpool = p->kpool;
+        h.hist = w.hist;
+        if (launch_hist(h, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
         if (last) trace_record(3, s);
+        CollectArgs ca{};
+        ca.scores = w.scores;
+        ca.scores_ld = pl.scores_ld;
+        ca.row_ctx = w.row_ctx;
+        ca.topk = p->index_topk;
+        ca.kpool = p->kpool;
+        ca.hist = w.hist;
+        ca.row_count = w.row_count;
+        ca.row_sel = w.row_sel;
+        ca.cand = w.cand;
+        ca.cand_cap = kSelCandCap;
+        if (launch_collect(ca, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
+        if (last) trace_record(4, s);
+        FinalizeArgs fa{};
+        fa.scores = w.scores;
+        fa.scores_ld = pl.scores_ld;
+        fa.row_ctx = w.row_ctx;
+        fa.row_req = w.row_req;
+        fa.row_count = w.row_count;
+        fa.row_sel = w.row_sel;
+        fa.cand = w.cand;
+        fa.cand_cap = kSelCandCap;
+        fa.bm_words = pl.bm_words;
+        fa.bt_cap = pl.topk.bt_cap;
+        fa.row_begin = c0;
+        fa.topk = p->index_topk;
+        fa.kpool = p->kpool;
+        fa.out_width = out_width;
+        fa.slots = slots;
+        fa.token_idx = token_idx;
+        fa.counts = valid_counts;
+        fa.block_table = p->block_table;
+        fa.bt_ld = p->bt_ld;
+        fa.max_blocks = p->max_blocks_per_req;
+        fa.num_kv_blocks = p->num_kv_blocks;
+        fa.block_size = p->block_size;
+        fa.block_stride_rows = p->block_stride_rows;
+        if (launch_finalize(fa, c1 - c0, pl.fin_smem, true, s) != cudaSuccess) return SEL_ECUDA;
+        if (last) trace_record(5, s);
     }
     return SEL_OK;
 }
@@ -501,7 +523,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
 int32_t sel_select_launch_count(const sel_problem* p) {
     Plan pl;
     if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
-    return static_cast<int32_t>(3 * ceil_div(p->num_rows, pl.chunk_rows));
+    return static_cast<int32_t>(5 * ceil_div(p->num_rows, pl.chunk_rows));
 }
 
 size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {
@@ -573,16 +595,31 @@ int sel_select_host(const sel_problem* p, int32_t* slots_host, int32_t out_width
     return SEL_OK;
 }
 
+#ifdef SEL_PHASE_TRACE
+namespace {
+__device__ unsigned long long g_sel_marks[64];
+__global__ void k_mark(int slot) { g_sel_marks[slot] = sel::global_timer_ns(); }
+}  // namespace
+// diagnostics build only: a one-thread kernel that stamps the global timer into slot
+int sel_debug_mark(sel_stream_t stream, int slot) {
+    k_mark<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(slot & 63);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+int sel_debug_marks(void* dst) {
+    return cudaMemcpyFromSymbol(dst, g_sel_marks, sizeof(g_sel_marks)) == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+#endif
+
 int sel_set_trace_events(void* const* events, int32_t n) {
     std::lock_guard<std::mutex> g(g_trace_mu);
     if (n == 0) {
         g_trace_n = 0;
-        for (int i = 0; i < 4; ++i) g_trace[i] = nullptr;
+        for (int i = 0; i < kTraceEvents; ++i) g_trace[i] = nullptr;
         return SEL_OK;
     }
-    if (n < 4 || !events) return SEL_EINVAL;
-    for (int i = 0; i < 4; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
-    g_trace_n = 4;
+    if (n < kTraceEvents || !events) return SEL_EINVAL;
+    for (int i = 0; i < kTraceEvents; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    g_trace_n = kTraceEvents;
     return SEL_OK;
 }
 

@@ -88,6 +88,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Asynchronous global -> shared copies (no register staging); cp_async_wait_all waits for
+// every copy this thread issued.
+__device__ __forceinline__ void cp_async_4(void* smem, const void* gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
@@ -213,10 +223,12 @@ constexpr int kPhaseSlots = 512;
         return cudaMemcpyFromSymbol(dst, g_sel_phase, bytes) == cudaSuccess ? 0 : -3;     \
     }
 #define SEL_PHASE(slot) (g_sel_phase[(slot)] = ::sel::global_timer_ns())
+#define SEL_PHASE_CLK(slot) (g_sel_phase[(slot)] = clock64())
 #define SEL_PHASE_VALUE(slot, v) (g_sel_phase[(slot)] = static_cast<unsigned long long>(v))
 #else
 #define SEL_PHASE_TABLE(tag)
 #define SEL_PHASE(slot) ((void)0)
+#define SEL_PHASE_CLK(slot) ((void)0)
 #define SEL_PHASE_VALUE(slot, v) ((void)0)
 #endif
 

@@ -30,7 +30,7 @@ struct BuildArgs {
     int4* seg;                 // [max_segs] {req, first row, rows, pools to score}
     int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
     int4* tiles;               // [max_tiles] {segment, tile in segment, page 0, page 1}
-    int32_t* hdr;              // [0] segments, [1] tiles
+    int32_t* hdr;              // [0] segments, [1] tiles, [2] scorer's dynamic-tile counter (set to 0)
     int32_t* status;
     uint32_t* hist;            // per-row level-1 histograms the scorer fills; zeroed here (nullable)
     int64_t hist_words;
@@ -43,14 +43,13 @@ struct BuildArgs {
 // Segmented scorer (TMA + tcgen05): every CTA scores an even share of all tiles.
 struct ScoreArgs {
     const int4* seg;
-    const int32_t* hdr;
+    int32_t* hdr;            // [1] tiles; [2] dynamic-tile counter (zeroed by the builder)
     const int4* tiles;
     const int32_t* row_ctx;  // chunk-local
     int32_t row_begin;
     int32_t topk, kpool, score_all, pool_cap;
     float* scores;           // chunk-local rows
     int64_t scores_ld;
-    uint32_t* hist;          // chunk-local rows x kTopkBins: counts of the top 11 key bits (nullable)
     int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
     int32_t stages;
     uint32_t tmem_cols;      // TMEM columns allocated (power of two)
@@ -58,7 +57,51 @@ struct ScoreArgs {
     int32_t* status;
 };
 
-// Top-k pools + expansion (+ remap), one thread-block cluster per row.
+// Level-1 histogram of every row's scores (top 11 bits of the order-preserving keys),
+// accumulated into zeroed per-row counters: CTA (x, y) counts keys [x*kHistSlice, ...) of row y.
+struct HistArgs {
+    const float* scores;       // chunk-local rows
+    int64_t scores_ld;
+    const int32_t* row_ctx;    // chunk-local (builder output)
+    int32_t topk, kpool;
+    uint32_t* hist;            // [rows][kTopkBins]
+};
+
+// Collect the keys at or above each row's threshold bin (CTA = kHistSlice pools of a row).
+struct CollectArgs {
+    const float* scores;       // chunk-local rows
+    int64_t scores_ld;
+    const int32_t* row_ctx;
+    int32_t topk, kpool;
+    const uint32_t* hist;      // [rows][kTopkBins]
+    uint32_t* row_count;       // [rows] zeroed by the builder; candidates appended
+    int2* row_sel;             // [rows] (threshold bin b1, rank inside it)
+    uint2* cand;               // [rows][cand_cap] (key, pool)
+    int32_t cand_cap;
+};
+
+// Exact select among a row's candidates, ordered write-out with expansion and remap.
+struct FinalizeArgs {
+    const float* scores;       // chunk-local rows (re-read only for crowded ties)
+    int64_t scores_ld;
+    const int32_t* row_ctx;
+    const int32_t* row_req;
+    const uint32_t* row_count;
+    const int2* row_sel;
+    const uint2* cand;
+    int32_t cand_cap, bm_words, bt_cap;
+    int32_t row_begin;
+    int32_t topk, kpool, out_width;
+    int32_t* slots;            // global rows
+    int32_t* token_idx;        // nullable
+    int32_t* counts;           // nullable
+    const int32_t* block_table;
+    int64_t bt_ld;
+    int32_t max_blocks, num_kv_blocks, block_size;
+    int64_t block_stride_rows;
+};
+
+// Top-k pools + expansion (+ remap), one CTA per row.
 struct TopkArgs {
     const float* scores;       // chunk-local rows
     int64_t scores_ld;
@@ -69,8 +112,7 @@ struct TopkArgs {
     int32_t row_begin;
     int32_t topk, kpool, out_width;
     int64_t max_pools;         // rows with ctx / kpool beyond this are out of bound
-    int32_t slice_cap;         // keys staged in shared memory per CTA
-    int32_t bt_cap;            // block-table entries staged in shared memory per CTA
+    int32_t bt_cap;            // block-table entries staged in shared memory per row
     int32_t* token_idx;        // [rows][out_width] global rows, nullable
     int32_t* slots;            // [rows][out_width] global rows, with remap
     int32_t* counts;           // [rows] global rows, nullable
@@ -99,12 +141,17 @@ constexpr int kBuildThreads = 1024;
 constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 2048;
-constexpr int kTopkCandCap = 2048;   // threshold-bin keys gathered per row for the local select
+constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin listed per row
 constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
+constexpr int kHistThreads = 256;
+constexpr int kCollectThreads = 256;   // 8 histogram bins and 8 pools per thread
+constexpr int kFinalizeThreads = 512;
+constexpr int kSelCandCap = 4096;      // candidates kept per row
+constexpr int kHistSlice = 2048;     // keys counted per histogram CTA
 
 size_t score_smem_bytes(int stages, int npad_max);
-size_t topk_smem_bytes(int slice_cap, int bt_cap);
+size_t topk_smem_bytes(int bt_cap);
 
 // Launchers. With `pdl` the kernel is a programmatic dependent of the previous kernel
 // on the stream: its prologue may overlap that kernel, and it waits (griddepcontrol)
@@ -112,8 +159,11 @@ size_t topk_smem_bytes(int slice_cap, int bt_cap);
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
                          size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_topk(const TopkArgs& a, bool remap, int cluster, int rows, size_t smem, bool pdl,
-                        cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_remap(const RemapArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_hist(const HistArgs& a, int rows, int64_t max_pools, bool pdl, cudaStream_t s);
+cudaError_t launch_collect(const CollectArgs& a, int rows, int64_t max_pools, bool pdl, cudaStream_t s);
+size_t finalize_smem_bytes(int cand_cap, int bm_words, int bt_cap);
+cudaError_t launch_finalize(const FinalizeArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
 
 }  // namespace sel
