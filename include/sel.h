@@ -191,6 +191,27 @@ int sel_select(const sel_problem *p, int32_t *slots, int32_t out_width, int32_t 
                sel_stream_t stream);
 
 /*
+ * sel_select_static -- sel_select without a workspace argument, for callers that cannot
+ * allocate device memory per call (a serving engine that has reserved nearly all HBM for
+ * its paged KV cache at start-up; a plain C host program with no device allocator). The
+ * published method has no counterpart of this entry point.
+ * Arguments, layouts, results and the other error codes are those of sel_select. The
+ * scratch is one file-scope device array of SEL_STATIC_WS_MAX_BYTES bytes, held by every
+ * GPU that loads the library until the process exits; no call allocates or frees device
+ * memory. Returns SEL_EWORKSPACE, queueing nothing, when sel_workspace_bytes(p) exceeds
+ * SEL_STATIC_WS_MAX_BYTES (a smaller p->chunk_rows lowers that size).
+ * The first call on a device (with that device current) looks up the array's address
+ * and keeps it; make that first call before any stream capture. Every call on a device
+ * uses the same array: calls whose work overlaps on the GPU (unordered streams) race
+ * and give wrong results. The kernels clear every counter they rely on, so no zeroing
+ * is needed between calls.
+ */
+#define SEL_STATIC_WS_MAX_BYTES (16u << 20)
+int sel_select_static(const sel_problem *p, int32_t *slots, int32_t out_width,
+                      int32_t *valid_counts, int32_t *token_idx, int32_t *status,
+                      sel_stream_t stream);
+
+/*
  * sel_select_host -- sel_select for callers whose per-step inputs and outputs live
  * in HOST memory (ideally pinned). The key cache stays resident on the device
  * (p->key_cache is a device pointer). p's query_start_loc, positions, q,

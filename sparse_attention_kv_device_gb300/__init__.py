@@ -17,6 +17,7 @@ from .sel import (  # noqa: F401
     sel_select,
     sel_select_host,
     sel_select_launch_count,
+    sel_select_static,
     sel_set_trace_events,
     sel_topk_expand,
     sel_version,

@@ -70,6 +70,7 @@ def _load():
     lib.sel_topk_expand.argtypes = [P, I64, P, I32, I32, I32, P, I32, P, P, P]
     lib.sel_remap_global.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I64, P, P, P]
     lib.sel_select.argtypes = [PP, P, I32, P, P, P, P, SZ, P]
+    lib.sel_select_static.argtypes = [PP, P, I32, P, P, P, P]
     lib.sel_host_stage_bytes.argtypes = [PP, I32]
     lib.sel_host_stage_bytes.restype = SZ
     lib.sel_select_host.argtypes = [PP, P, I32, P, P, P, SZ, P, SZ, P]
@@ -77,7 +78,7 @@ def _load():
     lib.sel_select_launch_count.argtypes = [PP]
     lib.sel_select_launch_count.restype = I32
     for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
-              "sel_select_host", "sel_set_trace_events"):
+              "sel_select_static", "sel_select_host", "sel_set_trace_events"):
         getattr(lib, f).restype = C.c_int
     return lib
 
@@ -86,7 +87,7 @@ _lib = _load()
 
 EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_workspace_bytes",
            "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
-           "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
+           "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
            "sel_select_launch_count"]
 
 
@@ -293,6 +294,23 @@ def sel_select(problem: Problem, slots, valid_counts, token_idx=None, status=Non
     _check(_lib.sel_select(problem.byref(), _ptr(slots), int(slots.shape[1]), _ptr(valid_counts),
                            _ptr(token_idx), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
                            _stream(stream)), "sel_select")
+    return slots, valid_counts
+
+
+def sel_select_static(problem: Problem, slots, valid_counts, token_idx=None, status=None, stream=None):
+    """sel_select with the library's fixed device scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory per call; this binding allocates
+    nothing either. Calls on one device must not overlap on the GPU (they share the
+    array). Raises SelError(SEL_EWORKSPACE) when the problem needs more scratch than
+    SEL_STATIC_WS_MAX_BYTES."""
+    for t, n in ((slots, "slots"), (valid_counts, "valid_counts"), (token_idx, "token_idx"),
+                 (status, "status")):
+        _dev(t, torch.int32, n)
+    if not slots.is_contiguous() or (token_idx is not None and not token_idx.is_contiguous()):
+        raise ValueError("slots and token_idx must be contiguous")
+    _check(_lib.sel_select_static(problem.byref(), _ptr(slots), int(slots.shape[1]), _ptr(valid_counts),
+                                  _ptr(token_idx), _ptr(status), _stream(stream)), "sel_select_static")
     return slots, valid_counts
 
 

@@ -1,0 +1,77 @@
+"""sel_select_static (the fused selection on the library's fixed device scratch array)
+against sel_select with a caller-allocated workspace, through the C ABI.
+
+Both entry points queue the same kernels on the same inputs, so the outputs must agree
+exactly (the selection's score tolerance never comes into play). Two calls in a row
+check that the array carries nothing over from one call to the next. This file is
+collected last so that it also runs after every other GPU test in the same process."""
+
+import pytest
+import torch
+
+import workloads
+from _gpu import DEV, lib
+
+pytestmark = pytest.mark.gpu
+
+SEL_EWORKSPACE = -4
+STATIC_MAX = 16 << 20   # SEL_STATIC_WS_MAX_BYTES
+
+
+def _outputs(w):
+    slots = torch.full((w.num_rows, w.out_width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((w.num_rows,), -7, dtype=torch.int32, device=DEV)
+    tok = torch.full_like(slots, -7)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    return slots, counts, tok, status
+
+
+def _reference(sel, prob, w):
+    slots, counts, tok, status = _outputs(w)
+    sel.sel_select(prob, slots, counts, token_idx=tok, status=status)
+    torch.cuda.synchronize()
+    return slots, counts, tok, status
+
+
+def _assert_same(a, b):
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode32k", "decode128k"])
+def test_static_entry_matches_sel_select_twice(name):
+    sel = lib()
+    w = workloads.make_workload(name)
+    prob = sel.problem_from_workload(w, DEV)
+    assert sel.sel_workspace_bytes(prob) <= STATIC_MAX
+    ref = _reference(sel, prob, w)
+    first, second = _outputs(w), _outputs(w)
+    before = torch.cuda.memory_allocated()
+    sel.sel_select_static(prob, first[0], first[1], token_idx=first[2], status=first[3])
+    sel.sel_select_static(prob, second[0], second[1], token_idx=second[2], status=second[3])
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before
+    _assert_same(first, ref)
+    _assert_same(second, ref)
+
+
+def test_static_entry_rejects_problems_beyond_its_array():
+    sel = lib()
+    w = workloads.make_workload("mixed")
+    big = sel.problem_from_workload(w, DEV)                   # 256-row chunks at 128K context
+    assert sel.sel_workspace_bytes(big) > STATIC_MAX
+    out = _outputs(w)
+    with pytest.raises(sel.SelError) as err:
+        sel.sel_select_static(big, out[0], out[1], token_idx=out[2], status=out[3])
+    assert err.value.code == SEL_EWORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out[0] == -7).all()) and bool((out[1] == -7).all())   # nothing was queued
+
+    small = sel.problem_from_workload(w, DEV, chunk_rows=64)  # smaller chunks fit the array
+    assert sel.sel_workspace_bytes(small) <= STATIC_MAX
+    ref = _reference(sel, small, w)
+    for _ in range(2):
+        got = _outputs(w)
+        sel.sel_select_static(small, got[0], got[1], token_idx=got[2], status=got[3])
+        torch.cuda.synchronize()
+        _assert_same(got, ref)
