@@ -26,7 +26,8 @@
  * Conventions for every entry point:
  *  - All array arguments are DEVICE pointers unless stated otherwise, owned by the
  *    caller, and must stay valid until the work queued on `stream` has finished.
- *    The library allocates no memory and keeps no device state between calls.
+ *    The library allocates no memory; apart from the fixed scratch array of
+ *    sel_select_static it keeps no device state between calls.
  *  - Work is queued on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    No entry point synchronises the device or reads device memory on the host, so
  *    the device entry points can be captured into a CUDA graph. Values baked into a
@@ -227,12 +228,12 @@ int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width
                     void *ws, size_t ws_bytes, sel_stream_t stream);
 
 /*
- * Tracing hook. With n >= 6 events (cudaEvent_t handles, created by the caller with
+ * Tracing hook. With n >= 5 events (cudaEvent_t handles, created by the caller with
  * timing enabled), every following sel_select records, on `stream`: events[0] before its
  * first segment-builder launch, events[1] after that builder (before the first scorer
  * launch), events[2] after the last scorer launch, events[3] after the last row-histogram
- * launch, events[4] after the last candidate-collect launch and events[5] after the last
- * finalize (exact select, expansion, remap) launch. Inside stream capture the records
+ * launch and events[4] after the last row-select (exact top-k, expansion, remap) launch.
+ * Inside stream capture the records
  * become external event nodes. n == 0 switches tracing off. Calls to sel_select are
  * serialised while tracing state is read.
  */

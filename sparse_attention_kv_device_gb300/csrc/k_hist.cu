@@ -1,11 +1,11 @@
 // K-c0: level-1 histograms for the radix top-k.
 //
 // For every row that selects pools (ctx > index_topk), counts its complete pools' scores
-// by the top 11 bits of their order-preserving 32-bit keys. CTA (x, y) takes kHistSlice
-// consecutive pools of row y, counts them with shared-memory atomics, then adds each
-// non-zero bin to the row's global counters (zeroed by the segment builder). The top-k
-// kernel that follows reads the finished histogram and goes straight to the bin that
-// holds the K-th largest score.
+// by the top 11 bits of their order-preserving 32-bit keys (the scorer stores the keys).
+// CTA (x, y) takes kHistSlice consecutive pools of row y, counts them with shared-memory
+// atomics, then adds each non-zero bin to the row's global counters (zeroed by the
+// segment builder). The row select kernel that follows reads the finished histogram and
+// goes straight to the bin that holds the K-th largest score.
 #include "sel_device.cuh"
 #include "sel_kernels.h"
 
@@ -30,9 +30,9 @@ __global__ void __launch_bounds__(kHistThreads) k_row_histogram(const HistArgs a
     if (s0 >= P) return;
     const int n = static_cast<int>(P - s0 < kHistSlice ? P - s0 : kHistSlice);
     for (int b = tid; b < kTopkBins; b += kHistThreads) h[b] = 0;
-    const float4* src = reinterpret_cast<const float4*>(a.scores + static_cast<int64_t>(rl) * a.scores_ld + s0);
+    const uint4* src = reinterpret_cast<const uint4*>(a.keys + static_cast<int64_t>(rl) * a.keys_ld + s0);
     constexpr int kVec = kHistSlice / 4 / kHistThreads;
-    float4 v[kVec];
+    uint4 v[kVec];
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         const int i4 = tid + j * kHistThreads;
@@ -43,10 +43,10 @@ __global__ void __launch_bounds__(kHistThreads) k_row_histogram(const HistArgs a
     for (int j = 0; j < kVec; ++j) {
         const int i = 4 * (tid + j * kHistThreads);
         if (i < n) {
-            atomicAdd(&h[ordered_key(v[j].x) >> 21], 1u);
-            if (i + 1 < n) atomicAdd(&h[ordered_key(v[j].y) >> 21], 1u);
-            if (i + 2 < n) atomicAdd(&h[ordered_key(v[j].z) >> 21], 1u);
-            if (i + 3 < n) atomicAdd(&h[ordered_key(v[j].w) >> 21], 1u);
+            atomicAdd(&h[v[j].x >> 21], 1u);
+            if (i + 1 < n) atomicAdd(&h[v[j].y >> 21], 1u);
+            if (i + 2 < n) atomicAdd(&h[v[j].z >> 21], 1u);
+            if (i + 3 < n) atomicAdd(&h[v[j].w >> 21], 1u);
         }
     }
     __syncthreads();

@@ -13,9 +13,11 @@
 //     fp32 accumulate) with the keys as A and the segment's queries as B, into one
 //     of two TMEM accumulators;
 //   * four epilogue warps read the accumulator (one TMEM lane = one pool per thread),
-//     add each row's 4 head columns, and store the row scores coalesced;
-//   * every CTA takes an even share of all segments' tiles (segments may change
-//     inside a CTA's share, so the queries are double-buffered too).
+//     add each row's 4 head columns, and store the row scores coalesced (for the fused
+//     selection, the scores' order-preserving 32-bit keys instead);
+//   * every CTA takes a static share of the segments' tiles, and the rest through an
+//     atomic tile counter (segments may change inside a CTA's work, so the queries are
+//     double-buffered too).
 // Pools on key pages whose id is out of range score -inf and raise SEL_ST_KEYPAGE_OOB.
 #include "sel_device.cuh"
 #include "sel_kernels.h"
@@ -365,7 +367,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     const float h2 = __uint_as_float(v[4 * rr + 2]);
                     const float h3 = __uint_as_float(v[4 * rr + 3]);
                     const float sc = page_ok ? ((h0 + h1) + h2) + h3 : -__int_as_float(0x7f800000);
-                    if (okp) out[static_cast<int64_t>(r) * a.scores_ld] = sc;
+                    if (okp) {
+                        if (a.as_keys)
+                            reinterpret_cast<uint32_t*>(out)[static_cast<int64_t>(r) * a.scores_ld] = ordered_key(sc);
+                        else
+                            out[static_cast<int64_t>(r) * a.scores_ld] = sc;
+                    }
                 }
             }
             tc_fence_before();

@@ -125,7 +125,7 @@ struct Plan {
     int chunk_rows = 1, seg_rows = 1, max_segs = 1, max_tiles = 1;
     int64_t max_pools = 0, scores_ld = 4;
     size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0, off_tiles = 0,
-           off_scores = 0, off_hist = 0, off_rowsel = 0, off_cand = 0;
+           off_scores = 0, off_hist = 0;
     int64_t hist_words = 0;
     size_t ws_score = 0, ws_select = 0;
     int npad_max = 16, stages = 2;
@@ -134,8 +134,17 @@ struct Plan {
     TopkPlan topk;
     int sms = 0;
     int bm_words = 1;
-    size_t fin_smem = 0;
+    int stage_cap = 0;  // keys of a row the select kernel stages in shared memory
+    size_t sel_smem = 0;
 };
+
+// log2(v) when v is a power of two, else -1
+int log2_if_pow2(int v) {
+    if (v < 1 || (v & (v - 1)) != 0) return -1;
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
 
 int check_problem(const sel_problem* p) {
     if (!p) return SEL_EINVAL;
@@ -199,14 +208,10 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->ws_score = off;
     pl->off_scores = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
-    // per-row histograms followed by per-row candidate counts: one region the builder zeroes
+    // per-row level-1 histograms (zeroed by the builder)
     pl->off_hist = off;
-    pl->hist_words = (static_cast<int64_t>(pl->chunk_rows) * (kTopkBins + 1) + 3) & ~int64_t(3);
+    pl->hist_words = static_cast<int64_t>(pl->chunk_rows) * kTopkBins;
     off = align256(off + sizeof(uint32_t) * static_cast<size_t>(pl->hist_words));
-    pl->off_rowsel = off;
-    off = align256(off + sizeof(int2) * static_cast<size_t>(pl->chunk_rows));
-    pl->off_cand = off;
-    off = align256(off + sizeof(uint2) * static_cast<size_t>(pl->chunk_rows) * kSelCandCap);
     pl->bm_words = static_cast<int>((pl->max_pools + 31) / 32);
     pl->ws_select = off;
 
@@ -220,14 +225,20 @@ int make_plan(const sel_problem* p, Plan* pl) {
         --pl->stages;
     pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max);
     if ((rc = plan_topk(p->max_context, p->block_size, true, di.max_smem_optin, &pl->topk)) != SEL_OK) return rc;
-    pl->fin_smem = finalize_smem_bytes(kSelCandCap, pl->bm_words, pl->topk.bt_cap);
-    if (pl->fin_smem > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    // the select kernel stages as many of a row's keys as fit (longer rows read the rest from L2)
+    const int K = p->index_topk / p->kpool;
+    pl->stage_cap = static_cast<int>(std::min<int64_t>(kSelectMaxStage, (pl->max_pools + 3) & ~int64_t(3)));
+    const size_t fixed_sel = select_smem_bytes(0, pl->bm_words, K, pl->topk.bt_cap);
+    if (fixed_sel > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    const int64_t fit = ((static_cast<int64_t>(di.max_smem_optin) - static_cast<int64_t>(fixed_sel)) / 4) & ~int64_t(3);
+    pl->stage_cap = static_cast<int>(std::min<int64_t>(pl->stage_cap, fit));
+    pl->sel_smem = select_smem_bytes(pl->stage_cap, pl->bm_words, K, pl->topk.bt_cap);
     return SEL_OK;
 }
 
 // ------------------------------------------------------------------ tracing
 std::mutex g_trace_mu;
-constexpr int kTraceEvents = 6;
+constexpr int kTraceEvents = 5;
 cudaEvent_t g_trace[kTraceEvents] = {};
 int g_trace_n = 0;
 
@@ -251,9 +262,6 @@ struct Ws {
     int4* tiles;
     float* scores;
     uint32_t* hist;
-    uint32_t* row_count;
-    int2* row_sel;
-    uint2* cand;
 };
 
 Ws carve_ws(void* ws, const Plan& pl) {
@@ -267,9 +275,6 @@ Ws carve_ws(void* ws, const Plan& pl) {
     w.tiles = reinterpret_cast<int4*>(b + pl.off_tiles);
     w.scores = reinterpret_cast<float*>(b + pl.off_scores);
     w.hist = reinterpret_cast<uint32_t*>(b + pl.off_hist);
-    w.row_count = w.hist + static_cast<int64_t>(pl.chunk_rows) * kTopkBins;
-    w.row_sel = reinterpret_cast<int2*>(b + pl.off_rowsel);
-    w.cand = reinterpret_cast<uint2*>(b + pl.off_cand);
     return w;
 }
 
@@ -321,6 +326,7 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     a.pool_cap = b.pool_cap;
     a.scores = scores;
     a.scores_ld = ld;
+    a.as_keys = score_all ? 0 : 1;  // the fused selection (score_all = 0) works on ordered keys
     a.npad_max = pl.npad_max;
     a.stages = pl.stages;
     a.tmem_cols = pl.tmem_cols;
@@ -468,54 +474,42 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, w.hist, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
+        const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);
         HistArgs h{};
-        h.scores = w.scores;
-        h.scores_ld = pl.scores_ld;
+        h.keys = keys;
+        h.keys_ld = pl.scores_ld;
         h.row_ctx = w.row_ctx;
         h.topk = p->index_topk;
         h.kpool = p->kpool;
         h.hist = w.hist;
         if (launch_hist(h, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
         if (last) trace_record(3, s);
-        CollectArgs ca{};
-        ca.scores = w.scores;
-        ca.scores_ld = pl.scores_ld;
-        ca.row_ctx = w.row_ctx;
-        ca.topk = p->index_topk;
-        ca.kpool = p->kpool;
-        ca.hist = w.hist;
-        ca.row_count = w.row_count;
-        ca.row_sel = w.row_sel;
-        ca.cand = w.cand;
-        ca.cand_cap = kSelCandCap;
-        if (launch_collect(ca, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
+        RowSelectArgs ra{};
+        ra.keys = keys;
+        ra.keys_ld = pl.scores_ld;
+        ra.row_ctx = w.row_ctx;
+        ra.row_req = w.row_req;
+        ra.hist = w.hist;
+        ra.stage_cap = pl.stage_cap;
+        ra.bm_words = pl.bm_words;
+        ra.bt_cap = pl.topk.bt_cap;
+        ra.row_begin = c0;
+        ra.topk = p->index_topk;
+        ra.kpool = p->kpool;
+        ra.out_width = out_width;
+        ra.kpool_shift = log2_if_pow2(p->kpool);
+        ra.bs_shift = log2_if_pow2(p->block_size);
+        ra.slots = slots;
+        ra.token_idx = token_idx;
+        ra.counts = valid_counts;
+        ra.block_table = p->block_table;
+        ra.bt_ld = p->bt_ld;
+        ra.max_blocks = p->max_blocks_per_req;
+        ra.num_kv_blocks = p->num_kv_blocks;
+        ra.block_size = p->block_size;
+        ra.block_stride_rows = p->block_stride_rows;
+        if (launch_select_rows(ra, c1 - c0, pl.sel_smem, true, s) != cudaSuccess) return SEL_ECUDA;
         if (last) trace_record(4, s);
-        FinalizeArgs fa{};
-        fa.scores = w.scores;
-        fa.scores_ld = pl.scores_ld;
-        fa.row_ctx = w.row_ctx;
-        fa.row_req = w.row_req;
-        fa.row_count = w.row_count;
-        fa.row_sel = w.row_sel;
-        fa.cand = w.cand;
-        fa.cand_cap = kSelCandCap;
-        fa.bm_words = pl.bm_words;
-        fa.bt_cap = pl.topk.bt_cap;
-        fa.row_begin = c0;
-        fa.topk = p->index_topk;
-        fa.kpool = p->kpool;
-        fa.out_width = out_width;
-        fa.slots = slots;
-        fa.token_idx = token_idx;
-        fa.counts = valid_counts;
-        fa.block_table = p->block_table;
-        fa.bt_ld = p->bt_ld;
-        fa.max_blocks = p->max_blocks_per_req;
-        fa.num_kv_blocks = p->num_kv_blocks;
-        fa.block_size = p->block_size;
-        fa.block_stride_rows = p->block_stride_rows;
-        if (launch_finalize(fa, c1 - c0, pl.fin_smem, true, s) != cudaSuccess) return SEL_ECUDA;
-        if (last) trace_record(5, s);
     }
     return SEL_OK;
 }
@@ -523,7 +517,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
 int32_t sel_select_launch_count(const sel_problem* p) {
     Plan pl;
     if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
-    return static_cast<int32_t>(5 * ceil_div(p->num_rows, pl.chunk_rows));
+    return static_cast<int32_t>(4 * ceil_div(p->num_rows, pl.chunk_rows));
 }
 
 size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {

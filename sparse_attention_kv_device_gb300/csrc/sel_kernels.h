@@ -50,6 +50,7 @@ struct ScoreArgs {
     int32_t topk, kpool, score_all, pool_cap;
     float* scores;           // chunk-local rows
     int64_t scores_ld;
+    int32_t as_keys;         // 1: store ordered_key(score) (uint32 bits) instead of the fp32 score
     int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
     int32_t stages;
     uint32_t tmem_cols;      // TMEM columns allocated (power of two)
@@ -57,42 +58,31 @@ struct ScoreArgs {
     int32_t* status;
 };
 
-// Level-1 histogram of every row's scores (top 11 bits of the order-preserving keys),
-// accumulated into zeroed per-row counters: CTA (x, y) counts keys [x*kHistSlice, ...) of row y.
+// Level-1 histogram of every row's keys (their top 11 bits), accumulated into zeroed
+// per-row counters: CTA (x, y) counts keys [x*kHistSlice, ...) of row y.
 struct HistArgs {
-    const float* scores;       // chunk-local rows
-    int64_t scores_ld;
+    const uint32_t* keys;      // chunk-local rows (the scorer's ordered keys)
+    int64_t keys_ld;
     const int32_t* row_ctx;    // chunk-local (builder output)
     int32_t topk, kpool;
     uint32_t* hist;            // [rows][kTopkBins]
 };
 
-// Collect the keys at or above each row's threshold bin (CTA = kHistSlice pools of a row).
-struct CollectArgs {
-    const float* scores;       // chunk-local rows
-    int64_t scores_ld;
-    const int32_t* row_ctx;
-    int32_t topk, kpool;
-    const uint32_t* hist;      // [rows][kTopkBins]
-    uint32_t* row_count;       // [rows] zeroed by the builder; candidates appended
-    int2* row_sel;             // [rows] (threshold bin b1, rank inside it)
-    uint2* cand;               // [rows][cand_cap] (key, pool)
-    int32_t cand_cap;
-};
-
-// Exact select among a row's candidates, ordered write-out with expansion and remap.
-struct FinalizeArgs {
-    const float* scores;       // chunk-local rows (re-read only for crowded ties)
-    int64_t scores_ld;
-    const int32_t* row_ctx;
-    const int32_t* row_req;
-    const uint32_t* row_count;
-    const int2* row_sel;
-    const uint2* cand;
-    int32_t cand_cap, bm_words, bt_cap;
+// Per-row exact top-k pools, expansion and remap on the scorer's keys (one CTA per row).
+struct RowSelectArgs {
+    const uint32_t* keys;      // chunk-local rows: ordered_key of every complete pool's score
+    int64_t keys_ld;
+    const int32_t* row_ctx;    // chunk-local (builder output)
+    const int32_t* row_req;    // chunk-local (builder output)
+    const uint32_t* hist;      // chunk-local rows x kTopkBins level-1 histograms
+    int32_t stage_cap;         // keys staged in shared memory per row (multiple of 4)
+    int32_t bm_words;          // bitmap words per row, >= ceil(max pools / 32)
+    int32_t bt_cap;            // block-table entries staged in shared memory per row
     int32_t row_begin;
     int32_t topk, kpool, out_width;
-    int32_t* slots;            // global rows
+    int32_t kpool_shift;       // log2(kpool) when kpool is a power of two, else -1
+    int32_t bs_shift;          // log2(block_size) when block_size is a power of two, else -1
+    int32_t* slots;            // [rows][out_width] global rows
     int32_t* token_idx;        // nullable
     int32_t* counts;           // nullable
     const int32_t* block_table;
@@ -145,9 +135,9 @@ constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin liste
 constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
 constexpr int kHistThreads = 256;
-constexpr int kCollectThreads = 256;   // 8 histogram bins and 8 pools per thread
-constexpr int kFinalizeThreads = 512;
-constexpr int kSelCandCap = 4096;      // candidates kept per row
+constexpr int kSelectThreads = 1024;
+constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
+constexpr int kSelectListCap = 2048;    // keys of the threshold bin listed in shared memory
 constexpr int kHistSlice = 2048;     // keys counted per histogram CTA
 
 size_t score_smem_bytes(int stages, int npad_max);
@@ -162,8 +152,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_remap(const RemapArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_hist(const HistArgs& a, int rows, int64_t max_pools, bool pdl, cudaStream_t s);
-cudaError_t launch_collect(const CollectArgs& a, int rows, int64_t max_pools, bool pdl, cudaStream_t s);
-size_t finalize_smem_bytes(int cand_cap, int bm_words, int bt_cap);
-cudaError_t launch_finalize(const FinalizeArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
+size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
+cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
 
 }  // namespace sel
