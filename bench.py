@@ -294,7 +294,7 @@ def run_ours(args):
     ok_status = int(status.item())
 
     # ---- per-kernel times from trace events captured into a second graph
-    trace = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    trace = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     sel.sel_set_trace_events(trace)
     try:
         tgraph = torch.cuda.CUDAGraph()
@@ -303,20 +303,20 @@ def run_ours(args):
     finally:
         sel.sel_set_trace_events(None)
     n_tr = min(args.steps, 100)
-    parts = np.zeros((n_tr, 4))
+    parts = np.zeros((n_tr, 3))
     with torch.cuda.stream(stream):
         for i in range(n_tr):
             flush()
             tgraph.replay()
             stream.synchronize()
-            parts[i] = [trace[j].elapsed_time(trace[j + 1]) for j in range(4)]
-    kern_ms = parts.mean(axis=0)   # builder, scorer, row histogram, row select
+            parts[i] = [trace[j].elapsed_time(trace[j + 1]) for j in range(3)]
+    kern_ms = parts.mean(axis=0)   # builder, scorer, selection tail
 
     ab = algorithmic_bytes(w)
     peak, peak_kind = measured_peaks()
-    names = ["k_build_segments", "k_score_segments", "k_row_histogram", "k_select_rows"]
+    names = ["k_build_segments", "k_score_segments", "k_row_histogram+k_select_rows"]
     dom = int(np.argmax(kern_ms))
-    dom_bytes = [w.num_rows * 8 + (w.num_reqs + 1) * 4, ab["scorer"], 0, ab["topk_out"]][dom]
+    dom_bytes = [w.num_rows * 8 + (w.num_reqs + 1) * 4, ab["scorer"], ab["topk_out"]][dom]
     achieved = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
     traffic = recorded_traffic("k_score.cu", args.config) if dom == 1 else None
     step_gbs = ab["step"] / (total_ms / args.steps * 1e-3) / 1e9

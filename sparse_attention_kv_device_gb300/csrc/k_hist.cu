@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(kHistThreads) k_row_histogram(const HistArgs a
     if (threadIdx.x == 0 && cta < 128) SEL_PHASE(128 + cta);           // diagnostics: dependency met
     const int tid = threadIdx.x;
     const int rl = blockIdx.y;
-    const int32_t c = a.row_ctx[rl];
+    const int32_t c = __ldcg(a.row_ctx + rl);
     if (c <= a.topk) return;  // short rows and rows without output select no pools
     const int64_t P = c / a.kpool;
     const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kHistSlice;

@@ -80,7 +80,7 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
 
 // Pools a row may score: its complete pools, when the row needs scoring.
 __device__ __forceinline__ int row_pool_limit(const ScoreArgs& a, int row) {
-    const int32_t c = __ldg(a.row_ctx + row - a.row_begin);
+    const int32_t c = __ldcg(a.row_ctx + row - a.row_begin);
     return (c > 0 && (a.score_all || c > a.topk)) ? min(c / a.kpool, a.pool_cap) : 0;
 }
 
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ scheduler + TMA producer
         if (lane == 0) {
-            const int total = a.hdr[1];
+            const int total = __ldcg(a.hdr + 1);
             const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
             const int dyn0 = share * static_cast<int>(gridDim.x);
             int s_next = static_cast<int>(blockIdx.x) * share;
@@ -156,9 +156,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             };
             // two tiles ahead: their ids and records are in flight while the current one is issued
             int t_a = grab();
-            int4 r_a = t_a >= 0 ? a.tiles[t_a] : make_int4(0, 0, 0, 0);
+            int4 r_a = t_a >= 0 ? __ldcg(a.tiles + t_a) : make_int4(0, 0, 0, 0);
             int t_b = t_a >= 0 ? grab() : -1;
-            int4 r_b = t_b >= 0 ? a.tiles[t_b] : make_int4(0, 0, 0, 0);
+            int4 r_b = t_b >= 0 ? __ldcg(a.tiles + t_b) : make_int4(0, 0, 0, 0);
 
             const uint64_t pol_k = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 r_a = r_b;
                 if (t_a >= 0) {
                     t_b = grab();
-                    if (t_b >= 0) r_b = a.tiles[t_b];
+                    if (t_b >= 0) r_b = __ldcg(a.tiles + t_b);
                 } else {
                     t_b = -1;
                 }
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 if (rec.x != cur) {
                     // the segment's queries, after its first key tile is on its way
-                    const int4 sd = a.seg[rec.x];
+                    const int4 sd = __ldcg(a.seg + rec.x);
                     qb ^= 1;
                     if ((qb ? q_uses1 : q_uses0) > 0) {
                         if (!mbar_wait(&sm.qempty[qb], (qe_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (rec.x != cur) {
                     // the previous segment's queries are free once its MMAs complete
                     if (cur >= 0) umma_commit(&sm.qempty[qb]);
-                    const int4 sd = a.seg[rec.x];
+                    const int4 sd = __ldcg(a.seg + rec.x);
                     qb ^= 1;
                     if (!mbar_wait(&sm.qfull[qb], (qf_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
                     qf_phase ^= 1u << qb;
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(&sm.sempty[slot]);
             if (t < 0) break;
             if (rec.x != cur) {
-                sd = a.seg[rec.x];
+                sd = __ldcg(a.seg + rec.x);
                 lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
                 lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
                 cur = rec.x;

@@ -14,17 +14,15 @@
 //       before this grid can start) and its block-table entries are copied into shared
 //       memory with cp.async, so the copies overlap the histogram kernel;
 //   after it: level 1 reads the finished histogram and finds the bin b1 that holds the
-//       K-th largest key. One sweep over the staged keys then marks every pool whose bin
-//       is above b1 in a bitmap, and lists the keys of bin b1 (a few hundred for real
-//       scores) in shared memory while counting them by bits 20..10 (level 2). Level 3
-//       (bits 9..0) and the marks of the pools above and at the exact threshold key work
-//       on that list alone. One block scan over the bitmap words ranks the kept pools in
-//       ascending order into a list, which is written out one column per thread
-//       (coalesced), expanded and remapped.
-// Rows longer than the staging capacity read the rest of their keys from global memory
-// (L2). When bin b1 holds more keys than the list takes (massive ties), levels 3 and the
-// threshold marks sweep the row again instead; equal keys are ranked by a scan over their
-// bitmap either way.
+//       K-th largest key. One sweep over the staged keys (one compare for each key below
+//       bin b1, about 97% of them) sets the bit of every pool above b1 in a kept bitmap
+//       and of every pool in b1 in a second bitmap, and counts bin b1's keys by bits
+//       20..10 (level 2), with fire-and-forget shared-memory atomics only. Level 3 (bits
+//       9..0) and the marks at the exact threshold key visit only the bin-b1 bits, each
+//       thread on its own run of bitmap words. One block scan over the words then ranks the
+//       kept pools in ascending order into a list, which is written out one column per
+//       thread (coalesced), expanded and remapped. Massive ties take the same path.
+// Rows longer than the staging capacity read the rest of their keys from global memory (L2).
 #include "sel_device.cuh"
 #include "sel_kernels.h"
 
@@ -35,7 +33,6 @@ SEL_PHASE_TABLE(select)
 namespace {
 
 constexpr int T = kSelectThreads;
-constexpr int kWarps = T / 32;
 static_assert(T * 2 == kTopkBins, "level 1 holds two histogram bins per thread");
 static_assert(T == 1024, "level 3 holds one of its 1024 bins per thread");
 
@@ -43,13 +40,12 @@ struct SelSmem {
     uint32_t* keys;     // [stage_cap] the row's keys
     uint32_t* hist;     // [kTopkBins] level-2 counts
     uint32_t* hist3;    // [1024] level-3 counts
-    uint2* blist;       // [kSelectListCap] (key, pool) of the keys in bin b1
     uint32_t* gbm;      // [bm_words] pools whose key is above the threshold
     uint32_t* ebm;      // [bm_words] pools whose key equals it
     int32_t* list;      // [K] kept pools, ascending
     int32_t* btab;      // [bt_cap] the row's block-table entries
     uint32_t* scratch;  // [64]
-    uint32_t* res;      // [8]; res[4] counts the keys of bin b1
+    uint32_t* res;      // [8]
 };
 
 __device__ __forceinline__ int pad4(int n) { return (n + 3) & ~3; }
@@ -59,8 +55,7 @@ __device__ __forceinline__ SelSmem carve_sel(uint32_t* base, int stage_cap, int 
     s.keys = base;
     s.hist = s.keys + pad4(stage_cap);
     s.hist3 = s.hist + kTopkBins;
-    s.blist = reinterpret_cast<uint2*>(s.hist3 + 1024);
-    s.gbm = reinterpret_cast<uint32_t*>(s.blist + kSelectListCap);
+    s.gbm = s.hist3 + 1024;
     s.ebm = s.gbm + pad4(bm_words);
     s.list = reinterpret_cast<int32_t*>(s.ebm + pad4(bm_words));
     s.btab = s.list + pad4(K);
@@ -96,32 +91,8 @@ __device__ __forceinline__ void find_bin_desc(const uint32_t (&h)[n], uint32_t f
     krem = sm.res[1];
 }
 
-// Four keys of the row: staged in shared memory below vector ns4, else from global memory.
-__device__ __forceinline__ uint4 keys4(const SelSmem& sm, const uint32_t* krow, int i4, int ns4) {
-    return i4 < ns4 ? reinterpret_cast<const uint4*>(sm.keys)[i4] : __ldcg(reinterpret_cast<const uint4*>(krow) + i4);
-}
-
 __device__ __forceinline__ uint32_t key_at(const SelSmem& sm, const uint32_t* krow, int p, int ns4) {
     return p < 4 * ns4 ? sm.keys[p] : __ldcg(krow + p);
-}
-
-// Calls f(pool, key) for every pool of the row whose key k has pred(k) (the slow path).
-template <class Pred, class F>
-__device__ __forceinline__ void sweep(const SelSmem& sm, const uint32_t* krow, int P, int ns4, Pred&& pred, F&& f) {
-    const int full4 = P >> 2;
-    for (int i4 = threadIdx.x; i4 < full4; i4 += T) {
-        const uint4 v = keys4(sm, krow, i4, ns4);
-        if (pred(v.x)) f(4 * i4 + 0, v.x);
-        if (pred(v.y)) f(4 * i4 + 1, v.y);
-        if (pred(v.z)) f(4 * i4 + 2, v.z);
-        if (pred(v.w)) f(4 * i4 + 3, v.w);
-    }
-    const int tail = P - 4 * full4;
-    if (static_cast<int>(threadIdx.x) < tail) {
-        const int p = 4 * full4 + threadIdx.x;
-        const uint32_t k = key_at(sm, krow, p, ns4);
-        if (pred(k)) f(p, k);
-    }
 }
 
 __device__ __forceinline__ int32_t slot_of(const RowSelectArgs& a, const int32_t* btab, int nblk, const int32_t* bt_row,
@@ -143,7 +114,7 @@ __device__ __forceinline__ int32_t slot_of(const RowSelectArgs& a, const int32_t
 
 __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSelectArgs a) {
     extern __shared__ __align__(16) uint32_t ssm[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int rl = blockIdx.x;
     const int r = a.row_begin + rl;
     const int K = a.topk / a.kpool;
@@ -194,7 +165,6 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
             sm.gbm[w] = 0;
             sm.ebm[w] = 0;
         }
-        if (tid == 0) sm.res[4] = 0;
         const uint32_t h1[2] = {hv.y, hv.x};
         uint32_t b1, k1;
         find_bin_desc<2>(h1, kTopkBins - 1 - 2 * tid, static_cast<uint32_t>(K), sm, b1, k1);
@@ -202,50 +172,50 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         __syncthreads();
         if (trace) SEL_PHASE(tb + 2);
 
-        // ---- the one full sweep: bins above b1 are kept; bin b1 is listed and counted by
-        //      bits 20..10. Warp-uniform trip count, so the warp can ballot.
-        const uint32_t lanes_below = (1u << lane) - 1u;
-        const int full4 = P >> 2;
-        for (int base = warp * 32; base < full4; base += T) {
-            const int i4 = base + lane;
-            const bool ok = i4 < full4;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (ok) v = keys4(sm, krow, i4, ns4);
-            const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+        // ---- the one full sweep: keys below bin b1 (nearly all of them) cost a compare each.
+        //      A thread first records which of its next 32 keys are at or above b1 in a mask,
+        //      then visits those few together with the other lanes (not one lane at a time):
+        //      a key above b1 sets its pool's bit in the kept bitmap, a key in b1 sets its
+        //      bit in the bin-b1 bitmap (ebm, until the marks below) and counts by bits 20..10.
+        const uint32_t lo1 = b1 << 21;
+        {
+            const int full4 = P >> 2;
+            const uint4* ks = reinterpret_cast<const uint4*>(sm.keys);
+            const uint4* kg = reinterpret_cast<const uint4*>(krow);
+            for (int base = 0; base < full4; base += 8 * T) {
+                uint32_t hits = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t k = kk[u], bin = k >> 21;
-                const int p = 4 * i4 + u;
-                if (ok && bin > b1) atomicOr(&sm.gbm[p >> 5], 1u << (p & 31));
-                const bool inb = ok && bin == b1;
-                const uint32_t m = __ballot_sync(0xffffffffu, inb);
-                if (m) {  // uniform over the warp
-                    const int leader = __ffs(m) - 1;
-                    uint32_t at = 0;
-                    if (lane == leader) at = atomicAdd(&sm.res[4], static_cast<uint32_t>(__popc(m)));
-                    at = __shfl_sync(0xffffffffu, at, leader) + __popc(m & lanes_below);
-                    if (inb) {
-                        atomicAdd(&sm.hist[(k >> 10) & 2047u], 1u);
-                        if (at < static_cast<uint32_t>(kSelectListCap)) sm.blist[at] = make_uint2(k, p);
+                for (int j = 0; j < 8; ++j) {
+                    const int i4 = base + j * T + tid;
+                    if (i4 < full4) {
+                        const uint4 v = i4 < ns4 ? ks[i4] : __ldcg(kg + i4);
+                        hits |= ((v.x >= lo1 ? 1u : 0u) | (v.y >= lo1 ? 2u : 0u) | (v.z >= lo1 ? 4u : 0u) |
+                                 (v.w >= lo1 ? 8u : 0u))
+                                << (4 * j);
                     }
                 }
+                while (hits) {
+                    const int h = __ffs(hits) - 1;
+                    hits &= hits - 1;
+                    const int p = 4 * (base + (h >> 2) * T + tid) + (h & 3);
+                    const uint32_t k = key_at(sm, krow, p, ns4);
+                    const bool in_b1 = (k >> 21) == b1;
+                    atomicOr((in_b1 ? sm.ebm : sm.gbm) + (p >> 5), 1u << (p & 31));
+                    if (in_b1) atomicAdd(&sm.hist[(k >> 10) & 2047u], 1u);
+                }
             }
-        }
-        {
             const int tail = P - 4 * full4;
             if (tid < tail) {
                 const int p = 4 * full4 + tid;
-                const uint32_t k = key_at(sm, krow, p, ns4), bin = k >> 21;
-                if (bin > b1) atomicOr(&sm.gbm[p >> 5], 1u << (p & 31));
-                if (bin == b1) {
-                    atomicAdd(&sm.hist[(k >> 10) & 2047u], 1u);
-                    const uint32_t at = atomicAdd(&sm.res[4], 1u);
-                    if (at < static_cast<uint32_t>(kSelectListCap)) sm.blist[at] = make_uint2(k, p);
+                const uint32_t k = key_at(sm, krow, p, ns4);
+                if (k >= lo1) {
+                    const bool in_b1 = (k >> 21) == b1;
+                    atomicOr((in_b1 ? sm.ebm : sm.gbm) + (p >> 5), 1u << (p & 31));
+                    if (in_b1) atomicAdd(&sm.hist[(k >> 10) & 2047u], 1u);
                 }
             }
         }
         __syncthreads();
-        const uint32_t n1 = sm.res[4];
         uint32_t b2, k2;
         {
             const uint32_t h2[2] = {sm.hist[kTopkBins - 1 - 2 * tid], sm.hist[kTopkBins - 2 - 2 * tid]};
@@ -253,17 +223,19 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         }
         if (trace) SEL_PHASE(tb + 3);
 
-        // ---- level 3 and the marks at the threshold: on the list, or (list overflow) on the row
+        // ---- level 3 and the marks at the threshold, on the bin-b1 keys of the bitmap words
+        //      this thread also ranks below (a contiguous run of words per thread)
+        const int per = (nwords + T - 1) / T;
+        const int w0 = tid * per, w1 = min(nwords, w0 + per);
         const uint32_t pre22 = (b1 << 11) | b2;
-        const bool listed = n1 <= static_cast<uint32_t>(kSelectListCap);
-        if (listed) {
-            for (uint32_t g = tid; g < n1; g += T) {
-                const uint32_t k = sm.blist[g].x;
+        for (int w = w0; w < w1; ++w) {
+            uint32_t m = sm.ebm[w];
+            while (m) {
+                const int p = w * 32 + __ffs(m) - 1;
+                m &= m - 1;
+                const uint32_t k = key_at(sm, krow, p, ns4);
                 if ((k >> 10) == pre22) atomicAdd(&sm.hist3[k & 1023u], 1u);
             }
-        } else {
-            sweep(sm, krow, P, ns4, [pre22](uint32_t k) { return (k >> 10) == pre22; },
-                  [&](int, uint32_t k) { atomicAdd(&sm.hist3[k & 1023u], 1u); });
         }
         __syncthreads();
         uint32_t b3, need_eq;
@@ -274,24 +246,23 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         const uint32_t thr = (pre22 << 10) | b3;
         const uint32_t n_eq = sm.hist3[b3];
         if (trace) SEL_PHASE(tb + 4);
-        auto mark = [&](int p, uint32_t k) {
-            atomicOr(k == thr ? &sm.ebm[p >> 5] : &sm.gbm[p >> 5], 1u << (p & 31));
-        };
-        if (listed) {
-            for (uint32_t g = tid; g < n1; g += T) {
-                const uint2 e = sm.blist[g];
-                if (e.x >= thr) mark(static_cast<int>(e.y), e.x);
+        for (int w = w0; w < w1; ++w) {
+            uint32_t m = sm.ebm[w], gt = 0, eq = 0;
+            while (m) {
+                const int bit = __ffs(m) - 1;
+                m &= m - 1;
+                const uint32_t k = key_at(sm, krow, w * 32 + bit, ns4);
+                if (k > thr) gt |= 1u << bit;
+                else if (k == thr) eq |= 1u << bit;
             }
-        } else {  // bins above b1 are marked already; marking them again changes nothing
-            sweep(sm, krow, P, ns4, [thr](uint32_t k) { return k >= thr; }, mark);
+            sm.gbm[w] |= gt;
+            sm.ebm[w] = eq;  // from here on: the pools equal to the threshold
         }
         __syncthreads();
         if (trace) SEL_PHASE(tb + 5);
 
         // ---- kept pools in ascending order: all above the threshold and the first need_eq
-        //      equal ones; thread t ranks a contiguous run of bitmap words
-        const int per = (nwords + T - 1) / T;
-        const int w0 = tid * per, w1 = min(nwords, w0 + per);
+        //      equal ones
         uint32_t tot;
         if (n_eq > need_eq) {  // ties at the threshold: rank the equal keys (uniform branch)
             uint32_t eqc = 0;
@@ -361,7 +332,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
 
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap) {
     auto p4 = [](int64_t n) { return static_cast<size_t>((n + 3) & ~int64_t(3)); };
-    return 4 * (p4(stage_cap) + kTopkBins + 1024 + 2 * static_cast<size_t>(kSelectListCap) + 2 * p4(bm_words) +
+    return 4 * (p4(stage_cap) + kTopkBins + 1024 + 2 * p4(bm_words) +
                 p4(K) + p4(bt_cap) + 64 + 8);
 }
 

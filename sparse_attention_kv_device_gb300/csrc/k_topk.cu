@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     bool valid = true;
     int64_t ctx;
     if (a.row_ctx) {
-        const int32_t c = a.row_ctx[rl];
+        const int32_t c = __ldcg(a.row_ctx + rl);
         valid = c >= 0;
         ctx = c;
     } else {
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     }
     int req = 0;
     if (REMAP) {
-        req = a.row_req[rl];
+        req = __ldcg(a.row_req + rl);
         valid = valid && req >= 0;
     }
     const int K = a.topk / a.kpool;

@@ -238,7 +238,7 @@ int make_plan(const sel_problem* p, Plan* pl) {
 
 // ------------------------------------------------------------------ tracing
 std::mutex g_trace_mu;
-constexpr int kTraceEvents = 5;
+constexpr int kTraceEvents = 4;
 cudaEvent_t g_trace[kTraceEvents] = {};
 int g_trace_n = 0;
 
@@ -475,6 +475,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
         const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);
+
         HistArgs h{};
         h.keys = keys;
         h.keys_ld = pl.scores_ld;
@@ -483,7 +484,6 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         h.kpool = p->kpool;
         h.hist = w.hist;
         if (launch_hist(h, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
-        if (last) trace_record(3, s);
         RowSelectArgs ra{};
         ra.keys = keys;
         ra.keys_ld = pl.scores_ld;
@@ -509,7 +509,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         ra.block_size = p->block_size;
         ra.block_stride_rows = p->block_stride_rows;
         if (launch_select_rows(ra, c1 - c0, pl.sel_smem, true, s) != cudaSuccess) return SEL_ECUDA;
-        if (last) trace_record(4, s);
+        if (last) trace_record(3, s);
     }
     return SEL_OK;
 }

@@ -137,7 +137,6 @@ constexpr int kRemapThreads = 128;
 constexpr int kHistThreads = 256;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
-constexpr int kSelectListCap = 2048;    // keys of the threshold bin listed in shared memory
 constexpr int kHistSlice = 2048;     // keys counted per histogram CTA
 
 size_t score_smem_bytes(int stages, int npad_max);

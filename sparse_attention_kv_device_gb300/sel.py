@@ -329,7 +329,7 @@ def sel_select_host(problem: Problem, slots_host, counts_host, stage, ws, status
 
 
 def sel_set_trace_events(events) -> None:
-    """events: five torch.cuda.Event(enable_timing=True), or None to switch tracing off."""
+    """events: four torch.cuda.Event(enable_timing=True), or None to switch tracing off."""
     if not events:
         _check(_lib.sel_set_trace_events(None, 0), "sel_set_trace_events")
         return
