@@ -7,10 +7,7 @@
 //   row_req / row_ctx  per row (-1 ctx = no output: padding, out of bound, bad table)
 //   seg[]              {request, first row, rows (<= seg_rows), pools to score}
 //   seg_tile_prefix[]  exclusive prefix of ceil(pools / 128) over segments
-//   tiles[]            one record per 128-pool tile: {segment, tile in segment,
-//                      key page of pools 0-63, key page of pools 64-127}; a page id
-//                      is -1 when out of range and -2 when the tile has no second page
-//   hdr                {segments, tiles}
+//   hdr                {segments, tiles, 0 (the scorer's tile counter)}
 // The inputs are staged in shared memory when they fit (generic pointers fall back
 // to the global workspace copies otherwise), so the CTA pays few memory round trips.
 #include "sel_device.cuh"
@@ -141,10 +138,6 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
             const int4 d = make_int4(i, row0, nrows, pools);
             seg[s] = d;
             if (a.smem_segs) a.seg[s] = d;
-            // warm L2 with the key-page-table entries the tile records will read
-            const int npages = min((pools + kPagePools - 1) / kPagePools, a.max_key_pages);
-            const int32_t* kpt_row = a.key_page_table + static_cast<int64_t>(i) * a.kpt_ld;
-            for (int pg = 0; pg < npages; pg += 32) prefetch_l2(kpt_row + pg);
         }
         carry += total;
         __syncthreads();
@@ -166,7 +159,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
         tcarry += total;
         __syncthreads();
     }
-    const int ntiles = min(static_cast<int>(tcarry), a.max_tiles);
+    const int ntiles = static_cast<int>(tcarry);
     if (tid == 0) {
         prefix[nseg] = static_cast<int32_t>(tcarry);
         if (a.smem_segs) a.seg_tile_prefix[nseg] = static_cast<int32_t>(tcarry);
@@ -175,27 +168,6 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
         a.hdr[2] = 0;
         SEL_PHASE(4);
         SEL_PHASE_CLK(36);
-    }
-    __syncthreads();
-
-    // 5. one record per tile with its key pages (all page-table reads happen here).
-    for (int t = tid; t < ntiles; t += blockDim.x) {
-        const int s = last_le(prefix, nseg, t);
-        const int4 d = seg[s];
-        const int lt = t - prefix[s];
-        int pg0 = -1, pg1 = -2;  // -1: page id out of range; -2: the tile has no second page
-        if (2 * lt < a.max_key_pages) {
-            const int p = __ldg(a.key_page_table + static_cast<int64_t>(d.x) * a.kpt_ld + 2 * lt);
-            pg0 = (p >= 0 && p < a.num_key_pages) ? p : -1;
-        }
-        if (lt * kTilePools + kPagePools < d.w) {
-            pg1 = -1;
-            if (2 * lt + 1 < a.max_key_pages) {
-                const int p = __ldg(a.key_page_table + static_cast<int64_t>(d.x) * a.kpt_ld + 2 * lt + 1);
-                pg1 = (p >= 0 && p < a.num_key_pages) ? p : -1;
-            }
-        }
-        a.tiles[t] = make_int4(s, lt, pg0, pg1);
     }
 #ifdef SEL_PHASE_TRACE
     __syncthreads();

@@ -33,6 +33,8 @@ constexpr int kSchedRing = 16;  // tiles published ahead by the producer (> stag
 struct ScoreSmem {
     uint8_t* a;          // stages x kTileBytes (keys)
     uint8_t* q;          // 2 x npad_max x 256 B (queries, two K halves each)
+    int4* segs;          // [max_segs] the chunk's segments {request, first row, rows, pools}
+    int* prefix;         // [max_segs + 1] exclusive prefix of their tiles
     int4* rec_ring;      // [kSchedRing] tile records in the order this CTA processes them
     int* tile_ring;      // [kSchedRing] tile ids (-1: no more tiles)
     uint64_t* full;      // [stages]
@@ -49,7 +51,7 @@ struct ScoreSmem {
     int* oob_flag;
 };
 
-__device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_max) {
+__device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_max, int max_segs) {
     ScoreSmem s;
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + (((base + 1023u) & ~1023u) - base);
@@ -57,6 +59,10 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
     p += static_cast<size_t>(stages) * kTileBytes;
     s.q = p;
     p += 2u * static_cast<size_t>(npad_max) * 256u;
+    s.segs = reinterpret_cast<int4*>(p);
+    p += static_cast<size_t>(max_segs) * sizeof(int4);
+    s.prefix = reinterpret_cast<int*>(p);
+    p += ((static_cast<size_t>(max_segs) + 1) * sizeof(int) + 15) & ~size_t(15);
     s.rec_ring = reinterpret_cast<int4*>(p);
     p += kSchedRing * sizeof(int4);
     s.tile_ring = reinterpret_cast<int*>(p);
@@ -94,7 +100,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                      const __grid_constant__ CUtensorMap tmap_q) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ScoreSmem sm = carve(smem_raw, a.stages, a.npad_max);
+    ScoreSmem sm = carve(smem_raw, a.stages, a.npad_max, a.max_segs);
     const uint32_t qhalf_bytes = static_cast<uint32_t>(a.npad_max) * 128u;
     // diagnostics: CTA 0 and CTA gridDim/2 stamp their phases (slot bases 0 and 150)
     const int trace_base = blockIdx.x == 0 ? 0 : (blockIdx.x == gridDim.x / 2 ? 150 : -1);
@@ -143,10 +149,32 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ scheduler + TMA producer
+        // the builder's segments and tile prefix, staged once by the whole warp: every slot
+        // up to max_segs is loaded together with the header (entries past the builder's
+        // segment count are never used), so the loads overlap
+        const int nseg_raw = __ldcg(a.hdr + 0);
+        for (int i = lane; i < a.max_segs; i += 32) sm.segs[i] = __ldcg(a.seg + i);
+        for (int i = lane; i <= a.max_segs; i += 32) sm.prefix[i] = __ldcg(a.seg_tile_prefix + i);
+        const int nseg = min(nseg_raw, a.max_segs);
+        __syncwarp();
+        const int total = sm.prefix[nseg];
+        const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
+        const int dyn0 = share * static_cast<int>(gridDim.x);
+        {
+            // warm L2 with the page-table entries of this CTA's static share (one line per lane)
+            const int t = static_cast<int>(blockIdx.x) * share + lane * 8;
+            if (lane * 8 < share && t < total) {
+                int s = 0;
+                for (int lo = 0, hi = nseg - 1; lo <= hi;) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sm.prefix[mid] <= t) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
+                }
+                const int lt = t - sm.prefix[s];
+                if (2 * lt < a.max_key_pages)
+                    prefetch_l2(a.key_page_table + static_cast<int64_t>(sm.segs[s].x) * a.kpt_ld + 2 * lt);
+            }
+        }
         if (lane == 0) {
-            const int total = __ldcg(a.hdr + 1);
-            const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
-            const int dyn0 = share * static_cast<int>(gridDim.x);
             int s_next = static_cast<int>(blockIdx.x) * share;
             const int s_end = s_next + share;
             auto grab = [&]() -> int {
@@ -154,11 +182,49 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 const int t = dyn0 + atomicAdd(a.hdr + 2, 1);
                 return t < total ? t : -1;
             };
-            // two tiles ahead: their ids and records are in flight while the current one is issued
-            int t_a = grab();
-            int4 r_a = t_a >= 0 ? __ldcg(a.tiles + t_a) : make_int4(0, 0, 0, 0);
-            int t_b = t_a >= 0 ? grab() : -1;
-            int4 r_b = t_b >= 0 ? __ldcg(a.tiles + t_b) : make_int4(0, 0, 0, 0);
+            // A tile's record {segment, tile in segment, key page 0, key page 1}. Its two
+            // page-table loads are issued when the tile is taken (two tiles ahead of its
+            // TMA), and checked only when it is issued, so their latency is hidden.
+            struct Pending {
+                int t, seg, lt;
+                int p0, p1;            // raw page-table entries
+                bool has0, second, has1;
+            };
+            int cur_s = 0;  // the static share ascends: the search usually starts here
+            auto take = [&](int t) -> Pending {
+                Pending r;
+                r.t = t;
+                r.seg = 0;
+                r.lt = 0;
+                r.p0 = r.p1 = -1;
+                r.has0 = r.second = r.has1 = false;
+                if (t < 0) return r;
+                int lo = sm.prefix[cur_s] <= t ? cur_s : 0, hi = nseg - 1;
+                while (lo < hi) {  // last segment whose first tile is <= t
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (sm.prefix[mid] <= t) lo = mid; else hi = mid - 1;
+                }
+                cur_s = lo;
+                const int4 d = sm.segs[lo];
+                r.seg = lo;
+                r.lt = t - sm.prefix[lo];
+                const int32_t* kpt_row = a.key_page_table + static_cast<int64_t>(d.x) * a.kpt_ld;
+                r.has0 = 2 * r.lt < a.max_key_pages;
+                if (r.has0) r.p0 = __ldg(kpt_row + 2 * r.lt);
+                r.second = r.lt * kTilePools + kPagePools < d.w;
+                r.has1 = r.second && 2 * r.lt + 1 < a.max_key_pages;
+                if (r.has1) r.p1 = __ldg(kpt_row + 2 * r.lt + 1);
+                return r;
+            };
+            // -1: page id out of range; -2: the tile has no second page
+            auto record = [&](const Pending& r) -> int4 {
+                const int pg0 = r.has0 && r.p0 >= 0 && r.p0 < a.num_key_pages ? r.p0 : -1;
+                const int pg1 = !r.second ? -2 : (r.has1 && r.p1 >= 0 && r.p1 < a.num_key_pages ? r.p1 : -1);
+                return make_int4(r.seg, r.lt, pg0, pg1);
+            };
+            // two tiles ahead: their ids and page-table entries are in flight while the current one is issued
+            Pending t_a = take(grab());
+            Pending t_b = take(t_a.t >= 0 ? grab() : -1);
 
             const uint64_t pol_k = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
@@ -170,16 +236,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             uint32_t loaded = 0, last_parity = 0;  // stages holding a load, parity of their last load
             bool ok = true;
             for (int n = 0; ok; ++n) {
-                const int t = t_a;
-                const int4 rec = r_a;
+                const int t = t_a.t;
+                const int4 rec = t >= 0 ? record(t_a) : make_int4(0, 0, 0, 0);
                 t_a = t_b;
-                r_a = r_b;
-                if (t_a >= 0) {
-                    t_b = grab();
-                    if (t_b >= 0) r_b = __ldcg(a.tiles + t_b);
-                } else {
-                    t_b = -1;
-                }
+                t_b = take(t_a.t >= 0 ? grab() : -1);
                 // publish the tile (or the end) to the MMA thread and the epilogue warps
                 const int slot = n & (kSchedRing - 1);
                 if (!mbar_wait(&sm.sempty[slot], ((n / kSchedRing) & 1) ^ 1u, abort_flag)) { ok = false; break; }
@@ -203,7 +263,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 if (rec.x != cur) {
                     // the segment's queries, after its first key tile is on its way
-                    const int4 sd = __ldcg(a.seg + rec.x);
+                    const int4 sd = sm.segs[rec.x];
                     qb ^= 1;
                     if ((qb ? q_uses1 : q_uses0) > 0) {
                         if (!mbar_wait(&sm.qempty[qb], (qe_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
@@ -261,7 +321,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                 if (rec.x != cur) {
                     // the previous segment's queries are free once its MMAs complete
                     if (cur >= 0) umma_commit(&sm.qempty[qb]);
-                    const int4 sd = __ldcg(a.seg + rec.x);
+                    const int4 sd = sm.segs[rec.x];
                     qb ^= 1;
                     if (!mbar_wait(&sm.qfull[qb], (qf_phase >> qb) & 1u, abort_flag)) { ok = false; break; }
                     qf_phase ^= 1u << qb;
@@ -327,7 +387,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (lane == 0) mbar_arrive(&sm.sempty[slot]);
             if (t < 0) break;
             if (rec.x != cur) {
-                sd = __ldcg(a.seg + rec.x);
+                sd = sm.segs[rec.x];
                 lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
                 lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
                 cur = rec.x;
@@ -394,8 +454,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (threadIdx.x == 0 && blockIdx.x < 200) SEL_PHASE(300 + blockIdx.x);  // every CTA's end
 }
 
-size_t score_smem_bytes(int stages, int npad_max) {
+size_t score_smem_bytes(int stages, int npad_max, int max_segs) {
     return 1024 + static_cast<size_t>(stages) * kTileBytes + 2u * static_cast<size_t>(npad_max) * 256u +
+           static_cast<size_t>(max_segs) * sizeof(int4) + (((static_cast<size_t>(max_segs) + 1) * sizeof(int) + 15) & ~size_t(15)) +
            kSchedRing * (sizeof(int4) + sizeof(int)) + (2 * static_cast<size_t>(stages) + 9 + 2 * kSchedRing) * 8 + 64;
 }
 

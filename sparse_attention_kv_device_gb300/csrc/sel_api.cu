@@ -122,9 +122,9 @@ int plan_topk(int64_t max_context, int block_size, bool remap, int max_smem, Top
 }
 
 struct Plan {
-    int chunk_rows = 1, seg_rows = 1, max_segs = 1, max_tiles = 1;
+    int chunk_rows = 1, seg_rows = 1, max_segs = 1;
     int64_t max_pools = 0, scores_ld = 4;
-    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0, off_tiles = 0,
+    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0,
            off_scores = 0, off_hist = 0;
     int64_t hist_words = 0;
     size_t ws_score = 0, ws_select = 0;
@@ -189,8 +189,7 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->max_pools = p->max_context / p->kpool;
     pl->scores_ld = (std::max<int64_t>(pl->max_pools, 1) + 3) & ~int64_t(3);
     const int64_t tiles = static_cast<int64_t>(pl->max_segs) * std::max<int64_t>(1, ceil_div(pl->max_pools, 128));
-    if (tiles > INT32_MAX / 16) return SEL_EUNSUPPORTED;
-    pl->max_tiles = static_cast<int>(tiles);
+    if (tiles > INT32_MAX / 2) return SEL_EUNSUPPORTED;  // tile ids and the tile counter are int32
 
     size_t off = 0;
     pl->off_hdr = off;
@@ -203,8 +202,6 @@ int make_plan(const sel_problem* p, Plan* pl) {
     off = align256(off + sizeof(int4) * pl->max_segs);
     pl->off_prefix = off;
     off = align256(off + sizeof(int32_t) * (pl->max_segs + 1));
-    pl->off_tiles = off;
-    off = align256(off + sizeof(int4) * static_cast<size_t>(pl->max_tiles));
     pl->ws_score = off;
     pl->off_scores = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
@@ -218,12 +215,12 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->npad_max = ((4 * pl->seg_rows + 15) / 16) * 16;
     pl->acc_cols = std::max<uint32_t>(32, next_pow2(static_cast<uint32_t>(pl->npad_max)));
     pl->tmem_cols = 2 * pl->acc_cols;
-    const size_t fixed = score_smem_bytes(0, pl->npad_max);
+    const size_t fixed = score_smem_bytes(0, pl->npad_max, pl->max_segs);
     if (fixed + 2 * 32768 > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
     pl->stages = static_cast<int>(std::min<size_t>(8, (di.max_smem_optin - fixed) / 32768));
-    while (pl->stages > 2 && score_smem_bytes(pl->stages, pl->npad_max) > static_cast<size_t>(di.max_smem_optin))
+    while (pl->stages > 2 && score_smem_bytes(pl->stages, pl->npad_max, pl->max_segs) > static_cast<size_t>(di.max_smem_optin))
         --pl->stages;
-    pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max);
+    pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max, pl->max_segs);
     if ((rc = plan_topk(p->max_context, p->block_size, true, di.max_smem_optin, &pl->topk)) != SEL_OK) return rc;
     // the select kernel stages as many of a row's keys as fit (longer rows read the rest from L2)
     const int K = p->index_topk / p->kpool;
@@ -259,7 +256,6 @@ struct Ws {
     int32_t* row_ctx;
     int4* seg;
     int32_t* prefix;
-    int4* tiles;
     float* scores;
     uint32_t* hist;
 };
@@ -272,7 +268,6 @@ Ws carve_ws(void* ws, const Plan& pl) {
     w.row_ctx = reinterpret_cast<int32_t*>(b + pl.off_row_ctx);
     w.seg = reinterpret_cast<int4*>(b + pl.off_seg);
     w.prefix = reinterpret_cast<int32_t*>(b + pl.off_prefix);
-    w.tiles = reinterpret_cast<int4*>(b + pl.off_tiles);
     w.scores = reinterpret_cast<float*>(b + pl.off_scores);
     w.hist = reinterpret_cast<uint32_t*>(b + pl.off_hist);
     return w;
@@ -300,8 +295,6 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     b.score_all = score_all;
     b.pool_cap = static_cast<int32_t>(std::min<int64_t>(pool_cap, INT32_MAX));
     b.max_segs = pl.max_segs;
-    b.max_tiles = pl.max_tiles;
-    b.tiles = w.tiles;
     b.row_req = w.row_req;
     b.row_ctx = w.row_ctx;
     b.seg = w.seg;
@@ -317,7 +310,12 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     ScoreArgs a{};
     a.seg = w.seg;
     a.hdr = w.hdr;
-    a.tiles = w.tiles;
+    a.seg_tile_prefix = w.prefix;
+    a.key_page_table = p->key_page_table;
+    a.kpt_ld = p->kpt_ld;
+    a.max_key_pages = p->max_key_pages_per_req;
+    a.num_key_pages = p->num_key_pages;
+    a.max_segs = pl.max_segs;
     a.row_ctx = w.row_ctx;
     a.row_begin = c0;
     a.topk = p->index_topk;

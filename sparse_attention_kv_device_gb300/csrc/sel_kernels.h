@@ -11,7 +11,7 @@ namespace sel {
 
 // Segment builder: one CTA turns query_start_loc / positions into per-row request
 // ids and contexts and a list of request segments (<= seg_rows rows of one request)
-// with the number of 128-pool tiles each must score.
+// with the exclusive prefix of the 128-pool tiles each must score.
 struct BuildArgs {
     const int32_t* qsl;        // [num_reqs + 1]
     const int32_t* positions;  // [num_rows]
@@ -24,12 +24,11 @@ struct BuildArgs {
     int32_t topk, kpool, max_context;
     int32_t score_all;  // 1: score every row's complete pools; 0: only rows with ctx > topk
     int32_t pool_cap;   // no row scores more pools than this (the score row length)
-    int32_t max_segs, max_tiles;
+    int32_t max_segs;
     int32_t* row_req;          // [row_end - row_begin]
     int32_t* row_ctx;          // [row_end - row_begin]; -1 = no output (padding, bad row)
     int4* seg;                 // [max_segs] {req, first row, rows, pools to score}
     int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
-    int4* tiles;               // [max_tiles] {segment, tile in segment, page 0, page 1}
     int32_t* hdr;              // [0] segments, [1] tiles, [2] scorer's dynamic-tile counter (set to 0)
     int32_t* status;
     uint32_t* hist;            // per-row level-1 histograms the scorer fills; zeroed here (nullable)
@@ -40,11 +39,15 @@ struct BuildArgs {
     int32_t smem_rows_off, smem_segs_off, smem_prefix_off;
 };
 
-// Segmented scorer (TMA + tcgen05): every CTA scores an even share of all tiles.
+// Segmented scorer (TMA + tcgen05): CTAs take static shares of the tiles, then single
+// tiles from an atomic counter; each CTA resolves a tile's segment and key pages itself.
 struct ScoreArgs {
     const int4* seg;
-    int32_t* hdr;            // [1] tiles; [2] dynamic-tile counter (zeroed by the builder)
-    const int4* tiles;
+    const int32_t* seg_tile_prefix;  // [segments + 1]
+    int32_t* hdr;            // [0] segments, [1] tiles; [2] dynamic-tile counter (zeroed by the builder)
+    const int32_t* key_page_table;
+    int64_t kpt_ld;
+    int32_t max_key_pages, num_key_pages, max_segs;
     const int32_t* row_ctx;  // chunk-local
     int32_t row_begin;
     int32_t topk, kpool, score_all, pool_cap;
@@ -139,7 +142,7 @@ constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
 constexpr int kHistSlice = 2048;     // keys counted per histogram CTA
 
-size_t score_smem_bytes(int stages, int npad_max);
+size_t score_smem_bytes(int stages, int npad_max, int max_segs);
 size_t topk_smem_bytes(int bt_cap);
 
 // Launchers. With `pdl` the kernel is a programmatic dependent of the previous kernel
