@@ -314,7 +314,7 @@ def run_ours(args):
 
     ab = algorithmic_bytes(w)
     peak, peak_kind = measured_peaks()
-    names = ["k_build_segments", "k_score_segments", "k_row_histogram+k_select_rows"]
+    names = ["k_build_segments", "k_score_segments", "k_select_rows"]
     dom = int(np.argmax(kern_ms))
     dom_bytes = [w.num_rows * 8 + (w.num_reqs + 1) * 4, ab["scorer"], ab["topk_out"]][dom]
     achieved = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9

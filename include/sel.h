@@ -231,8 +231,8 @@ int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width
  * Tracing hook. With n >= 4 events (cudaEvent_t handles, created by the caller with
  * timing enabled), every following sel_select records, on `stream`: events[0] before its
  * first segment-builder launch, events[1] after that builder (before the first scorer
- * launch), events[2] after the last scorer launch and events[3] after the last launch of
- * the selection tail (exact top-k, expansion, remap). Inside stream capture the records
+ * launch), events[2] after the last scorer launch and events[3] after the last row-select
+ * launch (exact top-k, expansion, remap). Inside stream capture the records
  * become external event nodes. n == 0 switches tracing off. Calls to sel_select are
  * serialised while tracing state is read.
  */

@@ -36,15 +36,6 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
     __shared__ uint32_t scratch[40];
     pdl_launch_dependents();  // the scorer may start its prologue now
     const int tid = threadIdx.x;
-    if (blockIdx.x > 0) {
-        // zeroing CTAs: clear the level-1 histograms the scorer accumulates into
-        uint4* h = reinterpret_cast<uint4*>(a.hist);
-        const int64_t n4 = a.hist_words >> 2;
-        for (int64_t i = (blockIdx.x - 1) * static_cast<int64_t>(blockDim.x) + tid; i < n4;
-             i += static_cast<int64_t>(gridDim.x - 1) * blockDim.x)
-            h[i] = make_uint4(0, 0, 0, 0);
-        return;
-    }
     if (tid == 0) { SEL_PHASE(0); SEL_PHASE_CLK(32); }
     const int nchunk = a.row_end - a.row_begin;
 
@@ -207,7 +198,7 @@ cudaError_t launch_build(const BuildArgs& in, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured[dev] = static_cast<int>(smem);
     }
-    k_build_segments<<<1 + (a.hist ? a.zero_ctas : 0), kBuildThreads, smem, s>>>(a);
+    k_build_segments<<<1, kBuildThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

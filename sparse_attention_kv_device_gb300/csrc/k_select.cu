@@ -6,23 +6,24 @@
 // the trailing incomplete pool to ascending tokens, remap through the block table, -1 pad,
 // count the non -1 slots.
 //
-// Inputs: the scorer's order-preserving 32-bit keys of each row (ordered_key of the fp32
-// score) and the row's histogram of their top 11 bits from the histogram kernel.
+// Input: the scorer's order-preserving 32-bit key of every complete pool of each row
+// (ordered_key of the fp32 score).
 //
 // One 1024-thread CTA per row:
-//   before the dependency wait: the row's keys (made by the scorer, which has completed
-//       before this grid can start) and its block-table entries are copied into shared
-//       memory with cp.async, so the copies overlap the histogram kernel;
-//   after it: level 1 reads the finished histogram and finds the bin b1 that holds the
-//       K-th largest key. One sweep over the staged keys (one compare for each key below
-//       bin b1, about 97% of them) sets the bit of every pool above b1 in a kept bitmap
-//       and of every pool in b1 in a second bitmap, and counts bin b1's keys by bits
-//       20..10 (level 2), with fire-and-forget shared-memory atomics only. Level 3 (bits
-//       9..0) and the marks at the exact threshold key visit only the bin-b1 bits, each
-//       thread on its own run of bitmap words. One block scan over the words then ranks the
-//       kept pools in ascending order into a list, which is written out one column per
-//       thread (coalesced), expanded and remapped. Massive ties take the same path.
-// Rows longer than the staging capacity read the rest of their keys from global memory (L2).
+//   before the dependency wait: the row's descriptors (made by the segment builder, which
+//       has completed before this grid can start) and its block-table entries, copied into
+//       shared memory with cp.async; the histograms and bitmaps are cleared;
+//   after it: the row's keys are copied into shared memory (cp.async, up to stage_cap of
+//       them; longer rows read the rest from L2) and counted by their top 11 bits (level
+//       1), which gives the bin b1 that holds the K-th largest key. One sweep over the keys
+//       (one compare for each key below bin b1, about 97% of them) sets the bit of every
+//       pool above b1 in a kept bitmap and of every pool in b1 in a second bitmap, and
+//       counts bin b1's keys by bits 20..10 (level 2), with fire-and-forget shared-memory
+//       atomics only. Level 3 (bits 9..0) and the marks at the exact threshold key visit
+//       only the bin-b1 bits, each thread on its own run of bitmap words. One block scan
+//       over the words then ranks the kept pools in ascending order into a list, which is
+//       written out one column per thread (coalesced), expanded and remapped. Massive ties
+//       take the same path.
 #include "sel_device.cuh"
 #include "sel_kernels.h"
 
@@ -38,6 +39,7 @@ static_assert(T == 1024, "level 3 holds one of its 1024 bins per thread");
 
 struct SelSmem {
     uint32_t* keys;     // [stage_cap] the row's keys
+    uint32_t* hist1;    // [kTopkBins] level-1 counts
     uint32_t* hist;     // [kTopkBins] level-2 counts
     uint32_t* hist3;    // [1024] level-3 counts
     uint32_t* gbm;      // [bm_words] pools whose key is above the threshold
@@ -53,7 +55,8 @@ __device__ __forceinline__ int pad4(int n) { return (n + 3) & ~3; }
 __device__ __forceinline__ SelSmem carve_sel(uint32_t* base, int stage_cap, int bm_words, int K, int bt_cap) {
     SelSmem s;
     s.keys = base;
-    s.hist = s.keys + pad4(stage_cap);
+    s.hist1 = s.keys + pad4(stage_cap);
+    s.hist = s.hist1 + kTopkBins;
     s.hist3 = s.hist + kTopkBins;
     s.gbm = s.hist3 + 1024;
     s.ebm = s.gbm + pad4(bm_words);
@@ -143,33 +146,67 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         nblk = static_cast<int>(need < a.bt_cap ? need : a.bt_cap);
         for (int i = tid; i < nblk; i += T) cp_async_4(sm.btab + i, bt_row + i);
     }
-    // key vectors [0, ns4) are staged (padding past P is never read as a key)
-    const int pv = (P + 3) >> 2;
-    const int ns4 = pv < (a.stage_cap >> 2) ? pv : (a.stage_cap >> 2);
-    for (int i = tid; i < ns4; i += T) cp_async_16(sm.keys + 4 * i, krow + 4 * i);
+    // full key vectors [0, ns4) are staged in shared memory; keys past them (a longer row's
+    // rest, the last partial vector) are read from global memory
+    const int ns4 = (P >> 2) < (a.stage_cap >> 2) ? (P >> 2) : (a.stage_cap >> 2);
+    const int nwords = (P + 31) >> 5;
+    if (selects) {
+        for (int i = tid; i < kTopkBins; i += T) {
+            sm.hist1[i] = 0;
+            sm.hist[i] = 0;
+        }
+        sm.hist3[tid] = 0;
+        for (int w = tid; w < nwords; w += T) {
+            sm.gbm[w] = 0;
+            sm.ebm[w] = 0;
+        }
+    }
 
-    pdl_wait();  // the row histograms are complete
+    pdl_wait();  // the scorer's keys are complete
+    __syncthreads();  // every histogram and bitmap word is cleared before any thread counts into it
     if (trace) SEL_PHASE(tb + 1);  // diagnostics: dependency met
 
     uint32_t vcount = 0;
     int64_t run_from = 0;  // columns [col_run, out_width) get tokens run_from .. ctx-1, then -1
     int col_run = 0;
     if (selects) {
-        const int nwords = (P + 31) >> 5;
-        // level 1: thread t holds bins 2047-2t and 2046-2t of the row's histogram
-        const uint2 hv = __ldcg(reinterpret_cast<const uint2*>(a.hist + static_cast<int64_t>(rl) * kTopkBins) +
-                                (kTopkBins / 2 - 1 - tid));
-        for (int i = tid; i < kTopkBins; i += T) sm.hist[i] = 0;
-        sm.hist3[tid] = 0;
-        for (int w = tid; w < nwords; w += T) {
-            sm.gbm[w] = 0;
-            sm.ebm[w] = 0;
+        const int full4 = P >> 2;
+        const uint4* ks = reinterpret_cast<const uint4*>(sm.keys);
+        const uint4* kg = reinterpret_cast<const uint4*>(krow);
+        // level 1: the row's keys, eight vectors per thread loaded together into registers,
+        // stored into shared memory (the first ns4 vectors) and counted by bits 31..21 with
+        // fire-and-forget shared atomics
+        uint4* ksw = reinterpret_cast<uint4*>(sm.keys);
+        auto count1 = [&sm](uint32_t k) { atomicAdd(&sm.hist1[k >> 21], 1u); };
+        for (int base = 0; base < full4; base += 8 * T) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i4 = base + j * T + tid;
+                v[j] = i4 < full4 ? __ldcg(kg + i4) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i4 = base + j * T + tid;
+                if (i4 < full4) {
+                    if (i4 < ns4) ksw[i4] = v[j];
+                    count1(v[j].x);
+                    count1(v[j].y);
+                    count1(v[j].z);
+                    count1(v[j].w);
+                }
+            }
         }
-        const uint32_t h1[2] = {hv.y, hv.x};
+        {
+            // the last partial vector: its keys are read from global memory wherever needed
+            const int tail = P - 4 * full4;
+            if (tid < tail) count1(__ldcg(krow + 4 * full4 + tid));
+        }
+        cp_async_wait_all();  // the block-table entries
+        __syncthreads();
+        const uint32_t h1[2] = {sm.hist1[kTopkBins - 1 - 2 * tid], sm.hist1[kTopkBins - 2 - 2 * tid]};
         uint32_t b1, k1;
         find_bin_desc<2>(h1, kTopkBins - 1 - 2 * tid, static_cast<uint32_t>(K), sm, b1, k1);
-        cp_async_wait_all();
-        __syncthreads();
         if (trace) SEL_PHASE(tb + 2);
 
         // ---- the one full sweep: keys below bin b1 (nearly all of them) cost a compare each.
@@ -179,9 +216,6 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         //      bit in the bin-b1 bitmap (ebm, until the marks below) and counts by bits 20..10.
         const uint32_t lo1 = b1 << 21;
         {
-            const int full4 = P >> 2;
-            const uint4* ks = reinterpret_cast<const uint4*>(sm.keys);
-            const uint4* kg = reinterpret_cast<const uint4*>(krow);
             for (int base = 0; base < full4; base += 8 * T) {
                 uint32_t hits = 0;
 #pragma unroll
@@ -332,7 +366,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
 
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap) {
     auto p4 = [](int64_t n) { return static_cast<size_t>((n + 3) & ~int64_t(3)); };
-    return 4 * (p4(stage_cap) + kTopkBins + 1024 + 2 * p4(bm_words) +
+    return 4 * (p4(stage_cap) + 2 * kTopkBins + 1024 + 2 * p4(bm_words) +
                 p4(K) + p4(bt_cap) + 64 + 8);
 }
 

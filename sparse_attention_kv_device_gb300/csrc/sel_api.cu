@@ -125,8 +125,7 @@ struct Plan {
     int chunk_rows = 1, seg_rows = 1, max_segs = 1;
     int64_t max_pools = 0, scores_ld = 4;
     size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0,
-           off_scores = 0, off_hist = 0;
-    int64_t hist_words = 0;
+           off_scores = 0;
     size_t ws_score = 0, ws_select = 0;
     int npad_max = 16, stages = 2;
     uint32_t acc_cols = 32, tmem_cols = 64;
@@ -205,10 +204,6 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->ws_score = off;
     pl->off_scores = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
-    // per-row level-1 histograms (zeroed by the builder)
-    pl->off_hist = off;
-    pl->hist_words = static_cast<int64_t>(pl->chunk_rows) * kTopkBins;
-    off = align256(off + sizeof(uint32_t) * static_cast<size_t>(pl->hist_words));
     pl->bm_words = static_cast<int>((pl->max_pools + 31) / 32);
     pl->ws_select = off;
 
@@ -257,7 +252,6 @@ struct Ws {
     int4* seg;
     int32_t* prefix;
     float* scores;
-    uint32_t* hist;
 };
 
 Ws carve_ws(void* ws, const Plan& pl) {
@@ -269,13 +263,12 @@ Ws carve_ws(void* ws, const Plan& pl) {
     w.seg = reinterpret_cast<int4*>(b + pl.off_seg);
     w.prefix = reinterpret_cast<int32_t*>(b + pl.off_prefix);
     w.scores = reinterpret_cast<float*>(b + pl.off_scores);
-    w.hist = reinterpret_cast<uint32_t*>(b + pl.off_hist);
     return w;
 }
 
 // Builder + scorer for rows [c0, c1); scores row k of the chunk at scores + k*ld.
 int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int c1, int score_all,
-                         float* scores, int64_t ld, int64_t pool_cap, uint32_t* hist, int32_t* status,
+                         float* scores, int64_t ld, int64_t pool_cap, int32_t* status,
                          const CUtensorMap& tk, const CUtensorMap& tq, cudaStream_t s) {
     BuildArgs b{};
     b.qsl = p->query_start_loc;
@@ -301,9 +294,6 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     b.seg_tile_prefix = w.prefix;
     b.hdr = w.hdr;
     b.status = status;
-    b.hist = hist;
-    b.hist_words = pl.hist_words;
-    b.zero_ctas = static_cast<int32_t>(std::min<int64_t>(32, std::max<int64_t>(1, b.hist_words / 16384)));
     if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
     if (c0 == 0 && !score_all) trace_record(1, s);
 
@@ -378,7 +368,7 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
         const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
         rc = launch_chunk_scoring(p, pl, w, c0, c1, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
-                                  scores_ld, nullptr, st, tk, tq, s);
+                                  scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
     }
     return SEL_OK;
@@ -469,25 +459,16 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
         const bool last = c1 == p->num_rows;
         if (c0 == 0) trace_record(0, s);
-        rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, w.hist, st, tk, tq, s);
+        rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
         const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);
 
-        HistArgs h{};
-        h.keys = keys;
-        h.keys_ld = pl.scores_ld;
-        h.row_ctx = w.row_ctx;
-        h.topk = p->index_topk;
-        h.kpool = p->kpool;
-        h.hist = w.hist;
-        if (launch_hist(h, c1 - c0, pl.max_pools, true, s) != cudaSuccess) return SEL_ECUDA;
         RowSelectArgs ra{};
         ra.keys = keys;
         ra.keys_ld = pl.scores_ld;
         ra.row_ctx = w.row_ctx;
         ra.row_req = w.row_req;
-        ra.hist = w.hist;
         ra.stage_cap = pl.stage_cap;
         ra.bm_words = pl.bm_words;
         ra.bt_cap = pl.topk.bt_cap;
@@ -515,7 +496,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
 int32_t sel_select_launch_count(const sel_problem* p) {
     Plan pl;
     if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
-    return static_cast<int32_t>(4 * ceil_div(p->num_rows, pl.chunk_rows));
+    return static_cast<int32_t>(3 * ceil_div(p->num_rows, pl.chunk_rows));
 }
 
 size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {

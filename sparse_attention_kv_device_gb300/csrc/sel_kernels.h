@@ -31,9 +31,6 @@ struct BuildArgs {
     int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
     int32_t* hdr;              // [0] segments, [1] tiles, [2] scorer's dynamic-tile counter (set to 0)
     int32_t* status;
-    uint32_t* hist;            // per-row level-1 histograms the scorer fills; zeroed here (nullable)
-    int64_t hist_words;
-    int32_t zero_ctas;         // extra CTAs that zero `hist` while CTA 0 builds
     // shared-memory staging plan (filled by launch_build)
     int32_t smem_qsl, smem_rows, smem_segs;
     int32_t smem_rows_off, smem_segs_off, smem_prefix_off;
@@ -61,23 +58,12 @@ struct ScoreArgs {
     int32_t* status;
 };
 
-// Level-1 histogram of every row's keys (their top 11 bits), accumulated into zeroed
-// per-row counters: CTA (x, y) counts keys [x*kHistSlice, ...) of row y.
-struct HistArgs {
-    const uint32_t* keys;      // chunk-local rows (the scorer's ordered keys)
-    int64_t keys_ld;
-    const int32_t* row_ctx;    // chunk-local (builder output)
-    int32_t topk, kpool;
-    uint32_t* hist;            // [rows][kTopkBins]
-};
-
 // Per-row exact top-k pools, expansion and remap on the scorer's keys (one CTA per row).
 struct RowSelectArgs {
     const uint32_t* keys;      // chunk-local rows: ordered_key of every complete pool's score
     int64_t keys_ld;
     const int32_t* row_ctx;    // chunk-local (builder output)
     const int32_t* row_req;    // chunk-local (builder output)
-    const uint32_t* hist;      // chunk-local rows x kTopkBins level-1 histograms
     int32_t stage_cap;         // keys staged in shared memory per row (multiple of 4)
     int32_t bm_words;          // bitmap words per row, >= ceil(max pools / 32)
     int32_t bt_cap;            // block-table entries staged in shared memory per row
@@ -137,10 +123,8 @@ constexpr int kTopkBins = 2048;
 constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin listed per row
 constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
-constexpr int kHistThreads = 256;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
-constexpr int kHistSlice = 2048;     // keys counted per histogram CTA
 
 size_t score_smem_bytes(int stages, int npad_max, int max_segs);
 size_t topk_smem_bytes(int bt_cap);
@@ -153,7 +137,6 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
                          size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_remap(const RemapArgs& a, int rows, cudaStream_t s);
-cudaError_t launch_hist(const HistArgs& a, int rows, int64_t max_pools, bool pdl, cudaStream_t s);
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
 cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
 

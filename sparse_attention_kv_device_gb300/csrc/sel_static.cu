@@ -16,8 +16,8 @@
 // device before any stream capture, so that the look-up is not part of a capture.
 //
 // Zeroing: the launch sequence clears every counter it relies on before use (the segment
-// builder zeroes the tile header and the row histograms of each chunk), so the array
-// needs no clearing between calls.
+// builder resets the tile header and counter of each chunk; the row kernel clears its own
+// shared-memory histograms), so the array needs no clearing between calls.
 //
 // Sharing: all calls on one device share the one array. Two calls whose kernels overlap on
 // the GPU (different streams, no ordering between them) race on it and give wrong results;

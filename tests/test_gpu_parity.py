@@ -356,4 +356,4 @@ def test_trace_events_time_the_kernels():
         sel.sel_set_trace_events(None)
     torch.cuda.synchronize()
     assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
-    assert sel.sel_select_launch_count(prob) == 4   # builder, scorer, row histogram, row select
+    assert sel.sel_select_launch_count(prob) == 3   # builder, scorer, row select
