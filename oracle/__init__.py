@@ -72,6 +72,10 @@ def _load(path: str):
     L.orc_remap_token.argtypes = [I32, P, I32, I32, I32, I64]
     L.orc_remap_token.restype = I64
     L.orc_remap_rows.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I64, P, P]
+    L.orc_remap_ws_rows.argtypes = [P, I32, P, I64, I32, I32, P, P, I32, P, I32, I32, I32, I64, P, P]
+    L.orc_dcp_local_index.argtypes = [I32, I32, I32, I32]
+    L.orc_dcp_local_index.restype = I64
+    L.orc_remap_dcp_rows.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I32, I32, I32, I32, P, P]
     L.orc_select.argtypes = [C.POINTER(_Problem), P, I32, I32, P, P, P, P, P, I64]
     L.orc_select.restype = I32
     L.orc_score_rows.argtypes = [C.POINTER(_Problem), P, I32, P, P, I64]
@@ -153,6 +157,39 @@ def remap_rows(req_id, num_reqs, block_table, max_blocks, num_kv_blocks, token_i
     lib().orc_remap_rows(_p(rq), num_reqs, _p(bt), bt.shape[1], max_blocks, num_kv_blocks,
                          _p(ti), rows, width, block_size, int(block_stride_rows),
                          _p(slots), _p(counts))
+    return slots, counts
+
+
+def remap_ws_rows(req_id, num_reqs, block_table, max_blocks, num_kv_blocks, ws_req, ws_starts,
+                  token_idx, block_size, block_stride_rows):
+    """Remap with a prefill workspace: rows with ws_req >= 0 map t to ws_starts[ws_req] + t;
+    returns (slots int64 [rows, width], counts int32 [rows])."""
+    rq, bt, wr, ws, ti = (_c(req_id, np.int32), _c(block_table, np.int32), _c(ws_req, np.int32),
+                          _c(ws_starts, np.int32), _c(token_idx, np.int32))
+    rows, width = ti.shape
+    slots = np.empty((rows, width), dtype=np.int64)
+    counts = np.empty(rows, dtype=np.int32)
+    lib().orc_remap_ws_rows(_p(rq), num_reqs, _p(bt), bt.shape[1], max_blocks, num_kv_blocks, _p(wr),
+                            _p(ws), ws.size, _p(ti), rows, width, block_size, int(block_stride_rows),
+                            _p(slots), _p(counts))
+    return slots, counts
+
+
+def dcp_local_index(t: int, dcp_size: int, dcp_rank: int, interleave: int) -> int:
+    """Local index of token t on rank dcp_rank, or -1 when another rank owns it."""
+    return int(lib().orc_dcp_local_index(int(t), dcp_size, dcp_rank, interleave))
+
+
+def remap_dcp_rows(req_id, num_reqs, block_table, max_blocks, num_kv_blocks, token_idx, block_size,
+                   dcp_size, dcp_rank, interleave, compact):
+    """One decode-context-parallel rank's slots; returns (slots int64, counts int32)."""
+    rq, bt, ti = _c(req_id, np.int32), _c(block_table, np.int32), _c(token_idx, np.int32)
+    rows, width = ti.shape
+    slots = np.empty((rows, width), dtype=np.int64)
+    counts = np.empty(rows, dtype=np.int32)
+    lib().orc_remap_dcp_rows(_p(rq), num_reqs, _p(bt), bt.shape[1], max_blocks, num_kv_blocks, _p(ti),
+                             rows, width, block_size, dcp_size, dcp_rank, interleave, int(bool(compact)),
+                             _p(slots), _p(counts))
     return slots, counts
 
 

@@ -34,6 +34,10 @@
  *   7. valid count = number of entries that are not -1 ("the count of valid
  *      (non -1) indices per row").
  *
+ * The remap also has the page's two other modes: prefill rows mapped into a prefill
+ * workspace (orc_remap_ws_rows) and a decode-context-parallel rank's filter with optional
+ * compaction to the front (orc_remap_dcp_rows).
+ *
  * Readings where the pages are silent: the score has no weights, ReLU or scale;
  * only complete pools are scored; ties go to the lower pool index; -0.0 equals
  * +0.0; NaN (outside the input contract) ranks below -inf.
@@ -215,6 +219,102 @@ void orc_remap_rows(const int32_t *req_id, int32_t num_reqs, const int32_t *bloc
             slots[(int64_t)r * width + c] = s;
             cnt += (s != -1);
         }
+        if (counts)
+            counts[r] = cnt;
+    }
+}
+
+/* Prefill-workspace remap (vLLM page "sparse_utils", triton_convert_req_index_to_global_index
+ * with HAS_PREFILL_WORKSPACE): prefill rows map their tokens to offsets in a prefill
+ * workspace instead of global cache slots. ws_req[r] is -1 for a decode row (the global
+ * remap above) or the row's prefill request w, whose tokens start at ws_starts[w]:
+ *     out = t == -1 ? -1 : ws_starts[w] + t
+ * The pages give no formula; this is the plainest reading of "mapped to workspace offsets"
+ * with "0-indexed workspace starts for each prefill request". A w outside [-1, num_prefills)
+ * gives an all -1 row (the same guard as an out-of-range request id). */
+void orc_remap_ws_rows(const int32_t *req_id, int32_t num_reqs, const int32_t *block_table,
+                       int64_t bt_ld, int32_t max_blocks, int32_t num_kv_blocks,
+                       const int32_t *ws_req, const int32_t *ws_starts, int32_t num_prefills,
+                       const int32_t *token_idx, int32_t rows, int32_t width,
+                       int32_t block_size, int64_t block_stride_rows, int64_t *slots,
+                       int32_t *counts)
+{
+    for (int32_t r = 0; r < rows; ++r) {
+        int32_t w = ws_req[r];
+        int32_t req = req_id[r];
+        int32_t cnt = 0;
+        for (int32_t c = 0; c < width; ++c) {
+            int32_t t = token_idx[(int64_t)r * width + c];
+            int64_t s = -1;
+            if (w == -1) {
+                if (req >= 0 && req < num_reqs)
+                    s = orc_remap_token(t, block_table + (int64_t)req * bt_ld, max_blocks,
+                                        num_kv_blocks, block_size, block_stride_rows);
+            } else if (w >= 0 && w < num_prefills && t >= 0) {
+                s = (int64_t)ws_starts[w] + t;
+            }
+            slots[(int64_t)r * width + c] = s;
+            cnt += (s != -1);
+        }
+        if (counts)
+            counts[r] = cnt;
+    }
+}
+
+/* Decode context parallelism (vLLM page "sparse_utils", triton_filter_and_convert_dcp_index):
+ * dcp_size ranks each hold part of every request's KV, interleaved in groups of
+ * `interleave` tokens (block_size is a multiple of interleave, so a group never straddles
+ * a block). The page does not print the index formula; the plainest reading of a
+ * round-robin interleave is:
+ *     owner(t) = (t / interleave) % dcp_size
+ *     local(t) = (t / (interleave * dcp_size)) * interleave + t % interleave
+ * i.e. each rank stores its groups back to back. Returns local(t), or -1 when t is -1 or
+ * another rank owns t. */
+int64_t orc_dcp_local_index(int32_t t, int32_t dcp_size, int32_t dcp_rank, int32_t interleave)
+{
+    if (t < 0)
+        return -1;
+    int64_t group = t / interleave;
+    if (group % dcp_size != dcp_rank)
+        return -1;
+    return (group / dcp_size) * interleave + t % interleave;
+}
+
+/* The rank's slots: the local index goes through the rank's own block table, which on the
+ * DCP path is dense (block stride == block size, "dense caches on the DCP path"), with the
+ * same -1 guards as the global remap. Tokens owned by other ranks become -1 ("DCP filtering
+ * marks non-owned slots -1"). With compact != 0 the row's non -1 slots are moved, in
+ * ascending column order, to columns 0 .. count-1 and the rest is -1 (the page: "scatters
+ * this rank's owned slots to a contiguous prefix [0, valid_count) ... Prefix order is
+ * unspecified"; ascending is one valid order). count = number of non -1 entries. */
+void orc_remap_dcp_rows(const int32_t *req_id, int32_t num_reqs, const int32_t *block_table,
+                        int64_t bt_ld, int32_t max_blocks, int32_t num_kv_blocks,
+                        const int32_t *token_idx, int32_t rows, int32_t width, int32_t block_size,
+                        int32_t dcp_size, int32_t dcp_rank, int32_t interleave, int32_t compact,
+                        int64_t *slots, int32_t *counts)
+{
+    for (int32_t r = 0; r < rows; ++r) {
+        int32_t req = req_id[r];
+        int32_t cnt = 0;
+        int64_t *out = slots + (int64_t)r * width;
+        for (int32_t c = 0; c < width; ++c) {
+            int64_t s = -1;
+            int64_t l = orc_dcp_local_index(token_idx[(int64_t)r * width + c], dcp_size, dcp_rank,
+                                            interleave);
+            if (l >= 0 && l <= INT32_MAX && req >= 0 && req < num_reqs)
+                s = orc_remap_token((int32_t)l, block_table + (int64_t)req * bt_ld, max_blocks,
+                                    num_kv_blocks, block_size, block_size);
+            if (compact) {
+                if (s != -1)
+                    out[cnt] = s;
+            } else {
+                out[c] = s;
+            }
+            cnt += (s != -1);
+        }
+        if (compact)
+            for (int32_t c = cnt; c < width; ++c)
+                out[c] = -1;
         if (counts)
             counts[r] = cnt;
     }

@@ -248,7 +248,110 @@ def pin_integer_scores_match_exact(orc):
         assert np.array_equal(sc[r, :P], exact.astype(np.float32))
 
 
+def _golden(name):
+    import _golden
+    return _golden.load(name), _golden.ints
+
+
+def pin_workspace_worked_example(orc):
+    """Hand-worked prefill-workspace fixture (tests/golden/workspace_worked_example.txt)."""
+    d, ints = _golden("workspace_worked_example.txt")
+    toks = np.stack([ints(d, f"tokens_row{r}") for r in range(4)]).astype(np.int32)
+    slots, counts = orc.remap_ws_rows(ints(d, "req_id"), 1, ints(d, "block_table_row0")[None, :],
+                                      int(d["max_blocks"][0]), int(d["num_kv_blocks"][0]), ints(d, "ws_req"),
+                                      ints(d, "ws_starts"), toks, int(d["block_size"][0]), int(d["stride"][0]))
+    for r in range(4):
+        assert np.array_equal(slots[r], ints(d, f"slots_row{r}")), r
+    assert np.array_equal(counts, ints(d, "counts"))
+
+
+def pin_workspace_decode_rows_are_remap(orc, seed=31):
+    """Rows without a prefill request (-1) take exactly the global remap."""
+    rng = np.random.default_rng(seed)
+    bt = rng.permutation(64).astype(np.int32)[:48].reshape(3, 16)
+    toks = rng.integers(-1, 16 * 8, size=(9, 12)).astype(np.int32)
+    req = rng.integers(0, 3, size=9).astype(np.int32)
+    ref = orc.remap_rows(req, 3, bt, 16, 64, toks, 8, 24)
+    got = orc.remap_ws_rows(req, 3, bt, 16, 64, np.full(9, -1, np.int32), np.array([7], np.int32), toks, 8, 24)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def pin_dcp_worked_example(orc):
+    """Hand-worked decode-context-parallel fixture (tests/golden/dcp_worked_example.txt), both
+    ranks, with and without compaction."""
+    d, ints = _golden("dcp_worked_example.txt")
+    toks = np.stack([ints(d, f"tokens_row{r}") for r in range(3)]).astype(np.int32)
+    bt = np.stack([ints(d, "block_table_row0"), ints(d, "block_table_row1")]).astype(np.int32)
+    D, I, B = int(d["dcp_size"][0]), int(d["interleave"][0]), int(d["block_size"][0])
+    mb, nkv = int(d["max_blocks"][0]), int(d["num_kv_blocks"][0])
+    for rank in (0, 1):
+        slots, counts = orc.remap_dcp_rows(ints(d, "req_id"), 2, bt, mb, nkv, toks, B, D, rank, I, False)
+        for r in range(3):
+            assert np.array_equal(slots[r], ints(d, f"rank{rank}_row{r}")), (rank, r)
+        assert np.array_equal(counts, ints(d, f"rank{rank}_counts")), rank
+    slots, counts = orc.remap_dcp_rows(ints(d, "req_id"), 2, bt, mb, nkv, toks, B, D, 0, I, True)
+    for r in range(3):
+        assert np.array_equal(slots[r], ints(d, f"rank0_compact_row{r}")), r
+
+
+def pin_dcp_single_rank_is_remap(orc, seed=33):
+    """One rank owns every token: the filter is the global remap with a dense table."""
+    rng = np.random.default_rng(seed)
+    bt = rng.permutation(80).astype(np.int32)[:60].reshape(3, 20)
+    bt[1, 4] = -3
+    toks = rng.integers(-1, 20 * 16 + 40, size=(10, 16)).astype(np.int32)
+    req = rng.integers(0, 3, size=10).astype(np.int32)
+    ref = orc.remap_rows(req, 3, bt, 20, 70, toks, 16, 16)
+    for inter in (1, 2, 4, 16):
+        got = orc.remap_dcp_rows(req, 3, bt, 20, 70, toks, 16, 1, 0, inter, False)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]), inter
+
+
+def pin_dcp_interleave_partition(orc):
+    """The ranks partition a request's tokens: every token has exactly one owner; a group of
+    `interleave` consecutive tokens shares its owner and any dcp_size consecutive groups have
+    distinct owners (round robin); on each rank the owned tokens, in increasing order, get
+    the local indices 0, 1, 2, ... with no gap."""
+    for D, I in ((2, 1), (2, 2), (3, 4), (4, 8), (8, 2)):
+        n = D * I * 7 + 5
+        owners = np.full(n, -1)
+        local = np.full(n, -1)
+        for rank in range(D):
+            for t in range(n):
+                l = orc.dcp_local_index(t, D, rank, I)
+                if l >= 0:
+                    assert owners[t] == -1, (D, I, t)
+                    owners[t], local[t] = rank, l
+        assert (owners >= 0).all()
+        grp = owners[: (n // I) * I].reshape(-1, I)
+        assert (grp == grp[:, :1]).all()
+        g0 = grp[:, 0]
+        for k in range(len(g0) - D + 1):
+            assert len(set(g0[k:k + D].tolist())) == D
+        for rank in range(D):
+            assert np.array_equal(local[owners == rank], np.arange(int((owners == rank).sum())))
+        assert orc.dcp_local_index(-1, D, 0, I) == -1
+
+
+def pin_dcp_compaction(orc, seed=35):
+    """Compaction moves exactly the non -1 slots of the uncompacted row, in column order, to the
+    front and fills the rest with -1; the counts are unchanged."""
+    rng = np.random.default_rng(seed)
+    bt = rng.permutation(200).astype(np.int32)[:160].reshape(4, 40)
+    toks = rng.integers(-1, 40 * 8 * 2, size=(12, 24)).astype(np.int32)
+    req = rng.integers(0, 4, size=12).astype(np.int32)
+    for D, I, rank in ((2, 4, 1), (4, 2, 3), (3, 8, 0)):
+        a, ca = orc.remap_dcp_rows(req, 4, bt, 40, 200, toks, 8, D, rank, I, False)
+        b, cb = orc.remap_dcp_rows(req, 4, bt, 40, 200, toks, 8, D, rank, I, True)
+        assert np.array_equal(ca, cb)
+        for r in range(12):
+            kept = a[r][a[r] != -1]
+            assert np.array_equal(b[r][:ca[r]], kept) and (b[r][ca[r]:] == -1).all()
+
+
 ALL_PINS = [pin_half_decode, pin_score_integer_exact, pin_score_normal_bound,
             pin_topk_bruteforce, pin_topk_all_zero, pin_topk_stable_argsort,
             pin_expand_closed_form, pin_remap_identity, pin_remap_inverse, pin_remap_guards,
-            pin_planted_winners, pin_pipeline_counts, pin_integer_scores_match_exact]
+            pin_planted_winners, pin_pipeline_counts, pin_integer_scores_match_exact,
+            pin_workspace_worked_example, pin_workspace_decode_rows_are_remap, pin_dcp_worked_example,
+            pin_dcp_single_rank_is_remap, pin_dcp_interleave_partition, pin_dcp_compaction]

@@ -33,6 +33,15 @@ MUTANTS = {
                            "(int64_t)(j / p->key_page_size) * p->dim"),
                           ("(j % p->key_page_size) * p->dim", "(j / p->key_page_size) * p->dim")],
     "kept_pools_not_sorted": [("    qsort(out, (size_t)n, sizeof(int32_t), orc_cmp_int);\n", "")],
+    "workspace_start_ignored": [("s = (int64_t)ws_starts[w] + t;", "s = (int64_t)t;")],
+    "workspace_rows_use_global": [("if (w == -1) {", "if (w >= -1) {")],
+    "dcp_owner_by_token": [("if (group % dcp_size != dcp_rank)", "if (t % dcp_size != dcp_rank)")],
+    "dcp_local_drops_offset": [("return (group / dcp_size) * interleave + t % interleave;",
+                                "return (group / dcp_size) * interleave;")],
+    "dcp_local_not_divided": [("return (group / dcp_size) * interleave + t % interleave;",
+                               "return group * interleave + t % interleave;")],
+    "dcp_table_not_dense": [("num_kv_blocks, block_size, block_size);", "num_kv_blocks, block_size, 2 * block_size);")],
+    "dcp_compact_keeps_columns": [("                    out[cnt] = s;", "                    out[c] = s;")],
 }
 
 
