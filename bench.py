@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--config", default="decode128k", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-remap", action="store_true", help="skip the stand-alone remap measurements")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (profiling runs)")
     return ap.parse_args()
 
@@ -222,6 +223,46 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
+def remap_modes(sel, torch, dev, stream, flush, peak, iters):
+    """The remap kernel's three modes (global slots, prefill workspace, one DCP rank with
+    compaction) on the mixed step's output shape: 4,112 rows x 2,052 tokens (33.8 MB in,
+    33.8 MB out), L2 flushed before each launch, CUDA events on the launching stream."""
+    rows, width, nreq, nb, nkv = 4112, 2052, 17, 2048, 40000
+    rng = np.random.default_rng(77)
+    bt = torch.from_numpy(rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)).to(dev)
+    req = torch.from_numpy(np.minimum(np.arange(rows) // 242, nreq - 1).astype(np.int32)).to(dev)
+    wsr = torch.from_numpy(np.where(np.arange(rows) < 16, -1, np.arange(rows) % 3).astype(np.int32)).to(dev)
+    starts = torch.tensor([0, 1 << 20, 2 << 20], dtype=torch.int32, device=dev)
+    tok = torch.from_numpy(workloads.random_token_indices(rows, width, nb * 64, seed=5)).to(dev)
+    slots = torch.empty((rows, width), dtype=torch.int32, device=dev)
+    counts = torch.empty(rows, dtype=torch.int32, device=dev)
+    calls = {
+        "global": lambda: sel.sel_remap_global(req, bt, tok, slots, num_kv_blocks=nkv, valid_counts=counts,
+                                               stream=stream),
+        "workspace": lambda: sel.sel_remap_workspace(req, bt, wsr, starts, tok, slots, num_kv_blocks=nkv,
+                                                     valid_counts=counts, stream=stream),
+        "dcp_compact": lambda: sel.sel_remap_dcp(req, bt, tok, slots, num_kv_blocks=nkv, dcp_size=4, dcp_rank=1,
+                                                 interleave=16, compact=True, valid_counts=counts, stream=stream),
+    }
+    nbytes = 2 * rows * width * 4 + 3 * rows * 4 + nreq * nb * 4
+    out = {"shape": f"{rows} rows x {width} tokens", "algorithmic_bytes": nbytes}
+    with torch.cuda.stream(stream):
+        for name, call in calls.items():
+            for _ in range(3):
+                call()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            for a, b in ev:
+                flush()
+                a.record(stream)
+                call()
+                b.record(stream)
+            stream.synchronize()
+            ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[name] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -358,6 +399,10 @@ def run_ours(args):
         e2e = {"value": world * rows * args.steps / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
+    remap = None
+    if not args.no_remap:
+        remap = remap_modes(sel, torch, dev, stream, flush, peak, 20)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -391,6 +436,8 @@ def run_ours(args):
             line["e2e"] = e2e
         if cpu:
             line["cpu_baseline"] = cpu
+        if remap:
+            line["remap_modes"] = remap
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

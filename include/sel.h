@@ -177,6 +177,46 @@ int sel_remap_global(const int32_t *req_id, int32_t num_reqs, const int32_t *blo
                      int32_t *valid_counts, sel_stream_t stream);
 
 /*
+ * sel_remap_workspace -- the remap with a prefill workspace (the sparse_utils page,
+ * triton_convert_req_index_to_global_index with HAS_PREFILL_WORKSPACE: prefill tokens
+ * map to workspace offsets instead of global cache slots).
+ * ws_req [num_rows]: -1 for a decode row, which takes sel_remap_global's formula, else the
+ * row's prefill request w, whose tokens start at ws_starts[w] (ws_starts [num_prefills],
+ * 0-indexed). A prefill row writes ws_starts[w] + t for every t >= 0 and -1 for t == -1
+ * (reading: the page names the mapping but prints no formula; the plainest one is taken);
+ * a w outside [-1, num_prefills) gives an all -1 row. ws_starts[w] + t must fit in int32.
+ * valid_counts, columns and the other arguments as in sel_remap_global.
+ */
+int sel_remap_workspace(const int32_t *req_id, int32_t num_reqs, const int32_t *block_table,
+                        int64_t bt_ld, int32_t max_blocks_per_req, int32_t num_kv_blocks,
+                        const int32_t *ws_req, const int32_t *ws_starts, int32_t num_prefills,
+                        const int32_t *token_idx, int32_t num_rows, int32_t width,
+                        int32_t block_size, int64_t block_stride_rows, int32_t *slots,
+                        int32_t *valid_counts, sel_stream_t stream);
+
+/*
+ * sel_remap_dcp -- one decode-context-parallel rank's slots (the sparse_utils page,
+ * triton_filter_and_convert_dcp_index: filter global per-request indices to this rank's
+ * local slots; non-owned slots are -1; optionally compacted to a contiguous prefix).
+ * Tokens are dealt to the dcp_size ranks in groups of `interleave` consecutive tokens,
+ * round robin (reading: the page does not print the formula): token t belongs to rank
+ * (t / interleave) % dcp_size at local index (t / (interleave * dcp_size)) * interleave +
+ * t % interleave. An owned token's slot is block_table[q * bt_ld + l / block_size] *
+ * block_size + l % block_size for its local index l (this rank's dense cache), with the
+ * -1 guards of sel_remap_global; tokens of other ranks are -1. compact != 0 moves the
+ * row's non -1 slots, in ascending column order, to columns 0 .. count-1 and writes -1 to
+ * the rest (the page leaves the prefix order unspecified; no atomics are used here).
+ * valid_counts[r] (optional) = number of non -1 slots. Requires 1 <= dcp_size,
+ * 0 <= dcp_rank < dcp_size, interleave >= 1 and block_size % interleave == 0 (an
+ * interleave group never straddles a block), plus sel_remap_global's requirements.
+ */
+int sel_remap_dcp(const int32_t *req_id, int32_t num_reqs, const int32_t *block_table,
+                  int64_t bt_ld, int32_t max_blocks_per_req, int32_t num_kv_blocks,
+                  const int32_t *token_idx, int32_t num_rows, int32_t width, int32_t block_size,
+                  int32_t dcp_size, int32_t dcp_rank, int32_t interleave, int32_t compact,
+                  int32_t *slots, int32_t *valid_counts, sel_stream_t stream);
+
+/*
  * sel_select -- the fused path: segment builder, segmented scorer, top-k with
  * expansion and remap, per chunk of chunk_rows rows, all queued on `stream`.
  * slots [num_rows][out_width]: the remapped slots of each row's selected tokens in

@@ -324,6 +324,40 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     return SEL_OK;
 }
 
+// Validates the arguments every remap mode shares and fills them in.
+int remap_args(const int32_t* req_id, int32_t num_reqs, const int32_t* block_table, int64_t bt_ld,
+               int32_t max_blocks_per_req, int32_t num_kv_blocks, const int32_t* token_idx, int32_t num_rows,
+               int32_t width, int32_t block_size, int64_t block_stride_rows, int32_t* slots, int32_t* valid_counts,
+               RemapArgs* a) {
+    if (num_rows < 0 || width < 0 || num_reqs < 0 || block_size < 1 || block_stride_rows < block_size)
+        return SEL_EINVAL;
+    if (max_blocks_per_req < 0 || max_blocks_per_req > bt_ld || num_kv_blocks < 0) return SEL_EINVAL;
+    if (num_kv_blocks > 0 && static_cast<int64_t>(num_kv_blocks - 1) * block_stride_rows + block_size > INT32_MAX)
+        return SEL_EINVAL;
+    if (num_rows == 0) return SEL_OK;
+    if (!req_id || !block_table || !token_idx || !slots) return SEL_EINVAL;
+    if (width % 4 != 0) return SEL_EINVAL;
+    if (!aligned16(token_idx) || !aligned16(slots)) return SEL_EUNSUPPORTED;
+    a->req_id = req_id;
+    a->num_reqs = num_reqs;
+    a->block_table = block_table;
+    a->bt_ld = bt_ld;
+    a->max_blocks = max_blocks_per_req;
+    a->num_kv_blocks = num_kv_blocks;
+    a->block_size = block_size;
+    a->block_stride_rows = block_stride_rows;
+    a->token_idx = token_idx;
+    a->width = width;
+    a->slots = slots;
+    a->counts = valid_counts;
+    a->dcp_size = 1;
+    a->interleave = 1;
+    a->bs_shift = log2_if_pow2(block_size);
+    a->il_shift = 0;
+    a->dcp_shift = 0;
+    return SEL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -413,29 +447,55 @@ int sel_remap_global(const int32_t* req_id, int32_t num_reqs, const int32_t* blo
                      int32_t max_blocks_per_req, int32_t num_kv_blocks, const int32_t* token_idx,
                      int32_t num_rows, int32_t width, int32_t block_size, int64_t block_stride_rows,
                      int32_t* slots, int32_t* valid_counts, sel_stream_t stream) {
-    if (num_rows < 0 || width < 0 || num_reqs < 0 || block_size < 1 || block_stride_rows < block_size)
-        return SEL_EINVAL;
-    if (max_blocks_per_req < 0 || max_blocks_per_req > bt_ld || num_kv_blocks < 0) return SEL_EINVAL;
-    if (num_kv_blocks > 0 && static_cast<int64_t>(num_kv_blocks - 1) * block_stride_rows + block_size > INT32_MAX)
+    RemapArgs a{};
+    const int rc = remap_args(req_id, num_reqs, block_table, bt_ld, max_blocks_per_req, num_kv_blocks, token_idx,
+                              num_rows, width, block_size, block_stride_rows, slots, valid_counts, &a);
+    if (rc != SEL_OK || num_rows == 0) return rc;
+    return launch_remap(a, num_rows, kRemapGlobal, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
+}
+
+int sel_remap_workspace(const int32_t* req_id, int32_t num_reqs, const int32_t* block_table, int64_t bt_ld,
+                        int32_t max_blocks_per_req, int32_t num_kv_blocks, const int32_t* ws_req,
+                        const int32_t* ws_starts, int32_t num_prefills, const int32_t* token_idx, int32_t num_rows,
+                        int32_t width, int32_t block_size, int64_t block_stride_rows, int32_t* slots,
+                        int32_t* valid_counts, sel_stream_t stream) {
+    RemapArgs a{};
+    const int rc = remap_args(req_id, num_reqs, block_table, bt_ld, max_blocks_per_req, num_kv_blocks, token_idx,
+                              num_rows, width, block_size, block_stride_rows, slots, valid_counts, &a);
+    if (rc != SEL_OK) return rc;
+    if (num_prefills < 0) return SEL_EINVAL;
+    if (num_rows == 0) return SEL_OK;
+    if (!ws_req || (num_prefills > 0 && !ws_starts)) return SEL_EINVAL;
+    a.ws_req = ws_req;
+    a.ws_starts = ws_starts;
+    a.num_prefills = num_prefills;
+    return launch_remap(a, num_rows, kRemapWorkspace, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
+}
+
+int sel_remap_dcp(const int32_t* req_id, int32_t num_reqs, const int32_t* block_table, int64_t bt_ld,
+                  int32_t max_blocks_per_req, int32_t num_kv_blocks, const int32_t* token_idx, int32_t num_rows,
+                  int32_t width, int32_t block_size, int32_t dcp_size, int32_t dcp_rank, int32_t interleave,
+                  int32_t compact, int32_t* slots, int32_t* valid_counts, sel_stream_t stream) {
+    RemapArgs a{};
+    const int rc = remap_args(req_id, num_reqs, block_table, bt_ld, max_blocks_per_req, num_kv_blocks, token_idx,
+                              num_rows, width, block_size, block_size, slots, valid_counts, &a);
+    if (rc != SEL_OK) return rc;
+    if (dcp_size < 1 || dcp_rank < 0 || dcp_rank >= dcp_size || interleave < 1 || block_size % interleave != 0)
         return SEL_EINVAL;
     if (num_rows == 0) return SEL_OK;
-    if (!req_id || !block_table || !token_idx || !slots) return SEL_EINVAL;
-    if (width % 4 != 0) return SEL_EINVAL;
-    if (!aligned16(token_idx) || !aligned16(slots)) return SEL_EUNSUPPORTED;
-    RemapArgs a{};
-    a.req_id = req_id;
-    a.num_reqs = num_reqs;
-    a.block_table = block_table;
-    a.bt_ld = bt_ld;
-    a.max_blocks = max_blocks_per_req;
-    a.num_kv_blocks = num_kv_blocks;
-    a.block_size = block_size;
-    a.block_stride_rows = block_stride_rows;
-    a.token_idx = token_idx;
-    a.width = width;
-    a.slots = slots;
-    a.counts = valid_counts;
-    return launch_remap(a, num_rows, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    a.dcp_size = dcp_size;
+    a.dcp_rank = dcp_rank;
+    a.interleave = interleave;
+    a.il_shift = log2_if_pow2(interleave);
+    a.dcp_shift = log2_if_pow2(dcp_size);
+    a.compact = compact ? 1 : 0;
+    return launch_remap(a, num_rows, kRemapDcp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
 }
 
 int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,

@@ -294,16 +294,5 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// One token through a request's block-table row (the sparse_utils remap):
-// -1 for t < 0, a logical block past max_blocks, or a physical id outside [0, nkv).
-__device__ __forceinline__ int32_t remap_token(int32_t t, const int32_t* __restrict__ bt_row, int32_t max_blocks,
-                                               int32_t nkv, int32_t block_size, int64_t stride) {
-    if (t < 0) return -1;
-    const int32_t b = t / block_size;
-    if (b >= max_blocks) return -1;
-    const int32_t ph = __ldg(bt_row + b);
-    if (ph < 0 || ph >= nkv) return -1;
-    return static_cast<int32_t>(static_cast<int64_t>(ph) * stride + (t - b * block_size));
-}
 
 }  // namespace sel

@@ -114,7 +114,18 @@ struct RemapArgs {
     int32_t width;
     int32_t* slots;
     int32_t* counts;
+    // prefill-workspace mode: ws_req[row] -1 = decode row (global remap), else the row's
+    // prefill request, whose tokens map to ws_starts[ws_req[row]] + t
+    const int32_t* ws_req;
+    const int32_t* ws_starts;
+    int32_t num_prefills;
+    // decode-context-parallel mode: this rank's tokens only, through its dense block table
+    int32_t dcp_size, dcp_rank, interleave, compact;
+    // log2 of block_size, interleave and dcp_size when powers of two, else -1 (divisions)
+    int32_t bs_shift, il_shift, dcp_shift;
 };
+
+enum RemapMode { kRemapGlobal = 0, kRemapWorkspace = 1, kRemapDcp = 2 };
 
 constexpr int kBuildThreads = 1024;
 constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
@@ -136,7 +147,7 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
                          size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
-cudaError_t launch_remap(const RemapArgs& a, int rows, cudaStream_t s);
+cudaError_t launch_remap(const RemapArgs& a, int rows, RemapMode mode, cudaStream_t s);
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
 cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
 

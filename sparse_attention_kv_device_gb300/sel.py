@@ -69,6 +69,8 @@ def _load():
     lib.sel_score_paged.argtypes = [PP, P, I64, P, P, SZ, P]
     lib.sel_topk_expand.argtypes = [P, I64, P, I32, I32, I32, P, I32, P, P, P]
     lib.sel_remap_global.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I64, P, P, P]
+    lib.sel_remap_workspace.argtypes = [P, I32, P, I64, I32, I32, P, P, I32, P, I32, I32, I32, I64, P, P, P]
+    lib.sel_remap_dcp.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I32, I32, I32, I32, P, P, P]
     lib.sel_select.argtypes = [PP, P, I32, P, P, P, P, SZ, P]
     lib.sel_select_static.argtypes = [PP, P, I32, P, P, P, P]
     lib.sel_host_stage_bytes.argtypes = [PP, I32]
@@ -77,7 +79,8 @@ def _load():
     lib.sel_set_trace_events.argtypes = [C.POINTER(C.c_void_p), I32]
     lib.sel_select_launch_count.argtypes = [PP]
     lib.sel_select_launch_count.restype = I32
-    for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
+    for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
+              "sel_select",
               "sel_select_static", "sel_select_host", "sel_set_trace_events"):
         getattr(lib, f).restype = C.c_int
     return lib
@@ -86,7 +89,8 @@ def _load():
 _lib = _load()
 
 EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_workspace_bytes",
-           "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_select",
+           "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
+           "sel_select",
            "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
            "sel_select_launch_count"]
 
@@ -280,6 +284,42 @@ def sel_remap_global(req_id, block_table, token_idx, slots, *, num_kv_blocks, bl
                                  int(block_table.shape[1]), int(mb), int(num_kv_blocks), _ptr(token_idx),
                                  int(rows), int(width), int(block_size), int(stride), _ptr(slots),
                                  _ptr(valid_counts), _stream(stream)), "sel_remap_global")
+    return slots, valid_counts
+
+
+def sel_remap_workspace(req_id, block_table, ws_req, ws_starts, token_idx, slots, *, num_kv_blocks, block_size=64,
+                        block_stride_rows=None, max_blocks_per_req=None, valid_counts=None, stream=None):
+    """sel_remap_global, with rows of prefill requests (ws_req >= 0) mapped to ws_starts[ws_req] + t."""
+    for t, n in ((req_id, "req_id"), (block_table, "block_table"), (ws_req, "ws_req"), (ws_starts, "ws_starts"),
+                 (token_idx, "token_idx"), (slots, "slots"), (valid_counts, "valid_counts")):
+        _dev(t, torch.int32, n)
+    if not (token_idx.is_contiguous() and slots.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("token_idx, slots and block_table must be contiguous")
+    rows, width = token_idx.shape
+    mb = block_table.shape[1] if max_blocks_per_req is None else max_blocks_per_req
+    stride = block_size if block_stride_rows is None else block_stride_rows
+    _check(_lib.sel_remap_workspace(_ptr(req_id), int(block_table.shape[0]), _ptr(block_table),
+                                    int(block_table.shape[1]), int(mb), int(num_kv_blocks), _ptr(ws_req),
+                                    _ptr(ws_starts), int(ws_starts.numel()), _ptr(token_idx), int(rows), int(width),
+                                    int(block_size), int(stride), _ptr(slots), _ptr(valid_counts), _stream(stream)),
+           "sel_remap_workspace")
+    return slots, valid_counts
+
+
+def sel_remap_dcp(req_id, block_table, token_idx, slots, *, num_kv_blocks, dcp_size, dcp_rank, interleave=1,
+                  compact=True, block_size=64, max_blocks_per_req=None, valid_counts=None, stream=None):
+    """One decode-context-parallel rank's slots (its dense block table), optionally compacted to the front."""
+    for t, n in ((req_id, "req_id"), (block_table, "block_table"), (token_idx, "token_idx"),
+                 (slots, "slots"), (valid_counts, "valid_counts")):
+        _dev(t, torch.int32, n)
+    if not (token_idx.is_contiguous() and slots.is_contiguous() and block_table.is_contiguous()):
+        raise ValueError("token_idx, slots and block_table must be contiguous")
+    rows, width = token_idx.shape
+    mb = block_table.shape[1] if max_blocks_per_req is None else max_blocks_per_req
+    _check(_lib.sel_remap_dcp(_ptr(req_id), int(block_table.shape[0]), _ptr(block_table), int(block_table.shape[1]),
+                              int(mb), int(num_kv_blocks), _ptr(token_idx), int(rows), int(width), int(block_size),
+                              int(dcp_size), int(dcp_rank), int(interleave), int(bool(compact)), _ptr(slots),
+                              _ptr(valid_counts), _stream(stream)), "sel_remap_dcp")
     return slots, valid_counts
 
 

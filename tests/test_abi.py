@@ -104,6 +104,50 @@ def test_remap_rejects_bad_arguments(lib):
     assert call(rows=0, tok=None, slots=None) == 0   # empty batch: nothing to do
 
 
+def test_workspace_remap_rejects_bad_arguments(lib):
+    f = lib.sel_remap_workspace
+    f.argtypes = [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                  C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_void_p,
+                  C.c_void_p]
+    good = dict(req=0x1000, nreq=1, bt=0x2000, ld=8, mb=8, nkv=8, wsr=0x5000, wss=0x6000, npf=2, tok=0x3000,
+                rows=2, width=8, bs=64, stride=64, slots=0x4000)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["req"], a["nreq"], a["bt"], a["ld"], a["mb"], a["nkv"], a["wsr"], a["wss"], a["npf"], a["tok"],
+                 a["rows"], a["width"], a["bs"], a["stride"], a["slots"], None, None)
+
+    assert call(wsr=None) == -1                # no workspace request ids
+    assert call(wss=None) == -1                # prefill requests without starts
+    assert call(npf=-1) == -1
+    assert call(width=6) == -1
+    assert call(tok=0x3004) == -2
+    assert call(rows=0, tok=None, slots=None, wsr=None) == 0
+
+
+def test_dcp_remap_rejects_bad_arguments(lib):
+    f = lib.sel_remap_dcp
+    f.argtypes = [C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_void_p, C.c_int32,
+                  C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                  C.c_void_p]
+    good = dict(req=0x1000, nreq=1, bt=0x2000, ld=8, mb=8, nkv=8, tok=0x3000, rows=2, width=8, bs=64, size=2,
+                rank=1, inter=4, compact=1, slots=0x4000)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["req"], a["nreq"], a["bt"], a["ld"], a["mb"], a["nkv"], a["tok"], a["rows"], a["width"], a["bs"],
+                 a["size"], a["rank"], a["inter"], a["compact"], a["slots"], None, None)
+
+    assert call(size=0) == -1
+    assert call(rank=2) == -1                  # rank outside [0, dcp_size)
+    assert call(rank=-1) == -1
+    assert call(inter=0) == -1
+    assert call(inter=48) == -1                # an interleave group would straddle a block
+    assert call(width=6) == -1
+    assert call(slots=0x4004) == -2
+    assert call(rows=0, tok=None, slots=None) == 0
+
+
 def test_topk_rejects_bad_arguments(lib):
     f = lib.sel_topk_expand
     f.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,

@@ -62,6 +62,91 @@ def test_remap_golden_worked_example():
         np.testing.assert_array_equal(counts.cpu().numpy(), ints(g, "counts"))
 
 
+@pytest.mark.parametrize("rows,width", [(1, 4), (37, 2052), (300, 260), (4112, 2052)])
+def test_workspace_remap_matches_oracle(rows, width):
+    """Decode rows, prefill rows of 3 requests and rows with a bad prefill id, bit exact."""
+    sel = lib()
+    rng = np.random.default_rng(rows * 11 + width)
+    nreq, nb, nkv = 6, 40, 300
+    bt = rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)
+    bt[2, 7] = -5
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)
+    wsr = rng.choice(np.array([-1, -1, 0, 1, 2, 3, -2], np.int32), size=rows)   # 3 and -2: out of range
+    starts = np.array([0, 70000, 140000], np.int32)
+    tok = workloads.random_token_indices(rows, width, (nb + 2) * 64, seed=rows + 3 * width)
+    ref_slots, ref_counts = oracle.remap_ws_rows(req, nreq, bt, nb - 1, nkv, wsr, starts, tok, 64, 128)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    sel.sel_remap_workspace(t(req), t(bt), t(wsr), t(starts), t(tok), slots, num_kv_blocks=nkv, block_size=64,
+                            block_stride_rows=128, max_blocks_per_req=nb - 1, valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
+def test_workspace_remap_golden_worked_example():
+    sel = lib()
+    g = load("workspace_worked_example.txt")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    tok = np.stack([ints(g, f"tokens_row{r}") for r in range(4)])
+    slots = torch.empty((4, 4), dtype=torch.int32, device=DEV)
+    counts = torch.empty(4, dtype=torch.int32, device=DEV)
+    sel.sel_remap_workspace(t(ints(g, "req_id")), t(ints(g, "block_table_row0")[None, :]), t(ints(g, "ws_req")),
+                            t(ints(g, "ws_starts")), t(tok), slots, num_kv_blocks=int(g["num_kv_blocks"][0]),
+                            block_size=int(g["block_size"][0]), block_stride_rows=int(g["stride"][0]),
+                            max_blocks_per_req=int(g["max_blocks"][0]), valid_counts=counts)
+    torch.cuda.synchronize()
+    for r in range(4):
+        np.testing.assert_array_equal(slots.cpu().numpy()[r], ints(g, f"slots_row{r}"))
+    np.testing.assert_array_equal(counts.cpu().numpy(), ints(g, "counts"))
+
+
+@pytest.mark.parametrize("dcp,inter,rank", [(1, 1, 0), (2, 1, 1), (2, 4, 0), (4, 16, 3), (8, 64, 5)])
+@pytest.mark.parametrize("compact", [False, True])
+@pytest.mark.parametrize("rows,width", [(7, 260), (4112, 2052)])
+def test_dcp_remap_matches_oracle(dcp, inter, rank, compact, rows, width):
+    """One DCP rank's filtered (and compacted) slots, bit exact, with guarded blocks."""
+    sel = lib()
+    rng = np.random.default_rng(dcp * 1000 + inter * 10 + rank + rows)
+    nreq, nb, nkv = 5, 48, 400
+    bt = rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)
+    bt[1, 2] = -1
+    bt[3, 9] = nkv + 1
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)
+    tok = workloads.random_token_indices(rows, width, nb * 64 * dcp + 200, seed=rows + dcp + inter)
+    ref_slots, ref_counts = oracle.remap_dcp_rows(req, nreq, bt, nb - 2, nkv, tok, 64, dcp, rank, inter, compact)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    sel.sel_remap_dcp(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, dcp_size=dcp, dcp_rank=rank,
+                      interleave=inter, compact=compact, block_size=64, max_blocks_per_req=nb - 2,
+                      valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
+def test_dcp_remap_golden_worked_example():
+    sel = lib()
+    g = load("dcp_worked_example.txt")
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    tok = np.stack([ints(g, f"tokens_row{r}") for r in range(3)])
+    bt = np.stack([ints(g, "block_table_row0"), ints(g, "block_table_row1")])
+    kw = dict(num_kv_blocks=int(g["num_kv_blocks"][0]), dcp_size=int(g["dcp_size"][0]),
+              interleave=int(g["interleave"][0]), block_size=int(g["block_size"][0]),
+              max_blocks_per_req=int(g["max_blocks"][0]))
+    for rank, compact, key in ((0, False, "rank0_row"), (1, False, "rank1_row"), (0, True, "rank0_compact_row")):
+        slots = torch.empty((3, 8), dtype=torch.int32, device=DEV)
+        counts = torch.empty(3, dtype=torch.int32, device=DEV)
+        sel.sel_remap_dcp(t(ints(g, "req_id")), t(bt), t(tok), slots, dcp_rank=rank, compact=compact,
+                          valid_counts=counts, **kw)
+        torch.cuda.synchronize()
+        for r in range(3):
+            np.testing.assert_array_equal(slots.cpu().numpy()[r], ints(g, f"{key}{r}"), err_msg=key)
+        np.testing.assert_array_equal(counts.cpu().numpy(), ints(g, f"rank{rank}_counts"))
+
+
 # ---------------------------------------------------------------- top-k + expansion (K-c)
 TOPK_CASES = [
     # (topk, kpool, contexts)                          exercises
