@@ -76,6 +76,7 @@ def _load(path: str):
     L.orc_dcp_local_index.argtypes = [I32, I32, I32, I32]
     L.orc_dcp_local_index.restype = I64
     L.orc_remap_dcp_rows.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I32, I32, I32, I32, P, P]
+    L.orc_maxsim.argtypes = [P, I32, I32, P, I64, I64, P, P, I32, P, P]
     L.orc_select.argtypes = [C.POINTER(_Problem), P, I32, I32, P, P, P, P, P, I64]
     L.orc_select.restype = I32
     L.orc_score_rows.argtypes = [C.POINTER(_Problem), P, I32, P, P, I64]
@@ -191,6 +192,20 @@ def remap_dcp_rows(req_id, num_reqs, block_table, max_blocks, num_kv_blocks, tok
                              rows, width, block_size, dcp_size, dcp_rank, interleave, int(bool(compact)),
                              _p(slots), _p(counts))
     return slots, counts
+
+
+def maxsim(q, docs, offsets, lengths):
+    """MaxSim scores of query q [lq, d] (fp16) against the documents (offsets[i], lengths[i])
+    of the packed fp16 tensor docs [total_tokens, >= d] (vLLM page "flash_maxsim_rerank",
+    _maxsim_rerank_kernel). Returns (scores float32 [B], abs_bound float64 [B])."""
+    qb = _c(q, np.float16).view(np.uint16)
+    db = _c(docs, np.float16).view(np.uint16)
+    of, ln = _c(offsets, np.int32), _c(lengths, np.int32)
+    lq, d = qb.shape
+    scores = np.empty(of.size, dtype=np.float32)
+    bound = np.empty(of.size, dtype=np.float64)
+    lib().orc_maxsim(_p(qb), lq, d, _p(db), db.shape[1], db.shape[0], _p(of), _p(ln), of.size, _p(scores), _p(bound))
+    return scores, bound
 
 
 class _Held:

@@ -34,6 +34,8 @@
  *   7. valid count = number of entries that are not -1 ("the count of valid
  *      (non -1) indices per row").
  *
+ * Also here: the MaxSim rerank of a query against packed documents (orc_maxsim).
+ *
  * The remap also has the page's two other modes: prefill rows mapped into a prefill
  * workspace (orc_remap_ws_rows) and a decode-context-parallel rank's filter with optional
  * compaction to the front (orc_remap_dcp_rows).
@@ -317,6 +319,54 @@ void orc_remap_dcp_rows(const int32_t *req_id, int32_t num_reqs, const int32_t *
                 out[c] = -1;
         if (counts)
             counts[r] = cnt;
+    }
+}
+
+/* MaxSim rerank (vLLM page "flash_maxsim_rerank", _maxsim_rerank_kernel and
+ * flash_maxsim_rerank_direct): one query of lq token embeddings against num_docs documents
+ * whose token embeddings lie anywhere in a packed [total_tokens, doc_stride] tensor, doc i
+ * being rows offsets[i] .. offsets[i] + lengths[i] - 1. For every query token the best
+ * (largest) dot product over the document's tokens is taken, and the document's score is
+ * the sum of those maxima over the query tokens:
+ *     score_i = sum_{a < lq} max_{j < len_i} sum_{k < d} q[a][k] * doc[off_i + j][k]
+ * The page's masking fixes the degenerate cases: a running maximum starts at -inf, so a
+ * document with no tokens (length <= 0) scores -inf, and with no query tokens every
+ * document scores 0. A row outside [0, total_tokens) reads as a zero vector (it lies
+ * outside the page's contract; this is the reading the device path implements).
+ * Each dot product is accumulated in double from the exact fp16 x fp16 products, the
+ * maxima are summed in double and the score is rounded to float once. abs_bound[i]
+ * (optional) = sum_a max_j sum_k |q[a][k] * doc[off_i + j][k]|, the scale of the rounding
+ * of an implementation that accumulates in fp32. */
+void orc_maxsim(const uint16_t *q, int32_t lq, int32_t d, const uint16_t *docs, int64_t doc_stride,
+                int64_t total_tokens, const int32_t *offsets, const int32_t *lengths, int32_t num_docs,
+                float *scores, double *abs_bound)
+{
+    for (int32_t i = 0; i < num_docs; ++i) {
+        double total = 0.0, bound = 0.0;
+        for (int32_t a = 0; a < lq; ++a) {
+            double best = -INFINITY, best_abs = 0.0;
+            for (int32_t j = 0; j < lengths[i]; ++j) {
+                const int64_t r = (int64_t)offsets[i] + j;
+                double s = 0.0, sa = 0.0;
+                if (r >= 0 && r < total_tokens) {
+                    const uint16_t *row = docs + r * doc_stride;
+                    for (int32_t k = 0; k < d; ++k) {
+                        double t = (double)orc_half_to_float(q[(int64_t)a * d + k]) * (double)orc_half_to_float(row[k]);
+                        s += t;
+                        sa += fabs(t);
+                    }
+                }
+                if (s > best)
+                    best = s;
+                if (sa > best_abs)
+                    best_abs = sa;
+            }
+            total += best;
+            bound += best_abs;
+        }
+        scores[i] = (float)total;
+        if (abs_bound)
+            abs_bound[i] = bound;
     }
 }
 

@@ -349,9 +349,112 @@ def pin_dcp_compaction(orc, seed=35):
             assert np.array_equal(b[r][:ca[r]], kept) and (b[r][ca[r]:] == -1).all()
 
 
+
+# ---------------------------------------------------------------- MaxSim rerank
+def _maxsim_exact(q, rows, offsets, lengths):
+    """Brute force with integer arithmetic: numpy's int64 matmul, max over each doc's
+    rows, sum over the query rows (integer-valued inputs only)."""
+    qi = q.astype(np.int64)
+    out = []
+    for o, n in zip(offsets, lengths):
+        idx = np.arange(o, o + max(n, 0))
+        if idx.size == 0:
+            out.append(-np.inf if qi.shape[0] else 0.0)
+            continue
+        r = np.zeros((idx.size, qi.shape[1]), dtype=np.int64)
+        inside = (idx >= 0) & (idx < rows.shape[0])
+        r[inside] = rows[idx[inside], :qi.shape[1]].astype(np.int64)
+        out.append(float((qi @ r.T).max(axis=1).sum()))
+    return np.array(out)
+
+
+def pin_maxsim_worked_example(orc):
+    """Hand-worked MaxSim fixture (tests/golden/maxsim_worked_example.txt): scattered and
+    overlapping docs, an empty doc, a single-row doc."""
+    import _golden
+    d = _golden.load("maxsim_worked_example.txt")
+    lq, dim = int(d["lq"][0]), int(d["d"][0])
+    q = _golden.ints(d, "q").reshape(lq, dim).astype(np.float16)
+    rows = _golden.ints(d, "rows").reshape(-1, dim).astype(np.float16)
+    s, _ = orc.maxsim(q, rows, _golden.ints(d, "offsets"), _golden.ints(d, "lengths"))
+    assert np.array_equal(s, _golden.floats(d, "scores")), s
+
+
+def pin_maxsim_integer_exact(orc, seed=41):
+    """Integer-valued fp16 inputs (|score| < 2^24, so every step is exact): the oracle equals
+    the int64 brute force, over random scattered docs in a tensor wider than d."""
+    rng = np.random.default_rng(seed)
+    for lq, dim, width in ((3, 8, 8), (5, 16, 24), (1, 40, 48), (7, 4, 8)):
+        total = 57
+        rows = rng.integers(-3, 4, size=(total, width)).astype(np.float16)
+        q = rng.integers(-3, 4, size=(lq, dim)).astype(np.float16)
+        lengths = rng.integers(0, 9, size=11).astype(np.int32)
+        offsets = rng.integers(0, total - 8, size=11).astype(np.int32)
+        s, _ = orc.maxsim(q, rows, offsets, lengths)
+        ref = _maxsim_exact(q, rows, offsets, lengths)
+        assert np.array_equal(s.astype(np.float64), ref), (lq, dim, s, ref)
+
+
+def pin_maxsim_single_row_closed_form(orc, seed=43):
+    """A one-row doc has no max to take: its score is (sum_a q_a) . row, computed here in
+    float64 from the column sums of q."""
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((9, 32)) / 4).astype(np.float16)
+    rows = (rng.standard_normal((20, 32)) / 4).astype(np.float16)
+    offs = np.arange(20, dtype=np.int32)
+    s, _ = orc.maxsim(q, rows, offs, np.ones(20, np.int32))
+    ref = rows.astype(np.float64) @ q.astype(np.float64).sum(axis=0)
+    assert np.allclose(s, ref, rtol=1e-6, atol=1e-6), (s, ref)
+
+
+def pin_maxsim_order_invariance(orc, seed=45):
+    """The score is a function of the doc's set of rows: permuting the rows, or repeating
+    one, leaves it unchanged (bit for bit, as each dot product is computed alone)."""
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((6, 16))).astype(np.float16)
+    base = (rng.standard_normal((10, 16))).astype(np.float16)
+    perm = base[rng.permutation(10)]
+    dup = np.concatenate([base, base[3:4]])
+    rows = np.concatenate([base, perm, dup])
+    s, _ = orc.maxsim(q, rows, np.array([0, 10, 20], np.int32), np.array([10, 10, 11], np.int32))
+    assert s[0] == s[1] == s[2], s
+
+
+def pin_maxsim_degenerate(orc):
+    """The page's masking: an empty (or negative-length) doc scores -inf, no query rows
+    score 0; rows outside the tensor read as zero vectors."""
+    q = np.array([[1, -2], [3, 1]], np.float16)
+    rows = np.array([[-1, -1], [2, 0]], np.float16)
+    s, _ = orc.maxsim(q, rows, np.array([0, 1, 0, 1, -3], np.int32), np.array([0, -2, 1, 5, 2], np.int32))
+    # doc 2 = row 0: (-1+2) + (-3-1) = -3; doc 3 = row 1 and 4 zero rows: max(2,0) + max(6,0) = 8;
+    # doc 4 = two rows before the tensor: 0 + 0
+    assert s[0] == -np.inf and s[1] == -np.inf and s[2] == -3.0 and s[3] == 8.0 and s[4] == 0.0, s
+    s, _ = orc.maxsim(np.zeros((0, 2), np.float16), rows, np.array([0, 0], np.int32), np.array([2, 0], np.int32))
+    assert np.array_equal(s, np.zeros(2, np.float32)), s
+
+
+def pin_maxsim_normal_bound(orc, seed=47):
+    """Normal values: the oracle's score is within one fp32 rounding of the float64 brute
+    force (numpy matmul, max, sum), and abs_bound equals sum_a max_j sum_k |q_ak t_jk|."""
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((32, 128)) / np.sqrt(128)).astype(np.float16)
+    rows = rng.standard_normal((300, 128)).astype(np.float16)
+    offs = np.array([0, 17, 100, 250], np.int32)
+    lens = np.array([17, 83, 150, 50], np.int32)
+    s, b = orc.maxsim(q, rows, offs, lens)
+    q64, r64 = q.astype(np.float64), rows.astype(np.float64)
+    for i, (o, n) in enumerate(zip(offs, lens)):
+        sims = q64 @ r64[o:o + n].T
+        ref = sims.max(axis=1).sum()
+        absb = (np.abs(q64)[:, None, :] * np.abs(r64[o:o + n])[None, :, :]).sum(axis=2).max(axis=1).sum()
+        assert abs(s[i] - ref) <= 2.0 ** -23 * abs(ref) + 1e-12 * absb, (i, s[i], ref)
+        assert abs(b[i] - absb) <= 1e-12 * absb, (i, b[i], absb)
+
 ALL_PINS = [pin_half_decode, pin_score_integer_exact, pin_score_normal_bound,
             pin_topk_bruteforce, pin_topk_all_zero, pin_topk_stable_argsort,
             pin_expand_closed_form, pin_remap_identity, pin_remap_inverse, pin_remap_guards,
             pin_planted_winners, pin_pipeline_counts, pin_integer_scores_match_exact,
             pin_workspace_worked_example, pin_workspace_decode_rows_are_remap, pin_dcp_worked_example,
-            pin_dcp_single_rank_is_remap, pin_dcp_interleave_partition, pin_dcp_compaction]
+            pin_dcp_single_rank_is_remap, pin_dcp_interleave_partition, pin_dcp_compaction,
+            pin_maxsim_worked_example, pin_maxsim_integer_exact, pin_maxsim_single_row_closed_form,
+            pin_maxsim_order_invariance, pin_maxsim_degenerate, pin_maxsim_normal_bound]

@@ -41,6 +41,13 @@ MUTANTS = {
     "dcp_local_not_divided": [("return (group / dcp_size) * interleave + t % interleave;",
                                "return group * interleave + t % interleave;")],
     "dcp_table_not_dense": [("num_kv_blocks, block_size, block_size);", "num_kv_blocks, block_size, 2 * block_size);")],
+    "maxsim_min_not_max": [("                if (s > best)\n", "                if (s < best || best == -INFINITY)\n")],
+    "maxsim_max_starts_at_zero": [("double best = -INFINITY, best_abs = 0.0;", "double best = 0.0, best_abs = 0.0;")],
+    "maxsim_last_row_dropped": [("for (int32_t j = 0; j < lengths[i]; ++j) {", "for (int32_t j = 0; j < lengths[i] - 1; ++j) {")],
+    "maxsim_q_transposed": [("orc_half_to_float(q[(int64_t)a * d + k])", "orc_half_to_float(q[(int64_t)k * lq + a])")],
+    "maxsim_stride_is_d": [("const uint16_t *row = docs + r * doc_stride;", "const uint16_t *row = docs + r * d;")],
+    "maxsim_first_query_row_only": [("for (int32_t a = 0; a < lq; ++a) {\n            double best", "for (int32_t a = 0; a < 1; ++a) {\n            double best")],
+    "maxsim_oob_not_zero": [("double s = 0.0, sa = 0.0;\n                if (r >= 0", "double s = -1.0, sa = 0.0;\n                if (r >= 0")],
     "dcp_compact_keeps_columns": [("                    out[cnt] = s;", "                    out[c] = s;")],
 }
 
