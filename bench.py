@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-remap", action="store_true", help="skip the stand-alone remap measurements")
+    ap.add_argument("--no-maxsim", action="store_true", help="skip the MaxSim rerank measurement")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (profiling runs)")
     return ap.parse_args()
 
@@ -263,6 +264,42 @@ def remap_modes(sel, torch, dev, stream, flush, peak, iters):
     return out
 
 
+def maxsim_rerank(sel, torch, dev, stream, flush, peak, iters):
+    """MaxSim rerank of a 32 x 128 query against 4,096 packed documents of 1..512 rows
+    (about 1.05 M rows, 270 MB of fp16, above L2; L2 flushed before each call as well),
+    CUDA events on the launching stream around each call (its memset and kernel).
+    Algorithmic bytes: every document row once (d * 2 bytes), each document's offset,
+    length and score (12 bytes), and the query once."""
+    from workloads.maxsim import make_maxsim
+    w = make_maxsim("maxsim_rerank4k")
+    lq, d = w.q.shape
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, docs, off, ln = t(w.q), t(w.docs), t(w.offsets), t(w.lengths)
+    scores = torch.empty(w.num_docs, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(sel.sel_maxsim_workspace_bytes(), dtype=torch.uint8, device=dev)
+    call = lambda: sel.sel_maxsim_rerank(q, docs, off, ln, scores=scores, status=status, ws=ws, stream=stream)
+    nbytes = w.doc_rows * d * 2 + w.num_docs * 12 + lq * d * 2
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the MaxSim rerank")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"maxsim_rerank4k: lq {lq}, d {d}, {w.num_docs} docs, {w.doc_rows} rows",
+            "algorithmic_bytes": nbytes, "us": ms * 1e3, "doc_rows_per_s": w.doc_rows / (ms * 1e-3),
+            "docs_per_s": w.num_docs / (ms * 1e-3), "GB/s": gbs, "frac": gbs / peak,
+            "gpu_launches": sel.sel_maxsim_launch_count(lq, d)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -402,6 +439,9 @@ def run_ours(args):
     remap = None
     if not args.no_remap:
         remap = remap_modes(sel, torch, dev, stream, flush, peak, 20)
+    maxsim = None
+    if not args.no_maxsim:
+        maxsim = maxsim_rerank(sel, torch, dev, stream, flush, peak, 20)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -438,6 +478,8 @@ def run_ours(args):
             line["cpu_baseline"] = cpu
         if remap:
             line["remap_modes"] = remap
+        if maxsim:
+            line["maxsim_rerank"] = maxsim
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -18,6 +18,9 @@
  *    segment of rows of one request, 4 heads x 128 dims in fp16, int32 metadata,
  *    segment descriptors built on the device so the call is CUDA-graph safe; the
  *    selection keeps the top-512 pools (index_topk 2048 / kpool 4).
+ *  - "flash_maxsim_rerank" page: the MaxSim rerank of a query against documents
+ *    packed in one tensor (sel_maxsim_rerank), a second workload on the same
+ *    segmented tensor-core scoring.
  *  - "flashinfer_mla_sparse_sm90" page, _kv_lens_host: a row's context is
  *    position + 1; contexts up to index_topk select every token, longer ones keep
  *    index_topk pool-expanded tokens plus the trailing incomplete pool, so the valid
@@ -215,6 +218,36 @@ int sel_remap_dcp(const int32_t *req_id, int32_t num_reqs, const int32_t *block_
                   const int32_t *token_idx, int32_t num_rows, int32_t width, int32_t block_size,
                   int32_t dcp_size, int32_t dcp_rank, int32_t interleave, int32_t compact,
                   int32_t *slots, int32_t *valid_counts, sel_stream_t stream);
+
+/*
+ * sel_maxsim_rerank -- MaxSim scores of one query against documents packed in one tensor
+ * (vLLM page "flash_maxsim_rerank", _maxsim_rerank_kernel / flash_maxsim_rerank_direct).
+ *   q [lq][q_stride] fp16: the query's token embeddings, d used columns per row.
+ *   docs [total_tokens][doc_stride] fp16: the packed tensor; document b is rows
+ *     doc_offsets[b] .. doc_offsets[b] + doc_lengths[b] - 1 (int32 [num_docs] each; documents
+ *     may be scattered, out of order or overlapping; read in place, never copied).
+ *   scores [num_docs] fp32 (written): score[b] = sum_{a<lq} max_{j<len_b} q[a] . docs[off_b+j],
+ *     each dot product on the tensor cores with fp32 accumulation.
+ * The page's masking decides the degenerate cases: a document with doc_lengths[b] <= 0
+ * scores -inf; lq == 0 gives 0 for every document (q and docs may then be NULL);
+ * num_docs == 0 queues nothing. Rows outside [0, total_tokens) read as zero vectors (no
+ * fault; outside the page's contract).
+ * Requires 1 <= d <= 1024, q_stride and doc_stride >= d and multiples of 8, q and docs
+ * 16-B aligned, total_tokens <= INT32_MAX - 64, and a 4-B aligned device workspace of
+ * sel_maxsim_workspace_bytes() bytes, ZERO-FILLED before its first use: it holds the
+ * kernel's work counters, and every launch leaves them zero again when it finishes (also
+ * after a timeout), so a workspace kept for this entry point needs zeroing only once.
+ * Calls sharing one workspace must not overlap on the GPU. Queues one kernel per block of
+ * up to 128 query rows (64 for d > 256, 32 for d > 512); later blocks add to scores.
+ * status (optional): SEL_ST_TIMEOUT if a bounded wait expired.
+ */
+size_t sel_maxsim_workspace_bytes(void);
+int sel_maxsim_rerank(const void *q, int32_t lq, int32_t d, int64_t q_stride, const void *docs,
+                      int64_t total_tokens, int64_t doc_stride, const int32_t *doc_offsets,
+                      const int32_t *doc_lengths, int32_t num_docs, float *scores, int32_t *status,
+                      void *ws, size_t ws_bytes, sel_stream_t stream);
+/* Kernel launches one sel_maxsim_rerank call with this lq and d queues. */
+int32_t sel_maxsim_launch_count(int32_t lq, int32_t d);
 
 /*
  * sel_select -- the fused path: segment builder, segmented scorer, top-k with

@@ -11,6 +11,9 @@ from .sel import (  # noqa: F401
     problem_from_workload,
     sel_error_string,
     sel_host_stage_bytes,
+    sel_maxsim_launch_count,
+    sel_maxsim_rerank,
+    sel_maxsim_workspace_bytes,
     sel_remap_dcp,
     sel_remap_global,
     sel_remap_workspace,

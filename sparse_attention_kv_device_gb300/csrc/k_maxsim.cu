@@ -1,0 +1,569 @@
+// K-m: MaxSim rerank of one query against documents packed in one tensor, on the
+// 5th-generation tensor cores.
+//
+// What it computes (vLLM page "flash_maxsim_rerank", _maxsim_rerank_kernel):
+//     score[b] = sum_{a < lq} max_{j < len_b} q[a] . docs[off_b + j]
+// with fp16 inputs and fp32 accumulation; a document with no rows scores -inf (the page's
+// running maxima start at -inf). The page runs one program per document over power-of-two
+// buckets of rows. The design here is GB300's own:
+//   * documents are cut into 32-row chunks and packed, in the order the CTA takes them, four
+//     chunks to a 128-row tile (a document may span tiles), so tiles stay full until the
+//     CTA's last one;
+//   * each tile streams through a ring of 64-column (128-byte swizzle) K slabs; full chunks
+//     that continue one another (one document's consecutive rows) are copied by one TMA box
+//     of 32, 64, 96 or 128 rows, and a document's partial last chunk by a box of its valid
+//     rows rounded up to 8, so a document over-reads at most 7 rows;
+//   * one thread issues tcgen05.mma with the query block as A (M = 128: up to 128 query rows,
+//     resident in shared memory) and the tile as B (N = 128 document rows, K = 16 per
+//     instruction, fp16 in, fp32 accumulate) into one of two TMEM accumulators, so TMEM lane
+//     a holds query row a's dot products with the tile's 128 rows;
+//   * epilogue warp w reads the lanes of query rows 32w .. 32w + 31: each thread takes the
+//     maximum over a chunk's valid rows in registers, folds it into its document's running
+//     maximum, and at the document's last chunk the warp sums its 32 rows; with more than 32
+//     query rows the warp finishing a tile last adds the warps' sums in a fixed order;
+//   * roles: warp 0 schedules (documents -> chunks -> tile records, up to 16 tiles ahead),
+//     warp 6 only issues TMA copies, so the copy engine is never left idle while the schedule
+//     is built; warp 1 issues the MMAs; warps 2-5 are the epilogue;
+//   * CTAs take documents in grabs of docs_per_grab: CTA g's first four grabs are static, the
+//     rest come from an atomic counter in the caller's workspace (the last CTA to finish sets
+//     it back to zero, so no memset is queued), so a CTA's tail is at most one grab; a grab's id and its offsets/lengths are fetched one step
+//     ahead (an atomic, then cp.async), late enough that few claimed documents are left
+//     unscheduled when the counter runs dry. Every document is finished by the CTA that took it.
+// Rows outside [0, total_tokens) read as zero vectors (the TMA's out-of-bounds fill).
+#include <algorithm>
+
+#include "sel_device.cuh"
+#include "sel_kernels.h"
+
+namespace sel {
+
+SEL_PHASE_TABLE(maxsim)
+
+namespace {
+
+constexpr int kMsRing = 16;                     // tile records published ahead by the scheduler
+constexpr int kMsRec = 16;                      // ints per tile record: {doc, info, first row, box chunks} x 4
+constexpr uint32_t kMsChunkBytes = 32 * 128;    // 32 rows x 64 fp16 columns
+constexpr uint32_t kMsSlabBytes = 4 * kMsChunkBytes;  // one 128-row K slab of a tile
+constexpr int kMsPartBufs = 4;                  // tiles whose per-warp sums may be pending at once
+
+// chunk info word: rows valid (1..32) | first chunk of its document << 6 | last << 7
+constexpr int kInfoFirst = 64;
+constexpr int kInfoLast = 128;
+
+struct MsSmem {
+    uint8_t* q;          // kslabs x nq_pad x 128 B (the query block, K slab by K slab)
+    uint8_t* a;          // stages x kMsSlabBytes
+    int* ring;           // [kMsRing][kMsRec] tile records; chunk c: doc (-1: none), info, first row,
+                         // rows in the box starting at c (0: none); word 3 of chunk 0 = -1: end
+    float* part;         // [kMsPartBufs][4 chunks][4 warps] per-warp sums of documents ending in a tile
+    int* part_cnt;       // [kMsPartBufs] warps done with the tile
+    int* qoff;           // [2][32] document offsets of the current and next grab (copied ahead by cp.async)
+    int* qlen;           // [2][32] document lengths of the current and next grab
+    uint64_t* full;      // [stages]
+    uint64_t* empty;     // [stages]
+    uint64_t* tfull;     // [2]
+    uint64_t* tempty;    // [2]
+    uint64_t* sfull;     // [kMsRing]
+    uint64_t* sempty;    // [kMsRing] read by the TMA thread, the MMA thread and the epilogue warps
+    uint64_t* qfull;     // [1]
+    uint64_t* done;      // [1]
+    uint32_t* tmem_base;
+    int* abort_flag;
+};
+
+__device__ __forceinline__ MsSmem ms_carve(uint8_t* raw, int stages, int nq_pad, int kslabs) {
+    MsSmem s;
+    const uint32_t base = smem_u32(raw);
+    uint8_t* p = raw + (((base + 1023u) & ~1023u) - base);
+    s.q = p;
+    p += static_cast<size_t>(kslabs) * nq_pad * 128u;
+    s.a = p;
+    p += static_cast<size_t>(stages) * kMsSlabBytes;
+    s.ring = reinterpret_cast<int*>(p);
+    p += kMsRing * kMsRec * sizeof(int);
+    s.part = reinterpret_cast<float*>(p);
+    p += kMsPartBufs * 16 * sizeof(float);
+    s.part_cnt = reinterpret_cast<int*>(p);
+    p += kMsPartBufs * sizeof(int);
+    s.qoff = reinterpret_cast<int*>(p);
+    p += 2 * 32 * sizeof(int);
+    s.qlen = reinterpret_cast<int*>(p);
+    p += 2 * 32 * sizeof(int);
+    uint64_t* b = reinterpret_cast<uint64_t*>(p);
+    s.full = b;
+    s.empty = b + stages;
+    s.tfull = b + 2 * stages;
+    s.tempty = s.tfull + 2;
+    s.sfull = s.tempty + 2;
+    s.sempty = s.sfull + kMsRing;
+    s.qfull = s.sempty + kMsRing;
+    s.done = s.qfull + 1;
+    uint32_t* w = reinterpret_cast<uint32_t*>(s.done + 1);
+    s.tmem_base = w;
+    s.abort_flag = reinterpret_cast<int*>(w + 1);
+    return s;
+}
+
+// Waits on `bar` with lane 0 polling; every lane learns the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+// Maximum of v[0 .. rows-1] (1 <= rows <= 32), as fp32: a five-level tree (independent
+// operations at each level); rows past `rows` are masked only when the chunk is partial.
+__device__ __forceinline__ float row_max(const uint32_t (&v)[32], int rows) {
+    float x[16];
+    if (rows >= 32) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = fmaxf(__uint_as_float(v[j]), __uint_as_float(v[j + 16]));
+    } else {
+        const float ninf = -__int_as_float(0x7f800000);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            x[j] = fmaxf(__uint_as_float(v[j]), j + 16 < rows ? __uint_as_float(v[j + 16]) : ninf);
+#pragma unroll
+        for (int j = 1; j < 16; ++j)
+            if (j >= rows) x[j] = ninf;
+    }
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) x[j] = fmaxf(x[j], x[j + w]);
+    return x[0];
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kMaxsimThreads, 1)
+    k_maxsim(const MaxsimArgs a, const __grid_constant__ MaxsimMaps maps) {
+    const CUtensorMap* tmap_d = maps.d;
+    const CUtensorMap& tmap_q = maps.q;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    MsSmem sm = ms_carve(smem_raw, a.stages, a.nq_pad, a.kslabs);
+    const int nwarps = a.nq_pad >> 5;  // epilogue warps with query rows
+    // diagnostics: CTA 0 stamps its phases, every CTA its end (300 + CTA)
+    const bool tr = blockIdx.x == 0;
+    (void)tr;
+    if (tr && threadIdx.x == 0) SEL_PHASE(0);
+    // the scheduler's first round trips start before the setup: the atomic for the CTA's
+    // grab 4 and the offsets/lengths of its grab 0 (blockIdx.x, always < the grab count)
+    int pend = 0;  // warp 0, lane 0: an atomic's value in flight
+    if (warp == 0) {
+        if (lane == 0) pend = atomicAdd(a.counter, 1);
+        const int doc = static_cast<int>(blockIdx.x) * a.docs_per_grab + lane;
+        if (lane < a.docs_per_grab && doc < a.num_docs) {
+            cp_async_4(&sm.qoff[lane], a.offsets + doc);
+            cp_async_4(&sm.qlen[lane], a.lengths + doc);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 32 * nwarps);
+        }
+        for (int i = 0; i < kMsRing; ++i) {
+            mbar_init(&sm.sfull[i], 1);
+            mbar_init(&sm.sempty[i], 2 + nwarps);
+        }
+        for (int i = 0; i < kMsPartBufs; ++i) sm.part_cnt[i] = 0;
+        mbar_init(sm.qfull, 1);
+        mbar_init(sm.done, 1);
+        *sm.abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 6 && lane < kMaxsimDocMaps) tma_prefetch_desc(&tmap_d[lane]);
+    if (warp == 6 && lane == kMaxsimDocMaps) tma_prefetch_desc(&tmap_q);
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_base, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_base;
+    volatile int* abort_flag = sm.abort_flag;
+    if (tr && threadIdx.x == 0) SEL_PHASE(1);
+    const float neg_inf = -__int_as_float(0x7f800000);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ scheduler: documents -> chunks -> tiles
+        const int dpg = a.docs_per_grab;
+        const int ngrabs = (a.num_docs + dpg - 1) / dpg;
+        // Document source, in grabs of dpg documents. The CTA's grab s is static for s < 4
+        // (blockIdx.x + s * gridDim.x, no atomic), else 4 * gridDim.x + an atomic counter value.
+        // Claims are made as late as the round trips allow, so that few claimed documents are
+        // still unscheduled when the counter runs dry (they decide the CTAs' tails): one atomic
+        // is in flight (issued one step before its value is needed), and at step s (consuming
+        // grab s) the id of grab s + 1 is resolved and its offsets and lengths are copied by
+        // cp.async into a shared-memory queue slot.
+        bool has_pend = true;        // warp-uniform: `pend` holds an atomic in flight
+        bool issuing = true;
+        auto fetch_meta = [&](int s, int g) {  // cp.async the grab's offsets and lengths into queue slot s % 2
+            const int doc = g * dpg + lane;
+            if (g >= 0 && lane < dpg && doc < a.num_docs) {
+                cp_async_4(&sm.qoff[(s & 1) * 32 + lane], a.offsets + doc);
+                cp_async_4(&sm.qlen[(s & 1) * 32 + lane], a.lengths + doc);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto resolve = [&](int s) -> int {  // the id of grab s, -1 if none; warp-uniform
+            int id = -1;
+            if (s < 4) {
+                id = static_cast<int>(blockIdx.x) + s * static_cast<int>(gridDim.x);
+            } else if (has_pend) {
+                id = 4 * static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, pend, 0);
+                has_pend = id < ngrabs && issuing;
+                if (has_pend && lane == 0) pend = atomicAdd(a.counter, 1);
+            }
+            if (id >= ngrabs) {
+                id = -1;
+                issuing = false;
+            }
+            return id;
+        };
+        int gid0 = resolve(0);  // its metadata copy was started before the setup
+        // the tile being gathered: lane c < nc holds chunk c
+        int nc = 0, my_doc = -1, my_info = 0, my_row = 0;
+        int n = 0;
+        bool ok = true;
+
+        // publishes the gathered tile (nc == 0: the end record)
+        auto publish = [&]() -> bool {
+            const int slot = n & (kMsRing - 1);
+            if (tr && lane == 0 && n < 50) SEL_PHASE(8 + n);
+            if (!warp_wait(&sm.sempty[slot], ((n / kMsRing) & 1) ^ 1u, abort_flag)) return false;
+            int doc[4], row[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                doc[c] = __shfl_sync(0xffffffffu, c < nc ? my_doc : -1, c);
+                row[c] = __shfl_sync(0xffffffffu, my_row, c);
+            }
+            // full chunks that continue one another (one document, consecutive rows) share one
+            // box of 32 * run rows; a document's partial last chunk gets its own box of its valid
+            // rows rounded up to 8
+            int rows[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rows[c] = __shfl_sync(0xffffffffu, my_info, c) & 63;
+            bool cont[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                cont[c] = c > 0 && c < nc && doc[c] == doc[c - 1] && row[c] == row[c - 1] + 32 && rows[c] == 32;
+            int box = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                int l = c < nc && !cont[c] ? 1 : 0;
+#pragma unroll
+                for (int e = c + 1; e < 4; ++e)
+                    if (l == e - c && cont[e]) ++l;
+                const int h = l == 1 && rows[c] < 32 ? (rows[c] + 7) & ~7 : 32 * l;
+                if (c == lane) box = h;
+            }
+            if (lane < 4) {
+                const int4 v = make_int4(lane < nc ? my_doc : -1, my_info, my_row, (nc == 0 && lane == 0) ? -1 : box);
+                *reinterpret_cast<int4*>(sm.ring + slot * kMsRec + 4 * lane) = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sfull[slot]);
+            ++n;
+            nc = 0;
+            return true;
+        };
+
+        for (int step = 0; ok; ++step) {
+            // grab step + 1: resolve its id and start its metadata copy
+            const int gid1 = resolve(step + 1);
+            fetch_meta(step + 1, gid1);
+            if (gid0 < 0 && gid1 < 0 && !has_pend) break;  // nothing left anywhere
+            // grab step's metadata (copied one step ago): wait for all but the newest group
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            const int g = gid0;
+            int cur_off = 0, cur_len = 0;
+            if (g >= 0 && lane < dpg && g * dpg + lane < a.num_docs) {  // each lane reads what it copied
+                cur_off = sm.qoff[(step & 1) * 32 + lane];
+                cur_len = sm.qlen[(step & 1) * 32 + lane];
+            }
+            gid0 = gid1;
+            for (int i = 0; g >= 0 && i < dpg && ok; ++i) {
+                const int doc = g * dpg + i;
+                if (doc >= a.num_docs) break;
+                const int off = __shfl_sync(0xffffffffu, cur_off, i);
+                const int len = __shfl_sync(0xffffffffu, cur_len, i);
+                if (len <= 0) {
+                    if (lane == 0) a.scores[doc] = neg_inf;
+                    continue;
+                }
+                const int nch = (len + 31) >> 5;
+                for (int k = 0; k < nch; ++k) {
+                    if (lane == nc) {
+                        // clamp the first row into [-32, total_tokens]: rows outside read as zeros
+                        int64_t r = static_cast<int64_t>(off) + 32 * static_cast<int64_t>(k);
+                        r = r < -32 ? -32 : (r > a.total_tokens ? a.total_tokens : r);
+                        my_doc = doc;
+                        my_row = static_cast<int>(r);
+                        my_info = min(32, len - 32 * k) | (k == 0 ? kInfoFirst : 0) | (k == nch - 1 ? kInfoLast : 0);
+                    }
+                    if (++nc == 4 && !(ok = publish())) break;
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        // an atomic still in flight (only after an abort) completes before the counter is reset
+        if (has_pend && lane == 0) asm volatile("" ::"r"(pend));
+        if (ok && nc > 0) ok = publish();
+        if (ok) ok = publish();  // the end record
+        if (lane == 0 && blockIdx.x < 152) SEL_PHASE_VALUE(110 + blockIdx.x, n);
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            report(a.status, kStTimeout);
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ TMA issuer
+        if (lane == 0) {
+            const uint64_t pol_d = l2_policy_evict_first();
+            const uint32_t qslab = static_cast<uint32_t>(a.nq_pad) * 128u;
+            mbar_expect_tx(sm.qfull, static_cast<uint32_t>(a.kslabs) * qslab);
+            for (int g = 0; g < a.kslabs; ++g)
+                tma_load_2d(sm.q + static_cast<size_t>(g) * qslab, &tmap_q, sm.qfull, g * 64, a.q_row0,
+                            l2_policy_evict_last());
+            int stage = 0;
+            uint32_t phase = 0, loaded = 0, last_parity = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int slot = n & (kMsRing - 1);
+                if (!mbar_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
+                int4 r[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int4*>(sm.ring + slot * kMsRec + 4 * c);
+                mbar_arrive(&sm.sempty[slot]);
+                if (r[0].w < 0) break;
+                const uint32_t bytes = static_cast<uint32_t>(max(r[0].w, 0) + max(r[1].w, 0) + max(r[2].w, 0) +
+                                                             max(r[3].w, 0)) * 128u;
+                for (int g = 0; g < a.kslabs; ++g) {
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_expect_tx(&sm.full[stage], bytes);
+                    uint8_t* dst = sm.a + static_cast<size_t>(stage) * kMsSlabBytes;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int h = r[c].w;  // rows in the box starting at chunk c (0: none)
+                        if (h > 0) {
+                            const CUtensorMap* m = h == 8 ? &tmap_d[0] : h == 16 ? &tmap_d[1] : h == 24 ? &tmap_d[2]
+                                                 : h == 32 ? &tmap_d[3] : h == 64 ? &tmap_d[4] : h == 96 ? &tmap_d[5]
+                                                 : &tmap_d[6];
+                            tma_load_2d(dst + c * kMsChunkBytes, m, &sm.full[stage], g * 64, r[c].z, pol_d);
+                        }
+                    }
+                    loaded |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (tr && n < 50) SEL_PHASE(60 + n);
+            }
+            if (ok) {
+                // drain: every stage's last copy consumed before the CTA leaves
+                for (int i = 0; i < a.stages && ok; ++i) {
+                    ok = mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, kStTimeout);
+                for (int i = 0; i < a.stages; ++i)
+                    if (loaded & (1u << i)) mbar_wait(&sm.full[i], (last_parity >> i) & 1u, nullptr);
+                mbar_wait(sm.qfull, 0, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t idesc = umma_idesc_f16_f32(128, 128);
+            const uint32_t a_base = smem_u32(sm.a);
+            const uint32_t q_base = smem_u32(sm.q);
+            const uint32_t qslab = static_cast<uint32_t>(a.nq_pad) * 128u;
+            bool ok = mbar_wait(sm.qfull, 0, abort_flag);
+            for (int n = 0; ok; ++n) {
+                const int slot = n & (kMsRing - 1);
+                if (!mbar_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
+                const bool end = sm.ring[slot * kMsRec + 3] < 0;
+                mbar_arrive(&sm.sempty[slot]);
+                if (end) break;
+                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * 128);
+                for (int g = 0; g < a.kslabs; ++g) {
+                    if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    // A: query rows (rows past nq_pad read what follows in shared memory and only
+                    // reach TMEM lanes no warp reads); B: the tile's 128 document rows
+                    const uint32_t qb = q_base + static_cast<uint32_t>(g) * qslab;
+                    const uint32_t db = a_base + static_cast<uint32_t>(stage) * kMsSlabBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f16(d, umma_desc_sw128(qb + kk * 32u), umma_desc_sw128(db + kk * 32u), idesc,
+                                 (g | kk) ? 1u : 0u);
+                    umma_commit(&sm.empty[stage]);
+                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(&sm.tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                report(a.status, kStTimeout);
+            }
+            umma_commit(sm.done);
+            mbar_wait(sm.done, 0, nullptr);
+        }
+    } else if (warp >= 2 && warp <= 5 && (warp & 3) < nwarps) {
+        // ------------------------------------------------------------ epilogue
+        // Warp w reads TMEM lanes 32 * (w % 4) .. = query rows qw * 32 + lane of the block.
+        const int qw = warp & 3;
+        const bool row_ok = qw * 32 + lane < a.nq;
+        float run = neg_inf;  // this query row's running maximum over the current document
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int n = 0;; ++n) {
+            const int slot = n & (kMsRing - 1);
+            if (!warp_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
+            int4 r[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int4*>(sm.ring + slot * kMsRec + 4 * c);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sempty[slot]);
+            if (r[0].w < 0) break;
+            if (!warp_wait(&sm.tfull[acc], acc_phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            // per chunk: this row's best dot product over the chunk's valid rows
+            float m[4];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + static_cast<uint32_t>(acc * 128);
+            {
+                uint32_t v0[32], v1[32], v2[32], v3[32];  // all four chunks in flight, one wait
+                tmem_ld32(taddr, v0);
+                tmem_ld32(taddr + 32u, v1);
+                tmem_ld32(taddr + 64u, v2);
+                tmem_ld32(taddr + 96u, v3);
+                tmem_ld_wait();
+                m[0] = r[0].x >= 0 ? row_max(v0, r[0].y & 63) : neg_inf;
+                m[1] = r[1].x >= 0 ? row_max(v1, r[1].y & 63) : neg_inf;
+                m[2] = r[2].x >= 0 ? row_max(v2, r[2].y & 63) : neg_inf;
+                m[3] = r[3].x >= 0 ? row_max(v3, r[3].y & 63) : neg_inf;
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+            // fold into the documents, in chunk order; a document's sum at its last chunk
+            const int pb = n & (kMsPartBufs - 1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (r[c].x < 0) continue;
+                run = (r[c].y & kInfoFirst) ? m[c] : fmaxf(run, m[c]);
+                if (r[c].y & kInfoLast) {
+                    const float s = warp_sum(row_ok ? run : 0.f);
+                    if (lane == 0) {
+                        if (nwarps == 1)
+                            a.scores[r[c].x] = a.accumulate ? a.scores[r[c].x] + s : s;
+                        else
+                            sm.part[(pb * 4 + c) * 4 + qw] = s;
+                    }
+                }
+            }
+            if (nwarps > 1 && lane == 0) {
+                // the warp that finishes the tile last adds the warps' sums in warp order
+                __threadfence_block();
+                const int before = atomicAdd(&sm.part_cnt[pb], 1);
+                if (before == nwarps - 1) {
+                    __threadfence_block();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (r[c].x >= 0 && (r[c].y & kInfoLast)) {
+                            float s = 0.f;
+                            for (int w = 0; w < nwarps; ++w) s += sm.part[(pb * 4 + c) * 4 + w];
+                            a.scores[r[c].x] = a.accumulate ? a.scores[r[c].x] + s : s;
+                        }
+                    }
+                    sm.part_cnt[pb] = 0;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            report(a.status, kStTimeout);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+    if (threadIdx.x == 0) {
+        // the last CTA to finish returns the grab counter and this done count to zero, so the
+        // workspace is ready for the next launch (every CTA's atomics have completed by now)
+        __threadfence();
+        if (atomicAdd(a.counter + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(a.counter, 0);
+            atomicExch(a.counter + 1, 0);
+        }
+    }
+    if (threadIdx.x == 0 && blockIdx.x < 152) SEL_PHASE(300 + blockIdx.x);
+}
+
+// Scores of a query with no rows: every document sums nothing.
+__global__ void k_fill_f32(float* out, int n, float v) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) out[i] = v;
+}
+
+size_t maxsim_smem_bytes(int stages, int nq_pad, int kslabs) {
+    return 1024 + static_cast<size_t>(kslabs) * nq_pad * 128u + static_cast<size_t>(stages) * kMsSlabBytes +
+           kMsRing * kMsRec * sizeof(int) + kMsPartBufs * (16 * sizeof(float) + sizeof(int)) + 2 * 2 * 32 * sizeof(int) +
+           (2 * static_cast<size_t>(stages) + 4 + 2 * kMsRing + 2) * 8 + 16;
+}
+
+cudaError_t launch_maxsim(const MaxsimArgs& a, const MaxsimMaps& maps, int grid, size_t smem, cudaStream_t s) {
+    static size_t configured[kMaxDevicesTracked] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_maxsim, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured[dev] = smem;
+    }
+    k_maxsim<<<grid, kMaxsimThreads, smem, s>>>(a, maps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_f32(float* out, int n, float v, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(std::min<int64_t>(1024, (static_cast<int64_t>(n) + 255) / 256));
+    k_fill_f32<<<grid, 256, 0, s>>>(out, n, v);
+    return cudaGetLastError();
+}
+
+}  // namespace sel

@@ -104,6 +104,22 @@ int encode_q_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_str
     return r == CUDA_SUCCESS ? SEL_OK : SEL_ECUDA;
 }
 
+// fp16 [rows][>= d] with row stride `row_stride` elements (a multiple of 8); box = `box_rows`
+// rows x 64 columns in the 128-byte swizzle layout. Rows past `rows` and columns past `d`
+// read as zeros.
+int encode_rows_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t row_stride, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return SEL_ECUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SEL_OK : SEL_ECUDA;
+}
+
 // ------------------------------------------------------------------ planning
 struct TopkPlan {
     int bt_cap = 0;
@@ -496,6 +512,88 @@ int sel_remap_dcp(const int32_t* req_id, int32_t num_reqs, const int32_t* block_
     return launch_remap(a, num_rows, kRemapDcp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SEL_OK
                : SEL_ECUDA;
+}
+
+// ------------------------------------------------------------------ MaxSim rerank
+namespace {
+
+constexpr int kMaxsimMaxD = 1024;
+constexpr size_t kMaxsimQBytes = 64 * 1024;  // query slabs resident per CTA
+constexpr int kMaxsimMaxStages = 12;
+
+// query rows per launch: a multiple of 32, at most 128 (the MMA's M), with the query's K
+// slabs in 64 KiB of shared memory
+int maxsim_nq_cap(int d) {
+    const int kslabs = (d + 63) / 64;
+    return std::min(128, static_cast<int>(kMaxsimQBytes / (static_cast<size_t>(kslabs) * 128)) & ~31);
+}
+
+}  // namespace
+
+size_t sel_maxsim_workspace_bytes(void) { return 256; }
+
+int32_t sel_maxsim_launch_count(int32_t lq, int32_t d) {
+    if (lq <= 0 || d < 1 || d > kMaxsimMaxD) return lq == 0 ? 1 : 0;
+    return static_cast<int32_t>(ceil_div(lq, maxsim_nq_cap(d)));
+}
+
+int sel_maxsim_rerank(const void* q, int32_t lq, int32_t d, int64_t q_stride, const void* docs, int64_t total_tokens,
+                      int64_t doc_stride, const int32_t* doc_offsets, const int32_t* doc_lengths, int32_t num_docs,
+                      float* scores, int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {
+    if (lq < 0 || d < 1 || num_docs < 0 || total_tokens < 0) return SEL_EINVAL;
+    if (num_docs == 0) return SEL_OK;
+    if (!scores || !doc_offsets || !doc_lengths) return SEL_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (lq == 0) return launch_fill_f32(scores, num_docs, 0.0f, s) == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    if (!q || !docs || !ws || total_tokens < 1 || q_stride < d || doc_stride < d) return SEL_EINVAL;
+    if (d > kMaxsimMaxD || total_tokens > INT32_MAX - 64 || q_stride % 8 != 0 || doc_stride % 8 != 0 ||
+        !aligned16(q) || !aligned16(docs) || (reinterpret_cast<uintptr_t>(ws) & 3u) != 0)
+        return SEL_EUNSUPPORTED;
+    if (ws_bytes < sel_maxsim_workspace_bytes()) return SEL_EWORKSPACE;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != SEL_OK) return rc;
+
+    const int kslabs = (d + 63) / 64;
+    const int nq_cap = maxsim_nq_cap(d);
+    // about 8 chunks of 32 rows per grab, judged from the mean rows per document
+    const int64_t mean_rows = std::max<int64_t>(1, total_tokens / num_docs);
+    const int dpg = static_cast<int>(std::min<int64_t>(32, std::max<int64_t>(1, 256 / mean_rows)));
+    const int ngrabs = static_cast<int>(ceil_div(num_docs, dpg));
+    const int grid = std::min(di.sms, ngrabs);
+    MaxsimMaps maps;
+    for (int i = 0; i < kMaxsimDocMaps; ++i)
+        if ((rc = encode_rows_map(&maps.d[i], docs, d, total_tokens, doc_stride, kMaxsimBoxRows[i])) != SEL_OK)
+            return rc;
+    int32_t* counter = static_cast<int32_t*>(ws);
+    for (int q0 = 0; q0 < lq; q0 += nq_cap) {
+        const int nq = std::min(nq_cap, lq - q0);
+        const int nq_pad = (nq + 31) & ~31;
+        int stages = kMaxsimMaxStages;
+        while (stages > 2 && maxsim_smem_bytes(stages, nq_pad, kslabs) > static_cast<size_t>(di.max_smem_optin))
+            --stages;
+        const size_t smem = maxsim_smem_bytes(stages, nq_pad, kslabs);
+        if (smem > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+        if ((rc = encode_rows_map(&maps.q, q, d, lq, q_stride, nq_pad)) != SEL_OK) return rc;
+        MaxsimArgs a{};
+        a.offsets = doc_offsets;
+        a.lengths = doc_lengths;
+        a.num_docs = num_docs;
+        a.docs_per_grab = dpg;
+        a.total_tokens = total_tokens;
+        a.scores = scores;
+        a.accumulate = q0 > 0 ? 1 : 0;
+        a.q_row0 = q0;
+        a.nq = nq;
+        a.nq_pad = nq_pad;
+        a.kslabs = kslabs;
+        a.stages = stages;
+        a.tmem_cols = 256;
+        a.counter = counter;
+        a.status = status;
+        if (launch_maxsim(a, maps, grid, smem, s) != cudaSuccess) return SEL_ECUDA;
+    }
+    return SEL_OK;
 }
 
 int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,

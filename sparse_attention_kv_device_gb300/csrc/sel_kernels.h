@@ -127,6 +127,26 @@ struct RemapArgs {
 
 enum RemapMode { kRemapGlobal = 0, kRemapWorkspace = 1, kRemapDcp = 2 };
 
+// MaxSim rerank (TMA + tcgen05): one block of up to 128 query rows against documents packed
+// in one tensor; CTAs take documents in grabs, the first four static, the rest from `counter`.
+struct MaxsimArgs {
+    const int32_t* offsets;  // [num_docs] first row of each document
+    const int32_t* lengths;  // [num_docs] rows of each document (<= 0: empty)
+    int32_t num_docs;
+    int32_t docs_per_grab;   // 1..32
+    int64_t total_tokens;    // rows of the packed tensor
+    float* scores;           // [num_docs]
+    int32_t accumulate;      // 1: add to scores (a later block of query rows)
+    int32_t q_row0;          // first query row of this block
+    int32_t nq;              // valid query rows of this block
+    int32_t nq_pad;          // nq rounded up to 32 (<= 128): the query rows held in shared memory
+    int32_t kslabs;          // 64-column K slabs (ceil(d / 64))
+    int32_t stages;          // K slabs in flight (<= 16)
+    uint32_t tmem_cols;      // 256: two 128-column accumulators
+    int32_t* counter;        // [2] grab counter and finished-CTA count: zero at the start, zero again at the end
+    int32_t* status;
+};
+
 constexpr int kBuildThreads = 1024;
 constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kTopkThreads = 512;
@@ -136,6 +156,7 @@ constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
+constexpr int kMaxsimThreads = 224;     // warp 0 schedule, 1 MMA + TMEM, 2-5 epilogue (2 also merges), 6 TMA
 
 size_t score_smem_bytes(int stages, int npad_max, int max_segs);
 size_t topk_smem_bytes(int bt_cap);
@@ -150,5 +171,16 @@ cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bo
 cudaError_t launch_remap(const RemapArgs& a, int rows, RemapMode mode, cudaStream_t s);
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
 cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
+size_t maxsim_smem_bytes(int stages, int nq_pad, int kslabs);
+// Tensor maps of one MaxSim launch: the packed tensor with boxes of 8, 16, 24, 32, 64, 96 and
+// 128 rows (64 columns each), and the query block.
+constexpr int kMaxsimDocMaps = 7;
+constexpr int kMaxsimBoxRows[kMaxsimDocMaps] = {8, 16, 24, 32, 64, 96, 128};
+struct MaxsimMaps {
+    CUtensorMap d[kMaxsimDocMaps];
+    CUtensorMap q;
+};
+cudaError_t launch_maxsim(const MaxsimArgs& a, const MaxsimMaps& maps, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_fill_f32(float* out, int n, float v, cudaStream_t s);
 
 }  // namespace sel

@@ -79,9 +79,14 @@ def _load():
     lib.sel_set_trace_events.argtypes = [C.POINTER(C.c_void_p), I32]
     lib.sel_select_launch_count.argtypes = [PP]
     lib.sel_select_launch_count.restype = I32
+    lib.sel_maxsim_workspace_bytes.argtypes = []
+    lib.sel_maxsim_workspace_bytes.restype = SZ
+    lib.sel_maxsim_rerank.argtypes = [P, I32, I32, I64, P, I64, I64, P, P, I32, P, P, P, SZ, P]
+    lib.sel_maxsim_launch_count.argtypes = [I32, I32]
+    lib.sel_maxsim_launch_count.restype = I32
     for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
               "sel_select",
-              "sel_select_static", "sel_select_host", "sel_set_trace_events"):
+              "sel_select_static", "sel_select_host", "sel_set_trace_events", "sel_maxsim_rerank"):
         getattr(lib, f).restype = C.c_int
     return lib
 
@@ -92,7 +97,7 @@ EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_
            "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
            "sel_select",
            "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
-           "sel_select_launch_count"]
+           "sel_select_launch_count", "sel_maxsim_workspace_bytes", "sel_maxsim_rerank", "sel_maxsim_launch_count"]
 
 
 def library_path() -> str:
@@ -382,3 +387,46 @@ def sel_set_trace_events(events) -> None:
 
 def sel_select_launch_count(problem: Problem) -> int:
     return int(_lib.sel_select_launch_count(problem.byref()))
+
+
+def sel_maxsim_workspace_bytes() -> int:
+    return int(_lib.sel_maxsim_workspace_bytes())
+
+
+def sel_maxsim_rerank(q, docs, doc_offsets, doc_lengths, scores=None, status=None, ws=None, stream=None):
+    """MaxSim scores of one query against documents packed in one tensor.
+
+    q fp16 [lq, d]; docs fp16 [total_tokens, d] (the packed tensor, read in place; a row
+    stride above d is allowed); doc_offsets, doc_lengths int32 [B]. Row strides must be
+    multiples of 8 elements. Returns scores fp32 [B]: per query row the best dot product
+    over the document's rows, summed over the query rows (-inf for an empty document).
+    ws (optional): a uint8 device tensor of sel_maxsim_workspace_bytes(), zero-filled before
+    its first use; the kernel leaves it zero-filled, so it can be kept across calls."""
+    _dev(q, torch.float16, "q")
+    _dev(docs, torch.float16, "docs")
+    _dev(doc_offsets, torch.int32, "doc_offsets")
+    _dev(doc_lengths, torch.int32, "doc_lengths")
+    _dev(status, torch.int32, "status")
+    if q.dim() != 2 or docs.dim() != 2 or q.shape[1] != docs.shape[1]:
+        raise ValueError("q [lq, d] and docs [total_tokens, d] must share d")
+    if q.stride(1) != 1 or docs.stride(1) != 1 or not doc_offsets.is_contiguous() or not doc_lengths.is_contiguous():
+        raise ValueError("q and docs need unit column stride; offsets and lengths must be contiguous")
+    if doc_offsets.numel() != doc_lengths.numel():
+        raise ValueError("doc_offsets and doc_lengths differ in length")
+    num_docs = doc_offsets.numel()
+    if scores is None:
+        scores = torch.empty(num_docs, dtype=torch.float32, device=docs.device)
+    _dev(scores, torch.float32, "scores")
+    if ws is None:  # the workspace must start zero-filled (the kernel leaves it so)
+        ws = torch.zeros(sel_maxsim_workspace_bytes(), dtype=torch.uint8, device=docs.device)
+    _dev(ws, torch.uint8, "ws")
+    lq, d = q.shape
+    _check(_lib.sel_maxsim_rerank(_ptr(q), int(lq), int(d), int(q.stride(0)), _ptr(docs), int(docs.shape[0]),
+                                  int(docs.stride(0)), _ptr(doc_offsets), _ptr(doc_lengths), int(num_docs),
+                                  _ptr(scores), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "sel_maxsim_rerank")
+    return scores
+
+
+def sel_maxsim_launch_count(lq: int, d: int) -> int:
+    return int(_lib.sel_maxsim_launch_count(int(lq), int(d)))

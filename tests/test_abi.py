@@ -157,3 +157,40 @@ def test_topk_rejects_bad_arguments(lib):
     assert f(0x1000, 514, 0x2000, 4, 2048, 4, 0x3000, 2052, None, None, None) == -1   # ld not a multiple of 4
     assert f(0x1004, 512, 0x2000, 4, 2048, 4, 0x3000, 2052, None, None, None) == -2   # misaligned scores
     assert f(None, 512, None, 0, 2048, 4, None, 2052, None, None, None) == 0          # empty batch
+
+
+def test_maxsim_rejects_bad_arguments(lib):
+    f = lib.sel_maxsim_rerank
+    f.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int64, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                  C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+    lib.sel_maxsim_workspace_bytes.restype = C.c_size_t
+    wsb = lib.sel_maxsim_workspace_bytes()
+    good = dict(q=0x1000, lq=32, d=128, qs=128, docs=0x2000, tot=1000, ds=128, off=0x3000, ln=0x4000, nd=10,
+                sc=0x5000, ws=0x6000, wsb=wsb)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["q"], a["lq"], a["d"], a["qs"], a["docs"], a["tot"], a["ds"], a["off"], a["ln"], a["nd"],
+                 a["sc"], None, a["ws"], a["wsb"], None)
+
+    assert call(lq=-1) == -1
+    assert call(d=0) == -1
+    assert call(nd=-1) == -1
+    assert call(nd=0, q=None, docs=None, off=None, ln=None, sc=None) == 0   # empty batch: nothing queued
+    assert call(sc=None) == -1
+    assert call(docs=None) == -1
+    assert call(ws=None) == -1
+    assert call(qs=64) == -1                  # row stride below d
+    assert call(tot=0) == -1
+    assert call(d=2048, qs=2048, ds=2048) == -2
+    assert call(qs=132) == -2                 # row stride not a multiple of 8
+    assert call(docs=0x2008) == -2            # misaligned
+    assert call(tot=1 << 31) == -2
+    assert call(wsb=wsb - 1) == -4
+    lib.sel_maxsim_launch_count.restype = C.c_int32
+    assert lib.sel_maxsim_launch_count(32, 128) == 1
+    assert lib.sel_maxsim_launch_count(300, 128) == 3
+    assert lib.sel_maxsim_launch_count(128, 256) == 1
+    assert lib.sel_maxsim_launch_count(128, 512) == 2
+    assert lib.sel_maxsim_launch_count(32, 1024) == 1
+    assert lib.sel_maxsim_launch_count(0, 128) == 1
