@@ -21,14 +21,17 @@
 //     maximum over a chunk's valid rows in registers, folds it into its document's running
 //     maximum, and at the document's last chunk the warp sums its 32 rows; with more than 32
 //     query rows the warp finishing a tile last adds the warps' sums in a fixed order;
-//   * roles: warp 0 schedules (documents -> chunks -> tile records, up to 16 tiles ahead),
-//     warp 6 only issues TMA copies, so the copy engine is never left idle while the schedule
-//     is built; warp 1 issues the MMAs; warps 2-5 are the epilogue;
-//   * CTAs take documents in grabs of docs_per_grab: CTA g's first four grabs are static, the
-//     rest come from an atomic counter in the caller's workspace (the last CTA to finish sets
-//     it back to zero, so no memset is queued), so a CTA's tail is at most one grab; a grab's id and its offsets/lengths are fetched one step
-//     ahead (an atomic, then cp.async), late enough that few claimed documents are left
-//     unscheduled when the counter runs dry. Every document is finished by the CTA that took it.
+//   * roles: warp 1 schedules (documents -> chunks -> tile records, at most 4 tiles ahead of
+//     the copies, so the work a CTA has committed to when the documents run out stays small),
+//     warp 3 only issues TMA copies, so the copy engine is never left idle while the schedule
+//     is built, and forwards each tile's chunk info to the MMA and epilogue; warp 2 issues the MMAs; warps 4-7 are the epilogue (warp 0 idles so that the
+//     busiest epilogue warp has its SM sub-partition to itself);
+//   * CTAs claim consecutive documents: each CTA's first claim is static, later ones come from
+//     an atomic counter in the caller's workspace (the last CTA to finish sets it back to zero,
+//     so no memset is queued), sized ceil(unclaimed / (8 * CTAs)) in [1, 32] documents (guided
+//     self-scheduling: fewer round trips early, one-document claims at the end); the next
+//     claim is taken when the last document of the current one starts, so a CTA never holds
+//     more than one unstarted document. Every document is finished by the CTA that claimed it.
 // Rows outside [0, total_tokens) read as zero vectors (the TMA's out-of-bounds fill).
 #include <algorithm>
 
@@ -41,7 +44,8 @@ SEL_PHASE_TABLE(maxsim)
 
 namespace {
 
-constexpr int kMsRing = 16;                     // tile records published ahead by the scheduler
+constexpr int kMsRing = 4;                      // tile records the scheduler may publish ahead of the TMA issuer
+constexpr int kMsInfo = 8;                      // tiles' chunk info forwarded by the TMA issuer to the MMA / epilogue
 constexpr int kMsRec = 16;                      // ints per tile record: {doc, info, first row, box chunks} x 4
 constexpr uint32_t kMsChunkBytes = 32 * 128;    // 32 rows x 64 fp16 columns
 constexpr uint32_t kMsSlabBytes = 4 * kMsChunkBytes;  // one 128-row K slab of a tile
@@ -50,6 +54,15 @@ constexpr int kMsPartBufs = 4;                  // tiles whose per-warp sums may
 // chunk info word: rows valid (1..32) | first chunk of its document << 6 | last << 7
 constexpr int kInfoFirst = 64;
 constexpr int kInfoLast = 128;
+
+// Warp roles. A warp issues on SM sub-partition warp % 4, and the epilogue warp of query
+// rows 0-31 (the only busy one for up to 32 query rows) must be a warp with warp % 4 == 0
+// (TMEM lanes 0-31); the scheduler, MMA and TMA warps sit on sub-partitions 1-3 and warp 0
+// idles, so that warp has its sub-partition to itself.
+constexpr int kWarpSched = 1;
+constexpr int kWarpMma = 2;
+constexpr int kWarpTma = 3;
+constexpr int kWarpEpi = 4;  // warps 4-7: query rows 32 * (warp % 4) ..
 
 struct MsSmem {
     uint8_t* q;          // kslabs x nq_pad x 128 B (the query block, K slab by K slab)
@@ -64,8 +77,11 @@ struct MsSmem {
     uint64_t* empty;     // [stages]
     uint64_t* tfull;     // [2]
     uint64_t* tempty;    // [2]
+    int* info;           // [kMsInfo][8] per tile, {doc, info} of chunks 0..3; info of chunk 0 = -1: end
     uint64_t* sfull;     // [kMsRing]
-    uint64_t* sempty;    // [kMsRing] read by the TMA thread, the MMA thread and the epilogue warps
+    uint64_t* sempty;    // [kMsRing] read by the TMA thread
+    uint64_t* ifull;     // [kMsInfo]
+    uint64_t* iempty;    // [kMsInfo] read by the MMA thread and the epilogue warps
     uint64_t* qfull;     // [1]
     uint64_t* done;      // [1]
     uint32_t* tmem_base;
@@ -82,6 +98,8 @@ __device__ __forceinline__ MsSmem ms_carve(uint8_t* raw, int stages, int nq_pad,
     p += static_cast<size_t>(stages) * kMsSlabBytes;
     s.ring = reinterpret_cast<int*>(p);
     p += kMsRing * kMsRec * sizeof(int);
+    s.info = reinterpret_cast<int*>(p);
+    p += kMsInfo * 8 * sizeof(int);
     s.part = reinterpret_cast<float*>(p);
     p += kMsPartBufs * 16 * sizeof(float);
     s.part_cnt = reinterpret_cast<int*>(p);
@@ -97,7 +115,9 @@ __device__ __forceinline__ MsSmem ms_carve(uint8_t* raw, int stages, int nq_pad,
     s.tempty = s.tfull + 2;
     s.sfull = s.tempty + 2;
     s.sempty = s.sfull + kMsRing;
-    s.qfull = s.sempty + kMsRing;
+    s.ifull = s.sempty + kMsRing;
+    s.iempty = s.ifull + kMsInfo;
+    s.qfull = s.iempty + kMsInfo;
     s.done = s.qfull + 1;
     uint32_t* w = reinterpret_cast<uint32_t*>(s.done + 1);
     s.tmem_base = w;
@@ -157,13 +177,13 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
     const bool tr = blockIdx.x == 0;
     (void)tr;
     if (tr && threadIdx.x == 0) SEL_PHASE(0);
-    // the scheduler's first round trips start before the setup: the atomic for the CTA's
-    // grab 4 and the offsets/lengths of its grab 0 (blockIdx.x, always < the grab count)
-    int pend = 0;  // warp 0, lane 0: an atomic's value in flight
-    if (warp == 0) {
-        if (lane == 0) pend = atomicAdd(a.counter, 1);
-        const int doc = static_cast<int>(blockIdx.x) * a.docs_per_grab + lane;
-        if (lane < a.docs_per_grab && doc < a.num_docs) {
+    // the scheduler's first round trips start before the setup: the offsets/lengths of the
+    // CTA's static first claim and the atomic for its second claim
+    int pend = 0;  // scheduler warp, lane 0: an atomic's value in flight
+    if (warp == kWarpSched) {
+        if (lane == 0) pend = atomicAdd(a.counter, a.first_claim);
+        const int doc = static_cast<int>(blockIdx.x) * a.first_claim + lane;
+        if (lane < a.first_claim && doc < a.num_docs) {
             cp_async_4(&sm.qoff[lane], a.offsets + doc);
             cp_async_4(&sm.qlen[lane], a.lengths + doc);
         }
@@ -181,7 +201,11 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         }
         for (int i = 0; i < kMsRing; ++i) {
             mbar_init(&sm.sfull[i], 1);
-            mbar_init(&sm.sempty[i], 2 + nwarps);
+            mbar_init(&sm.sempty[i], 1);
+        }
+        for (int i = 0; i < kMsInfo; ++i) {
+            mbar_init(&sm.ifull[i], 1);
+            mbar_init(&sm.iempty[i], 1 + nwarps);
         }
         for (int i = 0; i < kMsPartBufs; ++i) sm.part_cnt[i] = 0;
         mbar_init(sm.qfull, 1);
@@ -189,9 +213,9 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         *sm.abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 6 && lane < kMaxsimDocMaps) tma_prefetch_desc(&tmap_d[lane]);
-    if (warp == 6 && lane == kMaxsimDocMaps) tma_prefetch_desc(&tmap_q);
-    if (warp == 1) {
+    if (warp == kWarpTma && lane < kMaxsimDocMaps) tma_prefetch_desc(&tmap_d[lane]);
+    if (warp == kWarpTma && lane == kMaxsimDocMaps) tma_prefetch_desc(&tmap_q);
+    if (warp == kWarpMma) {
         tmem_alloc(sm.tmem_base, a.tmem_cols);
         tmem_relinquish();
     }
@@ -203,43 +227,45 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
     if (tr && threadIdx.x == 0) SEL_PHASE(1);
     const float neg_inf = -__int_as_float(0x7f800000);
 
-    if (warp == 0) {
+    if (warp == kWarpSched) {
         // ------------------------------------------------------------ scheduler: documents -> chunks -> tiles
-        const int dpg = a.docs_per_grab;
-        const int ngrabs = (a.num_docs + dpg - 1) / dpg;
-        // Document source, in grabs of dpg documents. The CTA's grab s is static for s < 4
-        // (blockIdx.x + s * gridDim.x, no atomic), else 4 * gridDim.x + an atomic counter value.
-        // Claims are made as late as the round trips allow, so that few claimed documents are
-        // still unscheduled when the counter runs dry (they decide the CTAs' tails): one atomic
-        // is in flight (issued one step before its value is needed), and at step s (consuming
-        // grab s) the id of grab s + 1 is resolved and its offsets and lengths are copied by
-        // cp.async into a shared-memory queue slot.
+        // Document source: claims of consecutive documents (guided self-scheduling). The CTA's
+        // first claim is static, first_claim documents from blockIdx.x * first_claim; later ones
+        // come from an atomic counter (claim_base + its value), each sized from the documents
+        // still unclaimed, ceil(remaining / (8 * CTAs)) clamped to [1, 32]: several while much is
+        // left (fewer round trips), one document at the end (balanced tails). One atomic is in
+        // flight (issued when the previous claim is resolved; a single thread issues them, so
+        // their values rise in issue order), and a claim's offsets and lengths are copied by
+        // cp.async into a queue slot.
+        const int nd = a.num_docs;
+        const int G = static_cast<int>(gridDim.x);
+        int pend_k = a.first_claim;  // size of the claim in flight
         bool has_pend = true;        // warp-uniform: `pend` holds an atomic in flight
-        bool issuing = true;
-        auto fetch_meta = [&](int s, int g) {  // cp.async the grab's offsets and lengths into queue slot s % 2
-            const int doc = g * dpg + lane;
-            if (g >= 0 && lane < dpg && doc < a.num_docs) {
-                cp_async_4(&sm.qoff[(s & 1) * 32 + lane], a.offsets + doc);
-                cp_async_4(&sm.qlen[(s & 1) * 32 + lane], a.lengths + doc);
+        auto fetch_meta = [&](int s, int start, int cnt) {  // cp.async a claim's offsets and lengths into slot s % 2
+            if (lane < cnt) {
+                cp_async_4(&sm.qoff[(s & 1) * 32 + lane], a.offsets + start + lane);
+                cp_async_4(&sm.qlen[(s & 1) * 32 + lane], a.lengths + start + lane);
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        auto resolve = [&](int s) -> int {  // the id of grab s, -1 if none; warp-uniform
-            int id = -1;
-            if (s < 4) {
-                id = static_cast<int>(blockIdx.x) + s * static_cast<int>(gridDim.x);
-            } else if (has_pend) {
-                id = 4 * static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, pend, 0);
-                has_pend = id < ngrabs && issuing;
-                if (has_pend && lane == 0) pend = atomicAdd(a.counter, 1);
+        auto resolve = [&](int& start, int& cnt) {  // the next claim (cnt 0: none); warp-uniform
+            start = 0;
+            cnt = 0;
+            if (!has_pend) return;
+            const int v = __shfl_sync(0xffffffffu, pend, 0);
+            has_pend = false;
+            if (v >= nd - a.claim_base) return;  // counter past the end: no claim, no more atomics
+            start = a.claim_base + v;
+            cnt = min(pend_k, nd - start);
+            const int left = nd - start - cnt;
+            if (left > 0) {
+                pend_k = min(32, max(1, (left + 8 * G - 1) / (8 * G)));
+                if (lane == 0) pend = atomicAdd(a.counter, pend_k);
+                has_pend = true;
             }
-            if (id >= ngrabs) {
-                id = -1;
-                issuing = false;
-            }
-            return id;
         };
-        int gid0 = resolve(0);  // its metadata copy was started before the setup
+        int start0 = static_cast<int>(blockIdx.x) * a.first_claim;  // its metadata copy started before the setup
+        int cnt0 = max(0, min(a.first_claim, nd - start0));
         // the tile being gathered: lane c < nc holds chunk c
         int nc = 0, my_doc = -1, my_info = 0, my_row = 0;
         int n = 0;
@@ -287,23 +313,30 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             return true;
         };
 
+        // The claim in hand is consumed document by document; the next claim is resolved (and
+        // its metadata copy started) only when the last document of this one begins, so a CTA
+        // holds at most one document beyond what it is scheduling.
         for (int step = 0; ok; ++step) {
-            // grab step + 1: resolve its id and start its metadata copy
-            const int gid1 = resolve(step + 1);
-            fetch_meta(step + 1, gid1);
-            if (gid0 < 0 && gid1 < 0 && !has_pend) break;  // nothing left anywhere
-            // grab step's metadata (copied one step ago): wait for all but the newest group
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            const int g = gid0;
+            if (cnt0 == 0) {  // nothing in hand (an empty first claim): resolve one now
+                if (!has_pend) break;
+                resolve(start0, cnt0);
+                fetch_meta(step, start0, cnt0);
+                if (cnt0 == 0) break;  // the counter is past the end
+            }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");  // this claim's metadata
+            const int base_doc = start0, ndocs = cnt0;
             int cur_off = 0, cur_len = 0;
-            if (g >= 0 && lane < dpg && g * dpg + lane < a.num_docs) {  // each lane reads what it copied
+            if (lane < ndocs) {  // each lane reads what it copied
                 cur_off = sm.qoff[(step & 1) * 32 + lane];
                 cur_len = sm.qlen[(step & 1) * 32 + lane];
             }
-            gid0 = gid1;
-            for (int i = 0; g >= 0 && i < dpg && ok; ++i) {
-                const int doc = g * dpg + i;
-                if (doc >= a.num_docs) break;
+            cnt0 = 0;
+            for (int i = 0; i < ndocs && ok; ++i) {
+                if (i == ndocs - 1) {  // the last document: line up the next claim
+                    resolve(start0, cnt0);
+                    fetch_meta(step + 1, start0, cnt0);
+                }
+                const int doc = base_doc + i;
                 const int off = __shfl_sync(0xffffffffu, cur_off, i);
                 const int len = __shfl_sync(0xffffffffu, cur_len, i);
                 if (len <= 0) {
@@ -334,7 +367,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             *abort_flag = 1;
             report(a.status, kStTimeout);
         }
-    } else if (warp == 6) {
+    } else if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA issuer
         if (lane == 0) {
             const uint64_t pol_d = l2_policy_evict_first();
@@ -353,6 +386,15 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int4*>(sm.ring + slot * kMsRec + 4 * c);
                 mbar_arrive(&sm.sempty[slot]);
+                // forward the chunks' {doc, info} (or the end) to the MMA thread and the epilogue
+                const int islot = n & (kMsInfo - 1);
+                if (!mbar_wait(&sm.iempty[islot], ((n / kMsInfo) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                {
+                    int4* dst = reinterpret_cast<int4*>(sm.info + islot * 8);
+                    dst[0] = make_int4(r[0].x, r[0].w < 0 ? -1 : r[0].y, r[1].x, r[1].y);
+                    dst[1] = make_int4(r[2].x, r[2].y, r[3].x, r[3].y);
+                }
+                mbar_arrive(&sm.ifull[islot]);
                 if (r[0].w < 0) break;
                 const uint32_t bytes = static_cast<uint32_t>(max(r[0].w, 0) + max(r[1].w, 0) + max(r[2].w, 0) +
                                                              max(r[3].w, 0)) * 128u;
@@ -391,7 +433,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
                 mbar_wait(sm.qfull, 0, nullptr);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             int stage = 0, acc = 0;
@@ -402,10 +444,10 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             const uint32_t qslab = static_cast<uint32_t>(a.nq_pad) * 128u;
             bool ok = mbar_wait(sm.qfull, 0, abort_flag);
             for (int n = 0; ok; ++n) {
-                const int slot = n & (kMsRing - 1);
-                if (!mbar_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
-                const bool end = sm.ring[slot * kMsRec + 3] < 0;
-                mbar_arrive(&sm.sempty[slot]);
+                const int islot = n & (kMsInfo - 1);
+                if (!mbar_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag)) { ok = false; break; }
+                const bool end = sm.info[islot * 8 + 1] < 0;
+                mbar_arrive(&sm.iempty[islot]);
                 if (end) break;
                 if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -436,7 +478,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             umma_commit(sm.done);
             mbar_wait(sm.done, 0, nullptr);
         }
-    } else if (warp >= 2 && warp <= 5 && (warp & 3) < nwarps) {
+    } else if (warp >= kWarpEpi && (warp & 3) < nwarps) {
         // ------------------------------------------------------------ epilogue
         // Warp w reads TMEM lanes 32 * (w % 4) .. = query rows qw * 32 + lane of the block.
         const int qw = warp & 3;
@@ -446,14 +488,14 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int n = 0;; ++n) {
-            const int slot = n & (kMsRing - 1);
-            if (!warp_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
-            int4 r[4];
+            const int islot = n & (kMsInfo - 1);
+            if (!warp_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag)) { ok = false; break; }
+            int2 r[4];  // {doc (-1: none), info} of chunks 0..3
 #pragma unroll
-            for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int4*>(sm.ring + slot * kMsRec + 4 * c);
+            for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int2*>(sm.info + islot * 8 + 2 * c);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.sempty[slot]);
-            if (r[0].w < 0) break;
+            if (lane == 0) mbar_arrive(&sm.iempty[islot]);
+            if (r[0].y < 0) break;
             if (!warp_wait(&sm.tfull[acc], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
             // per chunk: this row's best dot product over the chunk's valid rows
@@ -518,7 +560,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tmem_dealloc(tmem, a.tmem_cols);
     }
@@ -541,8 +583,8 @@ __global__ void k_fill_f32(float* out, int n, float v) {
 
 size_t maxsim_smem_bytes(int stages, int nq_pad, int kslabs) {
     return 1024 + static_cast<size_t>(kslabs) * nq_pad * 128u + static_cast<size_t>(stages) * kMsSlabBytes +
-           kMsRing * kMsRec * sizeof(int) + kMsPartBufs * (16 * sizeof(float) + sizeof(int)) + 2 * 2 * 32 * sizeof(int) +
-           (2 * static_cast<size_t>(stages) + 4 + 2 * kMsRing + 2) * 8 + 16;
+           kMsRing * kMsRec * sizeof(int) + kMsInfo * 8 * sizeof(int) + kMsPartBufs * (16 * sizeof(float) + sizeof(int)) +
+           2 * 2 * 32 * sizeof(int) + (2 * static_cast<size_t>(stages) + 4 + 2 * kMsRing + 2 * kMsInfo + 2) * 8 + 16;
 }
 
 cudaError_t launch_maxsim(const MaxsimArgs& a, const MaxsimMaps& maps, int grid, size_t smem, cudaStream_t s) {

@@ -556,11 +556,10 @@ int sel_maxsim_rerank(const void* q, int32_t lq, int32_t d, int64_t q_stride, co
 
     const int kslabs = (d + 63) / 64;
     const int nq_cap = maxsim_nq_cap(d);
-    // about 8 chunks of 32 rows per grab, judged from the mean rows per document
-    const int64_t mean_rows = std::max<int64_t>(1, total_tokens / num_docs);
-    const int dpg = static_cast<int>(std::min<int64_t>(32, std::max<int64_t>(1, 256 / mean_rows)));
-    const int ngrabs = static_cast<int>(ceil_div(num_docs, dpg));
-    const int grid = std::min(di.sms, ngrabs);
+    // each CTA's static first claim: about an eighth of its share of the documents (<= 32)
+    const int g0 = std::min(di.sms, num_docs);
+    const int first_claim = std::max(1, std::min(32, num_docs / (8 * g0)));
+    const int grid = std::min<int>(g0, static_cast<int>(ceil_div(num_docs, first_claim)));
     MaxsimMaps maps;
     for (int i = 0; i < kMaxsimDocMaps; ++i)
         if ((rc = encode_rows_map(&maps.d[i], docs, d, total_tokens, doc_stride, kMaxsimBoxRows[i])) != SEL_OK)
@@ -579,7 +578,8 @@ int sel_maxsim_rerank(const void* q, int32_t lq, int32_t d, int64_t q_stride, co
         a.offsets = doc_offsets;
         a.lengths = doc_lengths;
         a.num_docs = num_docs;
-        a.docs_per_grab = dpg;
+        a.first_claim = first_claim;
+        a.claim_base = grid * first_claim;
         a.total_tokens = total_tokens;
         a.scores = scores;
         a.accumulate = q0 > 0 ? 1 : 0;

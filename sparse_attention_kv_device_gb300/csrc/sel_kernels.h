@@ -128,12 +128,13 @@ struct RemapArgs {
 enum RemapMode { kRemapGlobal = 0, kRemapWorkspace = 1, kRemapDcp = 2 };
 
 // MaxSim rerank (TMA + tcgen05): one block of up to 128 query rows against documents packed
-// in one tensor; CTAs take documents in grabs, the first four static, the rest from `counter`.
+// in one tensor; CTAs claim documents, the first claim static, the rest through `counter`.
 struct MaxsimArgs {
     const int32_t* offsets;  // [num_docs] first row of each document
     const int32_t* lengths;  // [num_docs] rows of each document (<= 0: empty)
     int32_t num_docs;
-    int32_t docs_per_grab;   // 1..32
+    int32_t first_claim;     // documents in each CTA's static first claim (1..32)
+    int32_t claim_base;      // gridDim.x * first_claim: the first document the counter hands out
     int64_t total_tokens;    // rows of the packed tensor
     float* scores;           // [num_docs]
     int32_t accumulate;      // 1: add to scores (a later block of query rows)
@@ -156,7 +157,7 @@ constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
-constexpr int kMaxsimThreads = 224;     // warp 0 schedule, 1 MMA + TMEM, 2-5 epilogue (2 also merges), 6 TMA
+constexpr int kMaxsimThreads = 256;     // warp 1 schedule, 2 MMA + TMEM, 3 TMA, 4-7 epilogue, 0 idle
 
 size_t score_smem_bytes(int stages, int npad_max, int max_segs);
 size_t topk_smem_bytes(int bt_cap);
