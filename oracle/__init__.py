@@ -77,6 +77,9 @@ def _load(path: str):
     L.orc_dcp_local_index.restype = I64
     L.orc_remap_dcp_rows.argtypes = [P, I32, P, I64, I32, I32, P, I32, I32, I32, I32, I32, I32, I32, P, P]
     L.orc_maxsim.argtypes = [P, I32, I32, P, I64, I64, P, P, I32, P, P]
+    L.orc_bf16_to_double.argtypes = [C.c_uint16]
+    L.orc_bf16_to_double.restype = C.c_double
+    L.orc_mla_decode.argtypes = [P, P, I32, I32, I32, I32, P, I64, P, I64, I64, P, I32, P, C.c_double, P, P]
     L.orc_select.argtypes = [C.POINTER(_Problem), P, I32, I32, P, P, P, P, P, I64]
     L.orc_select.restype = I32
     L.orc_score_rows.argtypes = [C.POINTER(_Problem), P, I32, P, P, I64]
@@ -206,6 +209,34 @@ def maxsim(q, docs, offsets, lengths):
     bound = np.empty(of.size, dtype=np.float64)
     lib().orc_maxsim(_p(qb), lq, d, _p(db), db.shape[1], db.shape[0], _p(of), _p(ln), of.size, _p(scores), _p(bound))
     return scores, bound
+
+
+def bf16_to_double(bits) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64, decoded by the oracle's C routine."""
+    b = _c(bits, np.uint16).ravel()
+    return np.array([lib().orc_bf16_to_double(int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
+
+
+def mla_decode(q_nope, q_pe, ckv, kpe, slots, kv_len, sm_scale):
+    """Sparse MLA decode attention over selected slots (vLLM page "flashinfer_mla_sparse_sm90",
+    _SM90State). bf16 inputs as uint16 bit patterns: q_nope [rows, heads, dc], q_pe
+    [rows, heads, dr] (dr may be 0), ckv [num_slots, >= dc], kpe [num_slots, >= dr],
+    slots int32 [rows, width], kv_len int32 [rows]. Returns (out float64 [rows, heads, dc],
+    lse float64 [rows, heads])."""
+    qn = _c(q_nope, np.uint16)
+    qp = _c(q_pe, np.uint16)
+    ck = _c(ckv, np.uint16)
+    kp = _c(kpe, np.uint16)
+    sl = _c(slots, np.int32)
+    kl = _c(kv_len, np.int32)
+    rows, heads, dc = qn.shape
+    dr = qp.shape[2]
+    out = np.empty((rows, heads, dc), dtype=np.float64)
+    lse = np.empty((rows, heads), dtype=np.float64)
+    lib().orc_mla_decode(_p(qn), _p(qp), rows, heads, dc, dr, _p(ck), ck.shape[1], _p(kp),
+                         kp.shape[1] if kp.ndim == 2 else 0, ck.shape[0], _p(sl), sl.shape[1], _p(kl),
+                         float(sm_scale), _p(out), _p(lse))
+    return out, lse
 
 
 class _Held:

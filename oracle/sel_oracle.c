@@ -34,7 +34,8 @@
  *   7. valid count = number of entries that are not -1 ("the count of valid
  *      (non -1) indices per row").
  *
- * Also here: the MaxSim rerank of a query against packed documents (orc_maxsim).
+ * Also here: the MaxSim rerank of a query against packed documents (orc_maxsim), and the
+ * sparse MLA decode attention over the selected slots (orc_mla_decode).
  *
  * The remap also has the page's two other modes: prefill rows mapped into a prefill
  * workspace (orc_remap_ws_rows) and a decode-context-parallel rank's filter with optional
@@ -368,6 +369,83 @@ void orc_maxsim(const uint16_t *q, int32_t lq, int32_t d, const uint16_t *docs, 
         if (abs_bound)
             abs_bound[i] = bound;
     }
+}
+
+/* bfloat16 bit pattern -> double: the top 16 bits of a binary32 (the format's definition). */
+double orc_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Sparse MLA decode attention over selected KV slots (vLLM page
+ * "flashinfer_mla_sparse_sm90", _SM90State: FlashInfer's BatchMLAPagedAttentionWrapper planned
+ * with page_size 1 -- the selected slots are the page table --, head_dim_ckv = kv_lora_rank,
+ * qk_rope_head_dim 0 or 64, no causal mask, sm_scale, bf16 queries, and the exact per-row
+ * kv_len of _kv_lens_host; entries past kv_len (the -1 tail) are never read).
+ * The MLA computation in its absorbed form (the wrapper's head_dim_ckv output): for row r,
+ * head h and each entry j < kv_len[r] whose slot s = slots[r][j] lies in [0, num_slots)
+ * (a -1 or out-of-range slot inside kv_len contributes nothing):
+ *     logit_j    = sm_scale * (q_nope[r][h] . ckv[s] + q_pe[r][h] . kpe[s])
+ *     out[r][h]  = sum_j exp(logit_j - m) * ckv[s_j] / sum_j exp(logit_j - m),  m = max_j logit_j
+ *     lse[r][h]  = m + log(sum_j exp(logit_j - m))           (natural logarithm)
+ * A row with no such entry gives out = 0 and lse = -inf. Every input is bf16 (given as bit
+ * patterns); the dot products, exponentials and sums are taken in double.
+ * Layouts: q_nope [rows][heads][dc], q_pe [rows][heads][dr], ckv row s at s * ckv_stride,
+ * kpe row s at s * kpe_stride (unused when dr == 0), slots [rows][width], out [rows][heads][dc],
+ * lse [rows][heads]. */
+void orc_mla_decode(const uint16_t *q_nope, const uint16_t *q_pe, int32_t rows, int32_t heads,
+                    int32_t dc, int32_t dr, const uint16_t *ckv, int64_t ckv_stride,
+                    const uint16_t *kpe, int64_t kpe_stride, int64_t num_slots, const int32_t *slots,
+                    int32_t width, const int32_t *kv_len, double sm_scale, double *out, double *lse)
+{
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(width > 0 ? width : 1));
+    for (int32_t r = 0; r < rows; ++r) {
+        const int32_t n = kv_len[r] < width ? kv_len[r] : width;
+        for (int32_t h = 0; h < heads; ++h) {
+            const uint16_t *qn = q_nope + ((int64_t)r * heads + h) * dc;
+            const uint16_t *qp = q_pe + ((int64_t)r * heads + h) * dr;
+            double *o = out + ((int64_t)r * heads + h) * dc;
+            double m = -INFINITY;
+            int any = 0;
+            for (int32_t j = 0; j < n; ++j) {
+                const int64_t sl = slots[(int64_t)r * width + j];
+                if (sl < 0 || sl >= num_slots)
+                    continue;
+                double acc = 0.0;
+                for (int32_t d = 0; d < dc; ++d)
+                    acc += orc_bf16_to_double(qn[d]) * orc_bf16_to_double(ckv[sl * ckv_stride + d]);
+                for (int32_t d = 0; d < dr; ++d)
+                    acc += orc_bf16_to_double(qp[d]) * orc_bf16_to_double(kpe[sl * kpe_stride + d]);
+                logit[j] = sm_scale * acc;
+                if (logit[j] > m)
+                    m = logit[j];
+                any = 1;
+            }
+            for (int32_t d = 0; d < dc; ++d)
+                o[d] = 0.0;
+            if (!any) {
+                lse[(int64_t)r * heads + h] = -INFINITY;
+                continue;
+            }
+            double z = 0.0;
+            for (int32_t j = 0; j < n; ++j) {
+                const int64_t sl = slots[(int64_t)r * width + j];
+                if (sl < 0 || sl >= num_slots)
+                    continue;
+                const double p = exp(logit[j] - m);
+                z += p;
+                for (int32_t d = 0; d < dc; ++d)
+                    o[d] += p * orc_bf16_to_double(ckv[sl * ckv_stride + d]);
+            }
+            for (int32_t d = 0; d < dc; ++d)
+                o[d] /= z;
+            lse[(int64_t)r * heads + h] = m + log(z);
+        }
+    }
+    free(logit);
 }
 
 typedef struct {

@@ -450,6 +450,139 @@ def pin_maxsim_normal_bound(orc, seed=47):
         assert abs(s[i] - ref) <= 2.0 ** -23 * abs(ref) + 1e-12 * absb, (i, s[i], ref)
         assert abs(b[i] - absb) <= 1e-12 * absb, (i, b[i], absb)
 
+
+# ---------------------------------------------------------------- sparse MLA decode attention
+def _bf(x):
+    """float values that are exact in bfloat16 -> their bit patterns."""
+    return (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def pin_bf16_decode(orc):
+    """bfloat16 decoding of all 65,536 bit patterns equals torch's bfloat16 -> float64."""
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = orc.bf16_to_double(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_mla_worked_example(orc):
+    """Hand-worked fixture (tests/golden/mla_worked_example.txt): weights 1 : 2 : 4 from
+    sm_scale = ln 2, a -1 inside kv_len, an entry past kv_len, an empty row, one entry."""
+    import _golden
+    d = _golden.load("mla_worked_example.txt")
+    qn = _bf(_golden.floats(d, "q_nope").reshape(3, 1, 2))
+    qp = _bf(_golden.floats(d, "q_pe").reshape(3, 1, 1))
+    ckv = _bf(_golden.floats(d, "ckv").reshape(8, 2))
+    kpe = _bf(_golden.floats(d, "kpe").reshape(8, 1))
+    slots = np.stack([_golden.ints(d, f"slots_row{r}") for r in range(3)]).astype(np.int32)
+    out, lse = orc.mla_decode(qn, qp, ckv, kpe, slots, _golden.ints(d, "kv_len"), float(d["sm_scale"][0]))
+    for r in range(3):
+        assert np.allclose(out[r, 0], _golden.floats(d, f"out_row{r}").astype(np.float64), rtol=1e-7, atol=1e-7), r
+    want = np.array([float(x) for x in d["lse"]])
+    assert np.array_equal(np.isinf(lse[:, 0]), np.isinf(want))
+    fin = ~np.isinf(want)
+    assert np.allclose(lse[fin, 0], want[fin], rtol=1e-12, atol=1e-12), lse
+
+
+def _mla_int_inputs(rng, rows, heads, dc, dr, num_slots, lo=-3, hi=4):
+    qn = rng.integers(lo, hi, size=(rows, heads, dc)).astype(np.float32)
+    qp = rng.integers(lo, hi, size=(rows, heads, dr)).astype(np.float32)
+    ckv = rng.integers(lo, hi, size=(num_slots, dc)).astype(np.float32)
+    kpe = rng.integers(lo, hi, size=(num_slots, dr)).astype(np.float32)
+    return qn, qp, ckv, kpe
+
+
+def pin_mla_single_entry(orc, seed=51):
+    """One valid entry: the softmax is 1, so out is that slot's ckv row exactly and lse is its
+    logit, sm_scale times the exact int64 dot product (numpy)."""
+    rng = np.random.default_rng(seed)
+    qn, qp, ckv, kpe = _mla_int_inputs(rng, 4, 3, 16, 4, 10)
+    slots = np.array([[7, -1], [0, 3], [9, 9], [-1, 2]], np.int32)
+    kv_len = np.array([1, 1, 1, 2], np.int32)
+    scale = 0.125
+    out, lse = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), slots, kv_len, scale)
+    for r, s_ in enumerate([7, 0, 9, 2]):
+        for h in range(3):
+            assert np.array_equal(out[r, h], ckv[s_].astype(np.float64)), (r, h)
+            dot = int(qn[r, h].astype(np.int64) @ ckv[s_].astype(np.int64) + qp[r, h].astype(np.int64) @ kpe[s_].astype(np.int64))
+            assert lse[r, h] == scale * dot, (r, h, lse[r, h], scale * dot)
+
+
+def pin_mla_uniform(orc, seed=53):
+    """Zero queries: every logit is 0, so out is the plain mean of the row's valid ckv rows
+    and lse = log(number of valid entries)."""
+    rng = np.random.default_rng(seed)
+    _, _, ckv, kpe = _mla_int_inputs(rng, 1, 1, 8, 2, 30)
+    qn = np.zeros((2, 2, 8), np.float32)
+    qp = np.zeros((2, 2, 2), np.float32)
+    slots = np.array([[3, 11, -1, 29, 4, 40], [5, 6, 7, 8, 9, 10]], np.int32)
+    kv_len = np.array([6, 4], np.int32)
+    out, lse = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), slots, kv_len, 0.3)
+    for r, valid in enumerate([[3, 11, 29, 4], [5, 6, 7, 8]]):   # slot 40 is past num_slots = 30
+        ref = ckv[valid].astype(np.float64).mean(axis=0)
+        for h in range(2):
+            assert np.allclose(out[r, h], ref, rtol=1e-14, atol=1e-14), (r, h)
+            assert abs(lse[r, h] - np.log(len(valid))) < 1e-14
+
+
+def pin_mla_entry_set(orc, seed=55):
+    """The result depends only on the set of valid entries inside kv_len: permuting them, adding
+    -1 or out-of-range slots inside kv_len, or valid slots past kv_len changes nothing."""
+    rng = np.random.default_rng(seed)
+    qn, qp, ckv, kpe = _mla_int_inputs(rng, 1, 4, 32, 8, 64)
+    qn, qp = qn / 8, qp / 8
+    base = rng.choice(64, size=12, replace=False).astype(np.int32)
+    a = np.concatenate([base, np.full(4, -1, np.int32)])[None, :]
+    perm = rng.permutation(base)
+    b = np.concatenate([perm[:5], [-1, 70, -1], perm[5:], [0, 1, 2, 3, 5]]).astype(np.int32)[None, :]
+    out_a, lse_a = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), a, np.array([12], np.int32), 0.25)
+    out_b, lse_b = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), b, np.array([15], np.int32), 0.25)
+    assert np.allclose(out_a, out_b, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse_a, lse_b, rtol=1e-12, atol=1e-12)
+
+
+def pin_mla_shift(orc, seed=57):
+    """A constant added to every logit (a rotary key shared by all slots) leaves out unchanged
+    and moves lse by that constant."""
+    rng = np.random.default_rng(seed)
+    qn, _, ckv, _ = _mla_int_inputs(rng, 2, 2, 16, 4, 20)
+    kpe = np.ones((20, 4), np.float32)
+    qp0 = np.zeros((2, 2, 4), np.float32)
+    qp1 = np.full((2, 2, 4), 1.5, np.float32)        # q_pe . kpe = 6 for every slot
+    slots = rng.permutation(20)[:10].astype(np.int32).reshape(2, 5)
+    kv_len = np.array([5, 3], np.int32)
+    o0, l0 = orc.mla_decode(_bf(qn), _bf(qp0), _bf(ckv), _bf(kpe), slots, kv_len, 0.5)
+    o1, l1 = orc.mla_decode(_bf(qn), _bf(qp1), _bf(ckv), _bf(kpe), slots, kv_len, 0.5)
+    assert np.allclose(o0, o1, rtol=1e-12, atol=1e-12)
+    assert np.allclose(l1 - l0, 3.0, rtol=0, atol=1e-12)
+
+
+def pin_mla_large_logits(orc):
+    """Logits in the thousands (no overflow): a slot whose logit exceeds the others by 1000
+    takes all the weight, so out is its ckv row and lse its logit, exactly."""
+    ckv = np.array([[1, 2], [3, -4], [5, 6]], np.float32)
+    kpe = np.array([[0], [0], [0]], np.float32)
+    qn = np.array([[[1000, 1000]]], np.float32)        # dots 3000, -1000, 11000
+    qp = np.zeros((1, 1, 1), np.float32)
+    out, lse = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), np.array([[0, 1, 2]], np.int32),
+                              np.array([3], np.int32), 1.0)
+    assert np.array_equal(out[0, 0], [5.0, 6.0]) and lse[0, 0] == 11000.0, (out, lse)
+
+
+def pin_mla_duplicate_slot(orc):
+    """A slot listed twice counts twice: with logits 0, 0, ln 2 the weights are 1 : 1 : 2."""
+    ckv = np.array([[2, 0], [0, 8]], np.float32)
+    kpe = np.array([[0], [1]], np.float32)
+    qn = np.zeros((1, 1, 2), np.float32)
+    qp = np.ones((1, 1, 1), np.float32)
+    out, lse = orc.mla_decode(_bf(qn), _bf(qp), _bf(ckv), _bf(kpe), np.array([[0, 0, 1]], np.int32),
+                              np.array([3], np.int32), float(np.log(2.0)))
+    assert np.allclose(out[0, 0], [1.0, 4.0], rtol=1e-14, atol=1e-14), out
+    assert abs(lse[0, 0] - np.log(4.0)) < 1e-14
+
 ALL_PINS = [pin_half_decode, pin_score_integer_exact, pin_score_normal_bound,
             pin_topk_bruteforce, pin_topk_all_zero, pin_topk_stable_argsort,
             pin_expand_closed_form, pin_remap_identity, pin_remap_inverse, pin_remap_guards,
@@ -457,4 +590,6 @@ ALL_PINS = [pin_half_decode, pin_score_integer_exact, pin_score_normal_bound,
             pin_workspace_worked_example, pin_workspace_decode_rows_are_remap, pin_dcp_worked_example,
             pin_dcp_single_rank_is_remap, pin_dcp_interleave_partition, pin_dcp_compaction,
             pin_maxsim_worked_example, pin_maxsim_integer_exact, pin_maxsim_single_row_closed_form,
-            pin_maxsim_order_invariance, pin_maxsim_degenerate, pin_maxsim_normal_bound]
+            pin_maxsim_order_invariance, pin_maxsim_degenerate, pin_maxsim_normal_bound,
+            pin_bf16_decode, pin_mla_worked_example, pin_mla_single_entry, pin_mla_uniform,
+            pin_mla_entry_set, pin_mla_shift, pin_mla_large_logits, pin_mla_duplicate_slot]

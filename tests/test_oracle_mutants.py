@@ -48,6 +48,14 @@ MUTANTS = {
     "maxsim_stride_is_d": [("const uint16_t *row = docs + r * doc_stride;", "const uint16_t *row = docs + r * d;")],
     "maxsim_first_query_row_only": [("for (int32_t a = 0; a < lq; ++a) {\n            double best", "for (int32_t a = 0; a < 1; ++a) {\n            double best")],
     "maxsim_oob_not_zero": [("double s = 0.0, sa = 0.0;\n                if (r >= 0", "double s = -1.0, sa = 0.0;\n                if (r >= 0")],
+    "bf16_wrong_shift": [("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;")],
+    "mla_no_max_shift": [("const double p = exp(logit[j] - m);", "const double p = exp(logit[j]);")],
+    "mla_scale_dropped": [("logit[j] = sm_scale * acc;", "logit[j] = acc;")],
+    "mla_rope_dropped": [("for (int32_t d = 0; d < dr; ++d)\n                    acc +=",
+                          "for (int32_t d = 0; d < 0; ++d)\n                    acc +=")],
+    "mla_kv_len_ignored": [("const int32_t n = kv_len[r] < width ? kv_len[r] : width;", "const int32_t n = width;")],
+    "mla_not_normalised": [("o[d] /= z;", "o[d] /= 1.0;")],
+    "mla_lse_without_max": [("lse[(int64_t)r * heads + h] = m + log(z);", "lse[(int64_t)r * heads + h] = log(z);")],
     "dcp_compact_keeps_columns": [("                    out[cnt] = s;", "                    out[c] = s;")],
 }
 
