@@ -10,12 +10,11 @@
 // block_table[req, t / block_size] * block_stride_rows + t % block_size (-1 guarded), and
 // the valid count is the number of non -1 slots, reduced on chip without atomics.
 //
-// GB300 design: one 1024-thread CTA per row; no cluster, no distributed shared memory.
-// Thread t owns a contiguous run of the row's pools and holds up to 32 of their
-// order-preserving 32-bit keys in registers at a time. An exact three-level radix
+// GB300 design: one 512-thread CTA per row; no cluster, no distributed shared memory.
+// The row is read in chunks of 32 x 512 pools; in a chunk thread t holds the
+// order-preserving 32-bit keys of pools t, t + 512, ... (32 registers, coalesced loads). An exact three-level radix
 // select (11 + 11 + 10 key bits) finds the K-th largest key:
-//   level 1: the bin b1 holding it, from the row's histogram of the top 11 bits (made by
-//            the histogram kernel, or counted here when there is none);
+//   level 1: the bin b1 holding it, from the row's histogram of the top 11 bits;
 //   list:    the row's keys with bin >= b1 (the keys above the threshold bin and the
 //            threshold bin itself: about K plus a few hundred for real scores) are
 //            compacted, in index order, into a shared-memory list by one block scan;
@@ -237,14 +236,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     const float* row = a.scores + static_cast<int64_t>(rl) * a.scores_ld;
     const int64_t nchunks = (P + kChunkPools - 1) / kChunkPools;
     const int warp = tid >> 5;
-    const bool have_hist = a.hist != nullptr;
 
-    // every load is issued before any is waited on: histogram and block table (copied
-    // asynchronously into shared memory), first keys (registers)
-    if (have_hist) {
-        const uint32_t* hrow = a.hist + static_cast<int64_t>(rl) * kTopkBins;
-        for (int i = tid; i < kTopkBins / 4; i += T) cp_async_16(sm.hist + 4 * i, hrow + 4 * i);
-    }
+    // the block table is copied asynchronously into shared memory while the first keys load
     int nblk = 0;
     if (REMAP) {
         int64_t need = (ctx + a.block_size - 1) / a.block_size;
@@ -256,17 +249,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     load_chunk(row, 0, P, key);
 
     // ---- level 1: the bin b1 (top 11 key bits) of the K-th largest key
-    if (!have_hist) {
-        for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
-        __syncthreads();
-        for (int64_t c = 0; c < nchunks; ++c) {
-            if (c > 0) load_chunk(row, c, P, key);
+    for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
+    __syncthreads();
+    for (int64_t c = 0; c < nchunks; ++c) {
+        if (c > 0) load_chunk(row, c, P, key);
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i)
-                if (c * kChunkPools + static_cast<int64_t>(i) * T + tid < P) atomicAdd(&sm.hist[key[i] >> 21], 1u);
-        }
-        if (nchunks > 1) load_chunk(row, 0, P, key);
+        for (int i = 0; i < kChunk; ++i)
+            if (c * kChunkPools + static_cast<int64_t>(i) * T + tid < P) atomicAdd(&sm.hist[key[i] >> 21], 1u);
     }
+    if (nchunks > 1) load_chunk(row, 0, P, key);
     cp_async_wait_all();
     __syncthreads();
     TK_PHASE(2);

@@ -305,10 +305,5 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 }
 
 
-// Inverse of ordered_key for keys of non-NaN scores (-0.0 comes back as +0.0).
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 
 }  // namespace sel

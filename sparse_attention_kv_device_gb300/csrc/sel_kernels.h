@@ -87,7 +87,6 @@ struct TopkArgs {
     const int32_t* positions;  // global rows; used when row_ctx is null
     const int32_t* row_ctx;    // chunk-local (builder output) or null
     const int32_t* row_req;    // chunk-local (builder output), needed with remap
-    const uint32_t* hist;      // chunk-local rows x kTopkBins level-1 histograms (scorer output) or null
     int32_t row_begin;
     int32_t topk, kpool, out_width;
     int64_t max_pools;         // rows with ctx / kpool beyond this are out of bound
