@@ -309,6 +309,35 @@ def maxsim_rerank(sel, torch, dev, stream, flush, peak, iters):
             "gpu_launches": sel.sel_maxsim_launch_count(lq, d)}
 
 
+def eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, iters):
+    """The same step launched eagerly (sel_select called from Python every step, no graph), L2
+    flushed before each call, CUDA events on the stream around each call."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush()
+            sel.sel_select(prob, slots, counts, ws=ws, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            sel.sel_select(prob, slots, counts, ws=ws, stream=stream)
+            b.record(stream)
+    stream.synchronize()
+    ms = np.array([a.elapsed_time(b) for a, b in ev])
+    med = float(np.median(ms))
+    return {"median_ms": med, "p10_ms": float(np.percentile(ms, 10)), "p90_ms": float(np.percentile(ms, 90)),
+            "rows_per_s": rows / (med * 1e-3), "launches_per_step": sel.sel_select_launch_count(prob)}
+
+
+def auxiliary(fn):
+    """Runs one of the side measurements; a failure is reported in its place instead of
+    suppressing the headline line."""
+    try:
+        return fn()
+    except Exception as e:  # noqa: BLE001 -- any failure of a side measurement is reported as data
+        return {"error": f"{type(e).__name__}: {e}"[:400]}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -445,12 +474,13 @@ def run_ours(args):
         e2e = {"value": world * rows * args.steps / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
+    eager = auxiliary(lambda: eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, 50))
     remap = None
     if not args.no_remap:
-        remap = remap_modes(sel, torch, dev, stream, flush, peak, 20)
+        remap = auxiliary(lambda: remap_modes(sel, torch, dev, stream, flush, peak, 20))
     maxsim = None
     if not args.no_maxsim:
-        maxsim = maxsim_rerank(sel, torch, dev, stream, flush, peak, 20)
+        maxsim = auxiliary(lambda: maxsim_rerank(sel, torch, dev, stream, flush, peak, 20))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -485,6 +515,8 @@ def run_ours(args):
             line["e2e"] = e2e
         if cpu:
             line["cpu_baseline"] = cpu
+        if eager:
+            line["eager_step"] = eager
         if remap:
             line["remap_modes"] = remap
         if maxsim:
