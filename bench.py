@@ -197,9 +197,16 @@ def cpu_baseline(w, budget_s=12.0):
         oracle.select(w, rows=rows, nthreads=threads)
         t_total += time.perf_counter() - t0
         done += 1
+    # one thread on a few rows as well (the oracle's per-core rate)
+    one_rows = rows[:min(8, w.num_rows)]
+    t0 = time.perf_counter()
+    oracle.select(w, rows=one_rows, nthreads=1)
+    t_one = time.perf_counter() - t0
     return {"value": done * w.num_rows / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{done} full steps ({w.num_rows} rows each) of the {w.name} workload, "
-                      f"{threads} threads, {t_total:.1f} s"}
+                      f"{threads} threads, {t_total:.1f} s",
+            "single_thread": {"value": one_rows.size / t_one, "unit": UNIT,
+                              "sample": f"{one_rows.size} rows, 1 thread, {t_one:.2f} s"}}
 
 
 def run_reference(args):
