@@ -65,6 +65,23 @@ def dist_env():
     return rank, local, world
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (every rank gets it); x itself with one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world: int, rows: int, steps: int, slowest_ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank processes `rows` rows per step, and the
+    job takes as long as its slowest rank."""
+    return world * rows * steps / (slowest_ms / 1e3)
+
+
 # ---------------------------------------------------------------- byte accounting
 def algorithmic_bytes(w):
     """Per-step algorithmic bytes of the selection (and of the scorer alone).
@@ -408,12 +425,8 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     step_ms = np.array([a.elapsed_time(b) for a, b in zip(ev_s, ev_e)])
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * rows * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(float(step_ms.sum()), world, dev)
+    value = job_rows_per_s(world, rows, args.steps, total_ms)
     ok_status = int(status.item())
 
     # ---- per-kernel times from trace events captured into a second graph
@@ -470,15 +483,11 @@ def run_ours(args):
                 sel.sel_select_host(hprob, slots_h, counts_h, stage, ws, stream=stream)
                 e_e[i].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = float(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)))
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e))), world, dev)
         h2d = (w.qsl.nbytes + w.positions.nbytes + w.q.nbytes + w.key_page_table.nbytes
                + w.block_table.nbytes)
         d2h = rows * w.out_width * 4 + rows * 4
-        e2e = {"value": world * rows * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+        e2e = {"value": job_rows_per_s(world, rows, args.steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     eager = auxiliary(lambda: eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, 50))
