@@ -358,8 +358,9 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        // an atomic still in flight (only after an abort) completes before the counter is reset
-        if (has_pend && lane == 0) asm volatile("" ::"r"(pend));
+        // an atomic still in flight (only after an abort) completes before the counter is reset:
+        // storing its value makes this thread wait for it
+        if (has_pend && lane == 0) *reinterpret_cast<volatile int*>(sm.qoff) = pend;
         if (ok && nc > 0) ok = publish();
         if (ok) ok = publish();  // the end record
         if (lane == 0 && blockIdx.x < 152) SEL_PHASE_VALUE(110 + blockIdx.x, n);
