@@ -166,9 +166,18 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
+        with open(self.path) as f:
+            out = self.summarize(f)
+        os.unlink(self.path)
+        return out
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock, largest max clock and the throttle reasons seen active, from the
+        CSV rows of QUERY (rows that do not parse are skipped); None without a sample."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -180,7 +189,6 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        os.unlink(self.path)
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
