@@ -259,6 +259,8 @@ int32_t sel_maxsim_launch_count(int32_t lq, int32_t d);
  * status (optional): device int32 word, see SEL_ST_*.
  * Requires out_width >= index_topk + kpool - 1, out_width % 4 == 0, slots and
  * token_idx 16-B aligned, and a workspace of sel_workspace_bytes(p) bytes.
+ * The workspace (caller-owned device memory) needs no initialisation and carries nothing
+ * from one call to the next; calls that share one must not overlap on the GPU.
  */
 int sel_select(const sel_problem *p, int32_t *slots, int32_t out_width, int32_t *valid_counts,
                int32_t *token_idx, int32_t *status, void *ws, size_t ws_bytes,
