@@ -1,7 +1,8 @@
 """Benchmark of the fused sparse-attention token selection (sel_select) on GB300.
 
-One step = one pass of the whole selection (segment builder, scorer, top-k with
-expansion and remap) over one batch of the 128K-context decode workload: 8 requests
+One step = one pass of the whole selection (one fused kernel per chunk of rows: segment
+plan, tensor-core scorer, exact top-k with expansion and remap) over one batch of the
+128K-context decode workload: 8 requests
 x 5 rows at contexts 131,068..131,072, 4 heads x 128 dims fp16 queries and
 compressed keys drawn from N(0,1)/sqrt(128), kpool 4, index_topk 2048, shuffled 64-token
 blocks and key pages interleaved with other layers' pages. Inputs are synthetic and
@@ -53,8 +54,8 @@ def parse():
     ap.add_argument("--no-remap", action="store_true", help="skip the stand-alone remap measurements")
     ap.add_argument("--no-maxsim", action="store_true", help="skip the MaxSim rerank measurement")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (profiling runs)")
-    ap.add_argument("--maxsim-only", action="store_true",
-                    help="profiling driver: two plain calls of the MaxSim rerank on its benchmark workload, no timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the ragged and mixed workloads measured beside the headline")
     return ap.parse_args()
 
 
@@ -109,6 +110,17 @@ def algorithmic_bytes(w):
     return dict(step=keys + q + kpt + bt + meta + out, scorer=keys + q + kpt, keys=keys, topk_out=out + bt)
 
 
+def algorithmic_flops(w):
+    """Tensor-core work of a step: 2 flops per multiply-add of every scored row (context above
+    index_topk) against its own complete pools, 4 heads x 128 dims."""
+    ctx = w.positions.astype(np.int64) + 1
+    flops = 0
+    for i in range(w.num_reqs):
+        c = ctx[int(w.qsl[i]):int(w.qsl[i + 1])]
+        flops += int((c[c > w.index_topk] // w.kpool).sum()) * 2 * 4 * 128
+    return flops
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -116,6 +128,17 @@ def measured_peaks():
         return float(m["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s sustained under the power cap (fp16 has the same nominal
+    rate on this part), and where the number comes from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops_sustained"]), "measured (bf16_tflops_sustained)"
+    except Exception:
+        return 1700.0, "fallback"
 
 
 def recorded_traffic(kernel_file, workload):
@@ -361,6 +384,59 @@ def eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, iters)
             "rows_per_s": rows / (med * 1e-3), "launches_per_step": sel.sel_select_launch_count(prob)}
 
 
+def graph_steps(sel, torch, prob, slots, counts, ws, stream, flush, iters, warmup=5, status=None):
+    """CUDA-graph replays of one sel_select call, L2 flushed before each, CUDA events on the
+    replay stream around each replay; returns the per-step times in ms."""
+    with torch.cuda.stream(stream):
+        sel.sel_select(prob, slots, counts, status=status, ws=ws)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        sel.sel_select(prob, slots, counts, status=status, ws=ws)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    stream.synchronize()
+    return np.array([a.elapsed_time(b) for a, b in ev])
+
+
+def config_leg(sel, torch, dev, stream, flush, name, iters, peak, tpeak):
+    """One of the other workloads (ragged decode, the mixed step) timed like the headline:
+    rows/s, time per step, algorithmic bytes and the fraction of the HBM copy peak; for a
+    step with a large tensor-core share also the fraction of the tensor peak, and the
+    larger of the two as the roofline fraction."""
+    w = workloads.make_workload(name)
+    prob = sel.problem_from_workload(w, dev)
+    slots = torch.empty((w.num_rows, w.out_width), dtype=torch.int32, device=dev)
+    counts = torch.empty(w.num_rows, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sel.new_workspace(sel.sel_workspace_bytes(prob), dev)
+    ms = graph_steps(sel, torch, prob, slots, counts, ws, stream, flush, iters, status=status)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} on {name}")
+    ab = algorithmic_bytes(w)
+    fl = algorithmic_flops(w)
+    mean = float(ms.mean())
+    gbs = ab["step"] / (mean * 1e-3) / 1e9
+    tfs = fl / (mean * 1e-3) / 1e12
+    out = {"workload": name, "rows": w.num_rows, "requests": w.num_reqs,
+           "us_per_step": {"mean": mean * 1e3, "median": float(np.median(ms)) * 1e3,
+                           "p10": float(np.percentile(ms, 10)) * 1e3, "p90": float(np.percentile(ms, 90)) * 1e3},
+           "rows_per_s": w.num_rows / (mean * 1e-3), "algorithmic_bytes": ab["step"], "GB/s": gbs,
+           "hbm_frac": gbs / peak, "algorithmic_flops": fl, "TFLOP/s": tfs, "tensor_frac": tfs / tpeak,
+           "launches_per_step": sel.sel_select_launch_count(prob)}
+    out["bound"] = "tensor" if out["tensor_frac"] > out["hbm_frac"] else "hbm"
+    out["frac"] = max(out["hbm_frac"], out["tensor_frac"])
+    return out
+
+
 def auxiliary(fn):
     """Runs one of the side measurements; a failure is reported in its place instead of
     suppressing the headline line."""
@@ -388,7 +464,7 @@ def run_ours(args):
     slots = torch.empty((rows, w.out_width), dtype=torch.int32, device=dev)
     counts = torch.empty(rows, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = torch.empty(sel.sel_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    ws = sel.new_workspace(sel.sel_workspace_bytes(prob), dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
@@ -437,32 +513,16 @@ def run_ours(args):
     value = job_rows_per_s(world, rows, args.steps, total_ms)
     ok_status = int(status.item())
 
-    # ---- per-kernel times from trace events captured into a second graph
-    trace = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    sel.sel_set_trace_events(trace)
-    try:
-        tgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tgraph, stream=stream):
-            sel.sel_select(prob, slots, counts, status=status, ws=ws)
-    finally:
-        sel.sel_set_trace_events(None)
-    n_tr = min(args.steps, 100)
-    parts = np.zeros((n_tr, 3))
-    with torch.cuda.stream(stream):
-        for i in range(n_tr):
-            flush()
-            tgraph.replay()
-            stream.synchronize()
-            parts[i] = [trace[j].elapsed_time(trace[j + 1]) for j in range(3)]
-    kern_ms = parts.mean(axis=0)   # builder, scorer, selection tail
-
+    # ---- the step is one launch of the fused kernel per chunk of rows: the per-launch
+    #      duration is the step's event time divided by its launches
+    launches = sel.sel_select_launch_count(prob)
+    kern_ms = float(step_ms.mean()) / launches
     ab = algorithmic_bytes(w)
     peak, peak_kind = measured_peaks()
-    names = ["k_build_segments", "k_score_segments", "k_select_rows"]
-    dom = int(np.argmax(kern_ms))
-    dom_bytes = [w.num_rows * 8 + (w.num_reqs + 1) * 4, ab["scorer"], ab["topk_out"]][dom]
-    achieved = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
-    traffic = recorded_traffic("k_score.cu", args.config) if dom == 1 else None
+    tpeak, tpeak_kind = measured_tensor_peak()
+    dom_bytes = ab["step"] / launches
+    achieved = dom_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("k_fused.cu", args.config)
     step_gbs = ab["step"] / (total_ms / args.steps * 1e-3) / 1e9
 
     # ---- end to end through the host-buffer entry point (pinned host inputs and outputs)
@@ -499,6 +559,10 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     eager = auxiliary(lambda: eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, 50))
+    configs = None
+    if not args.no_configs:
+        configs = {n: auxiliary(lambda n=n: config_leg(sel, torch, dev, stream, flush, n, 20, peak, tpeak))
+                   for n in ("ragged", "mixed") if n != args.config}
     remap = None
     if not args.no_remap:
         remap = auxiliary(lambda: remap_modes(sel, torch, dev, stream, flush, peak, 20))
@@ -525,11 +589,15 @@ def run_ours(args):
                         "p90": float(np.percentile(step_ms, 90))},
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "algorithmic_bytes_per_step": ab["step"],
-            "kernel_ms": {n: float(v) for n, v in zip(names, kern_ms)},
-            "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
+            "kernel_ms": {"k_select_fused": kern_ms},
+            "roofline": {"bound": "hbm", "kernel": "k_select_fused", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes": dom_bytes, "peak_source": f"{peak_kind} (hbm_gbs)"},
-            "gpu_launches": sel.sel_select_launch_count(prob) * args.steps,
+                         "algorithmic_bytes": dom_bytes, "launches_per_step": launches,
+                         "peak_source": f"{peak_kind} (hbm_gbs, burst copy)",
+                         "tensor": {"algorithmic_flops": algorithmic_flops(w),
+                                    "TFLOP/s": algorithmic_flops(w) / (kern_ms * launches * 1e-3) / 1e12,
+                                    "peak": tpeak, "peak_source": tpeak_kind}},
+            "gpu_launches": launches * args.steps,
             "status": ok_status,
             "wall_s_timed_region": t_wall,
         }
@@ -545,37 +613,16 @@ def run_ours(args):
             line["remap_modes"] = remap
         if maxsim:
             line["maxsim_rerank"] = maxsim
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
-def run_maxsim_only():
-    """Two eager calls of sel_maxsim_rerank on the benchmark's rerank batch (the second is the
-    one a profiler captures with -s 1 -c 1), then a status check."""
-    import torch
-
-    import sparse_attention_kv_device_gb300 as sel
-    from workloads.maxsim import make_maxsim
-    w = make_maxsim("maxsim_rerank4k")
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    q, docs, off, ln = t(w.q), t(w.docs), t(w.offsets), t(w.lengths)
-    scores = torch.empty(w.num_docs, dtype=torch.float32, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for _ in range(2):
-        sel.sel_maxsim_rerank(q, docs, off, ln, scores=scores, status=status)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())}")
-    print(f"maxsim ok: {w.num_docs} documents, {w.doc_rows} rows")
-    return 0
-
-
 def main():
     args = parse()
-    if args.maxsim_only:
-        return run_maxsim_only()
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -8,6 +8,7 @@ and raises if it has not been built.
 from .sel import (  # noqa: F401
     Problem,
     SelError,
+    new_workspace,
     problem_from_workload,
     sel_error_string,
     sel_host_stage_bytes,
@@ -23,7 +24,7 @@ from .sel import (  # noqa: F401
     sel_select_host,
     sel_select_launch_count,
     sel_select_static,
-    sel_set_trace_events,
+    sel_debug_wait_limit,
     sel_topk_expand,
     sel_version,
     sel_workspace_bytes,

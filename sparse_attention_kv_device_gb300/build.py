@@ -51,8 +51,8 @@ def build(force: bool = False, verbose: bool = False, out_dir: str | None = None
           extra_flags: tuple = ()) -> str:
     """Compile and link; returns the path of libsel.so.
 
-    ``out_dir`` / ``extra_flags`` build a variant elsewhere (for example a
-    diagnostics build with -DSEL_PHASE_TRACE); the default build is the library."""
+    ``out_dir`` / ``extra_flags`` build a variant elsewhere with extra compiler flags;
+    the default build is the library."""
     lib = LIB if out_dir is None else os.path.join(out_dir, "libsel.so")
     if out_dir is None and not force and up_to_date():
         return LIB

@@ -40,8 +40,6 @@
 
 namespace sel {
 
-SEL_PHASE_TABLE(maxsim)
-
 namespace {
 
 constexpr int kMsRing = 4;                      // tile records the scheduler may publish ahead of the TMA issuer
@@ -174,9 +172,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
     MsSmem sm = ms_carve(smem_raw, a.stages, a.nq_pad, a.kslabs);
     const int nwarps = a.nq_pad >> 5;  // epilogue warps with query rows
     // diagnostics: CTA 0 stamps its phases, every CTA its end (300 + CTA)
-    const bool tr = blockIdx.x == 0;
-    (void)tr;
-    if (tr && threadIdx.x == 0) SEL_PHASE(0);
     // the scheduler's first round trips start before the setup: the offsets/lengths of the
     // CTA's static first claim and the atomic for its second claim
     int pend = 0;  // scheduler warp, lane 0: an atomic's value in flight
@@ -224,7 +219,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_base;
     volatile int* abort_flag = sm.abort_flag;
-    if (tr && threadIdx.x == 0) SEL_PHASE(1);
     const float neg_inf = -__int_as_float(0x7f800000);
 
     if (warp == kWarpSched) {
@@ -274,7 +268,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         // publishes the gathered tile (nc == 0: the end record)
         auto publish = [&]() -> bool {
             const int slot = n & (kMsRing - 1);
-            if (tr && lane == 0 && n < 50) SEL_PHASE(8 + n);
             if (!warp_wait(&sm.sempty[slot], ((n / kMsRing) & 1) ^ 1u, abort_flag)) return false;
             int doc[4], row[4];
 #pragma unroll
@@ -363,7 +356,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         if (has_pend && lane == 0) *reinterpret_cast<volatile int*>(sm.qoff) = pend;
         if (ok && nc > 0) ok = publish();
         if (ok) ok = publish();  // the end record
-        if (lane == 0 && blockIdx.x < 152) SEL_PHASE_VALUE(110 + blockIdx.x, n);
         if (!ok && lane == 0) {
             *abort_flag = 1;
             report(a.status, kStTimeout);
@@ -417,7 +409,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
-                if (tr && n < 50) SEL_PHASE(60 + n);
             }
             if (ok) {
                 // drain: every stage's last copy consumed before the CTA leaves
@@ -574,7 +565,6 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             atomicExch(a.counter + 1, 0);
         }
     }
-    if (threadIdx.x == 0 && blockIdx.x < 152) SEL_PHASE(300 + blockIdx.x);
 }
 
 // Scores of a query with no rows: every document sums nothing.

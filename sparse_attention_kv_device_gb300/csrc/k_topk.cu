@@ -28,8 +28,6 @@
 
 namespace sel {
 
-SEL_PHASE_TABLE(topk)
-
 namespace {
 
 constexpr int T = kTopkThreads;
@@ -187,13 +185,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     const int r = a.row_begin + rl;
     TopkSmem sm = carve(tk_smem, a.bt_cap);
     // diagnostics: rows 0 and gridDim.x/2 stamp their phases (bases 0, 256)
-    const int tb = rl == 0 ? 0 : (rl == static_cast<int>(gridDim.x) / 2 ? 256 : -1);
-    (void)tb;
-#define TK_PHASE(i) do { if (tb >= 0 && tid == 0) { SEL_PHASE(tb + (i)); SEL_PHASE_CLK(tb + 32 + (i)); } } while (0)
-    TK_PHASE(0);
 
     pdl_wait();  // scores, row descriptors and histograms come from the preceding kernels
-    TK_PHASE(1);
 
     // ---- the row: context, request, mode
     bool valid = true;
@@ -260,7 +253,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     if (nchunks > 1) load_chunk(row, 0, P, key);
     cp_async_wait_all();
     __syncthreads();
-    TK_PHASE(2);
     uint32_t b1, k1;
     block_find_bin(sm.hist, sm, kTopkBins, static_cast<uint32_t>(K), b1, k1);
     const uint32_t m_list = static_cast<uint32_t>(K) - k1 + sm.hist[b1];  // keys with bin >= b1
@@ -268,7 +260,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
         map.btab = sm.btab;
         map.nblk = nblk;
     }
-    TK_PHASE(3);
 
     uint32_t vcount = 0;
     if (m_list <= static_cast<uint32_t>(kTopkListCap)) {
@@ -303,7 +294,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
         }
         for (int b = tid; b < kTopkBins; b += T) sm.hist[b] = 0;
         __syncthreads();
-        TK_PHASE(4);
         const uint32_t n_list = min(listed, static_cast<uint32_t>(kTopkListCap));
 
         // ---- levels 2 and 3 among the list's keys of bin b1
@@ -325,7 +315,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
         block_find_bin(sm.hist, sm, 1024, k2, b3, k3);
         const uint32_t thr = (pre22 << 10) | b3;  // the K-th largest key of the row
         const uint32_t need_eq = k3;              // keys equal to thr that are kept (lowest index first)
-        TK_PHASE(5);
 
         // ---- kept entries: keys > thr and the first need_eq keys == thr; one packed scan
         //      gives each its output column
@@ -350,7 +339,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
                 vcount += emit_pool<REMAP>(a, map, tok_row, slot_row, static_cast<int64_t>(out) * a.kpool,
                                            static_cast<int32_t>(static_cast<int64_t>(e.y) * a.kpool));
         }
-        TK_PHASE(6);
     } else {
         // ---- crowded threshold bin (massive ties): levels 2 and 3 and the output re-read the row
         uint32_t pre = b1, shift = 21, krem = k1;
@@ -425,9 +413,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) k_topk_expand(const TopkArgs 
     vcount += emit_run<REMAP>(a, map, tok_row, slot_row, K * a.kpool, P * a.kpool, ctx);
     const uint32_t total_valid = block_sum(vcount, sm.scratch);
     if (tid == 0 && a.counts) a.counts[r] = static_cast<int32_t>(total_valid);
-    TK_PHASE(7);
-    if (tid == 0 && rl < 200) SEL_PHASE(300 + rl);  // diagnostics: every row's end
-#undef TK_PHASE
 }
 
 size_t topk_smem_bytes(int bt_cap) {

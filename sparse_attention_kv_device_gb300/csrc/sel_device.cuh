@@ -29,6 +29,7 @@ constexpr int kStKeyPageOob = 1;
 constexpr int kStCtxOverBound = 2;
 constexpr int kStTimeout = 4;
 constexpr int kStBadQsl = 8;
+constexpr int kStBadWorkspace = 16;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -75,8 +76,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Gives up (returns
-// false) once another role has raised *abort or after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// false) once another role has raised *abort or after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
@@ -84,8 +86,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (abort_flag && *abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// ---------------------------------------------------------------- gpu-scope synchronisation
+// Loads and stores that order other memory accesses at GPU scope (between CTAs of one grid).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(int32_t* p, int32_t v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// atomic add with acquire-release semantics at GPU scope; returns the old value
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 // Asynchronous global -> shared copies (no register staging); cp_async_wait_all waits for
@@ -218,29 +245,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
-// ---------------------------------------------------------------- phase tracing (diagnostics)
-// Built with -DSEL_PHASE_TRACE, each kernel file declares SEL_PHASE_TABLE(tag): a table
-// of kPhaseSlots global-timer stamps (ns) and an exported reader sel_debug_phases_<tag>.
-// SEL_PHASE(slot) stores the timer into the file's table. Without the define both
-// compile to nothing.
-constexpr int kPhaseSlots = 512;
-#ifdef SEL_PHASE_TRACE
-#define SEL_PHASE_TABLE(tag)                                                              \
-    static __device__ unsigned long long g_sel_phase[::sel::kPhaseSlots];                 \
-    extern "C" int sel_debug_phases_##tag(void* dst, size_t bytes) {                      \
-        if (bytes > sizeof(g_sel_phase)) bytes = sizeof(g_sel_phase);                     \
-        return cudaMemcpyFromSymbol(dst, g_sel_phase, bytes) == cudaSuccess ? 0 : -3;     \
-    }
-#define SEL_PHASE(slot) (g_sel_phase[(slot)] = ::sel::global_timer_ns())
-#define SEL_PHASE_CLK(slot) (g_sel_phase[(slot)] = clock64())
-#define SEL_PHASE_VALUE(slot, v) (g_sel_phase[(slot)] = static_cast<unsigned long long>(v))
-#else
-#define SEL_PHASE_TABLE(tag)
-#define SEL_PHASE(slot) ((void)0)
-#define SEL_PHASE_CLK(slot) ((void)0)
-#define SEL_PHASE_VALUE(slot, v) ((void)0)
-#endif
 
 // ---------------------------------------------------------------- programmatic dependent launch
 // Blocks until the grids this one depends on have completed and their writes are

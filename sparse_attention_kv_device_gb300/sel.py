@@ -29,6 +29,7 @@ ST_KEYPAGE_OOB = 1
 ST_CTX_OVER_BOUND = 2
 ST_TIMEOUT = 4
 ST_BAD_QSL = 8
+ST_BAD_WORKSPACE = 16
 
 
 class SelError(RuntimeError):
@@ -76,7 +77,7 @@ def _load():
     lib.sel_host_stage_bytes.argtypes = [PP, I32]
     lib.sel_host_stage_bytes.restype = SZ
     lib.sel_select_host.argtypes = [PP, P, I32, P, P, P, SZ, P, SZ, P]
-    lib.sel_set_trace_events.argtypes = [C.POINTER(C.c_void_p), I32]
+    lib.sel_debug_wait_limit.argtypes = [I32, I64]
     lib.sel_select_launch_count.argtypes = [PP]
     lib.sel_select_launch_count.restype = I32
     lib.sel_maxsim_workspace_bytes.argtypes = []
@@ -86,7 +87,7 @@ def _load():
     lib.sel_maxsim_launch_count.restype = I32
     for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
               "sel_select",
-              "sel_select_static", "sel_select_host", "sel_set_trace_events", "sel_maxsim_rerank"):
+              "sel_select_static", "sel_select_host", "sel_debug_wait_limit", "sel_maxsim_rerank"):
         getattr(lib, f).restype = C.c_int
     return lib
 
@@ -96,7 +97,7 @@ _lib = _load()
 EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_workspace_bytes",
            "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
            "sel_select",
-           "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
+           "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_debug_wait_limit",
            "sel_select_launch_count", "sel_maxsim_workspace_bytes", "sel_maxsim_rerank", "sel_maxsim_launch_count"]
 
 
@@ -237,12 +238,26 @@ def sel_score_workspace_bytes(problem: Problem) -> int:
     return n
 
 
+def new_workspace(nbytes, device):
+    """A device workspace of nbytes, zero-filled as the library requires before first use
+    (its kernels return the counter words to zero, so it can be kept across calls)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
 def _workspace(ws, nbytes, device):
     if ws is None:
-        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        ws = new_workspace(nbytes, device)
     elif ws.numel() * ws.element_size() < nbytes:
         raise SelError(SEL_EWORKSPACE, "workspace")
     return ws
+
+
+def _on_current_device(where, *tensors):
+    """The library queues work on the current CUDA device: every tensor must live there."""
+    cur = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.is_cuda and t.device.index != cur:
+            raise ValueError(f"{where}: tensor on {t.device}, but the current device is cuda:{cur}")
 
 
 def sel_score_paged(problem: Problem, scores, status=None, ws=None, stream=None):
@@ -251,6 +266,7 @@ def sel_score_paged(problem: Problem, scores, status=None, ws=None, stream=None)
     _dev(status, torch.int32, "status")
     if scores.stride(1) != 1:
         raise ValueError("scores rows must be contiguous")
+    _on_current_device("sel_score_paged", scores, status, ws, *problem.tensors)
     ws = _workspace(ws, sel_score_workspace_bytes(problem), scores.device)
     _check(_lib.sel_score_paged(problem.byref(), _ptr(scores), scores.stride(0), _ptr(status), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)), "sel_score_paged")
@@ -335,6 +351,7 @@ def sel_select(problem: Problem, slots, valid_counts, token_idx=None, status=Non
         _dev(t, torch.int32, n)
     if not slots.is_contiguous() or (token_idx is not None and not token_idx.is_contiguous()):
         raise ValueError("slots and token_idx must be contiguous")
+    _on_current_device("sel_select", slots, valid_counts, token_idx, status, ws, *problem.tensors)
     ws = _workspace(ws, sel_workspace_bytes(problem), slots.device)
     _check(_lib.sel_select(problem.byref(), _ptr(slots), int(slots.shape[1]), _ptr(valid_counts),
                            _ptr(token_idx), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(),
@@ -354,6 +371,7 @@ def sel_select_static(problem: Problem, slots, valid_counts, token_idx=None, sta
         _dev(t, torch.int32, n)
     if not slots.is_contiguous() or (token_idx is not None and not token_idx.is_contiguous()):
         raise ValueError("slots and token_idx must be contiguous")
+    _on_current_device("sel_select_static", slots, valid_counts, token_idx, status, *problem.tensors)
     _check(_lib.sel_select_static(problem.byref(), _ptr(slots), int(slots.shape[1]), _ptr(valid_counts),
                                   _ptr(token_idx), _ptr(status), _stream(stream)), "sel_select_static")
     return slots, valid_counts
@@ -373,16 +391,11 @@ def sel_select_host(problem: Problem, slots_host, counts_host, stage, ws, status
     return slots_host, counts_host
 
 
-def sel_set_trace_events(events) -> None:
-    """events: four torch.cuda.Event(enable_timing=True), or None to switch tracing off."""
-    if not events:
-        _check(_lib.sel_set_trace_events(None, 0), "sel_set_trace_events")
-        return
-    for e in events:
-        if not e.cuda_event:   # torch creates the CUDA event on its first record
-            e.record()
-    arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
-    _check(_lib.sel_set_trace_events(arr, len(events)), "sel_set_trace_events")
+def sel_debug_wait_limit(fault_tile: int = -1, wait_ns: int = 1_000_000_000) -> None:
+    """Failure-detection test hook: later fused launches give every bounded wait wait_ns and
+    (fault_tile >= 0) never load that tile's keys, so their waits expire. The defaults
+    restore normal operation."""
+    _check(_lib.sel_debug_wait_limit(int(fault_tile), int(wait_ns)), "sel_debug_wait_limit")
 
 
 def sel_select_launch_count(problem: Problem) -> int:
@@ -401,7 +414,7 @@ def sel_maxsim_rerank(q, docs, doc_offsets, doc_lengths, scores=None, status=Non
     multiples of 8 elements. Returns scores fp32 [B]: per query row the best dot product
     over the document's rows, summed over the query rows (-inf for an empty document).
     ws (optional): a uint8 device tensor of sel_maxsim_workspace_bytes(), zero-filled before
-    its first use; the kernel leaves it zero-filled, so it can be kept across calls."""
+    its first use (new_workspace); the kernel leaves it zero-filled, so it can be kept across calls."""
     _dev(q, torch.float16, "q")
     _dev(docs, torch.float16, "docs")
     _dev(doc_offsets, torch.int32, "doc_offsets")
@@ -418,7 +431,7 @@ def sel_maxsim_rerank(q, docs, doc_offsets, doc_lengths, scores=None, status=Non
         scores = torch.empty(num_docs, dtype=torch.float32, device=docs.device)
     _dev(scores, torch.float32, "scores")
     if ws is None:  # the workspace must start zero-filled (the kernel leaves it so)
-        ws = torch.zeros(sel_maxsim_workspace_bytes(), dtype=torch.uint8, device=docs.device)
+        ws = new_workspace(sel_maxsim_workspace_bytes(), docs.device)
     _dev(ws, torch.uint8, "ws")
     lq, d = q.shape
     _check(_lib.sel_maxsim_rerank(_ptr(q), int(lq), int(d), int(q.stride(0)), _ptr(docs), int(docs.shape[0]),

@@ -46,7 +46,16 @@ def test_error_strings(lib):
     lib.sel_error_string.restype = C.c_char_p
     for code in (0, -1, -2, -3, -4, -99):
         assert lib.sel_error_string(code)
-    assert lib.sel_version() == 100
+    assert lib.sel_version() == 200
+
+
+def test_wait_limit_hook_validates_and_restores(lib):
+    f = lib.sel_debug_wait_limit
+    f.argtypes = [C.c_int32, C.c_int64]
+    assert f(-2, 10**9) == -1        # no such tile
+    assert f(3, 10) == -1            # a limit below a microsecond is refused
+    assert f(5, 10**6) == 0
+    assert f(-1, 10**9) == 0         # normal operation again
 
 
 def _problem(**kw):

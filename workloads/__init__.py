@@ -86,19 +86,22 @@ def _ceil_div(a: int, b: int) -> int:
 
 def build_workload(requests: Sequence[Sequence[int]], *, name: str, seed: int,
                    integer_mode: bool, index_topk: int = 2048, kpool: int = 4,
-                   key_page_stride_pages: int = 1, block_stride_rows: int = BLOCK,
+                   key_page_stride_pages: int = 1, block_stride_rows: int | None = None,
                    oob_blocks: Sequence[tuple[int, int, int]] = (),
                    pad_rows: int = 0, chunk_rows: int = 256,
                    out_width: int | None = None, pool_factor: float = 1.25,
-                   max_context: int | None = None) -> Workload:
+                   max_context: int | None = None, block_size: int = BLOCK) -> Workload:
     """Lay out one batch.
 
     ``requests[i]`` lists the context length (position + 1) of each query row of
     request i, in row order. ``oob_blocks`` entries ``(req, logical_block, value)``
     overwrite block-table entries (value is the physical id written; a negative
     ``value`` is written as is, a value >= 0 is added to ``num_kv_blocks`` so that
-    it lands past the physical pool).
+    it lands past the physical pool). ``block_size`` is the KV block size in tokens
+    (``block_stride_rows`` defaults to it).
     """
+    if block_stride_rows is None:
+        block_stride_rows = block_size
     ss = np.random.SeedSequence(seed)
     rng_q, rng_k, rng_kp, rng_bt = (np.random.default_rng(s) for s in ss.spawn(4))
 
@@ -125,7 +128,7 @@ def build_workload(requests: Sequence[Sequence[int]], *, name: str, seed: int,
     ctx_max = [max(r) if len(r) else 0 for r in requests]
     pools = [c // kpool for c in ctx_max]
     kpages = [_ceil_div(p, KEY_PAGE) for p in pools]
-    blocks = [_ceil_div(c, BLOCK) for c in ctx_max]
+    blocks = [_ceil_div(c, block_size) for c in ctx_max]
 
     # key pages: physical pool = 1.25x needed, seeded placement
     num_key_pages = max(1, math.ceil(sum(kpages) * pool_factor))
@@ -172,7 +175,7 @@ def build_workload(requests: Sequence[Sequence[int]], *, name: str, seed: int,
         key_page_stride=key_page_stride, num_key_pages=num_key_pages,
         key_page_table=key_page_table, max_key_pages_per_req=kpt_ld,
         block_table=block_table, max_blocks_per_req=bt_ld, num_kv_blocks=num_kv_blocks,
-        block_size=BLOCK, block_stride_rows=block_stride_rows, index_topk=index_topk,
+        block_size=block_size, block_stride_rows=block_stride_rows, index_topk=index_topk,
         kpool=kpool, out_width=out_width,
         max_context=max_context if max_context is not None else max([0] + ctx_rows),
         max_q_len=max([1] + lens), chunk_rows=chunk_rows, oob_entries=tuple(applied))
