@@ -31,12 +31,6 @@
  *    caller, and must stay valid until the work queued on `stream` has finished.
  *    The library allocates no memory; apart from the fixed scratch array of
  *    sel_select_static it keeps no device state between calls.
- *  - Workspaces (sel_select, sel_select_host, sel_score_paged, sel_maxsim_rerank) begin
- *    with counter words that the kernels of one launch share (a fixed block, the same for
- *    every problem). A workspace must be ZERO-FILLED before its first use (e.g.
- *    cudaMemsetAsync); every launch returns its counter words to zero when it finishes
- *    (also after a timeout), so a workspace kept for later calls, of any problem shape,
- *    needs zeroing only once. Calls sharing a workspace must not overlap on the GPU.
  *  - Work is queued on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    No entry point synchronises the device or reads device memory on the host, so
  *    the device entry points can be captured into a CUDA graph. Values baked into a
@@ -74,7 +68,6 @@ typedef struct CUstream_st *sel_stream_t; /* same type as cudaStream_t */
 #define SEL_ST_CTX_OVER_BOUND 2u  /* a row's context exceeds max_context: the row is all -1, count 0 */
 #define SEL_ST_TIMEOUT 4u         /* a bounded wait inside a kernel expired: outputs are incomplete */
 #define SEL_ST_BAD_QSL 8u         /* query_start_loc not non-decreasing within [0, num_rows]: all rows -1 */
-#define SEL_ST_BAD_WORKSPACE 16u  /* the workspace's counter words were not zero at launch: outputs incomplete */
 
 /*
  * One selection problem. Host struct, read during the call only.
@@ -113,9 +106,8 @@ typedef struct sel_problem {
     int64_t kpt_ld;                /* row stride of key_page_table, in elements */
     int64_t bt_ld;                 /* row stride of block_table, in elements */
     int64_t q_row_stride;          /* fp16 elements between query rows (>= 512, multiple of 8) */
-    int32_t segment_rows;          /* rows of one request scored together (1..64; 0 = automatic; lowered
-                                      when the buffers of a larger segment do not fit on chip) */
-    int32_t chunk_rows;            /* rows per launch and per score workspace (0 = 256; at most 512) */
+    int32_t segment_rows;          /* rows of one request scored together (1..64; 0 = automatic) */
+    int32_t chunk_rows;            /* rows per score-workspace chunk (0 = 256) */
     const int32_t *query_start_loc; /* [num_reqs + 1] */
     const int32_t *positions;       /* [num_rows] */
     const void *q;                  /* fp16 [num_rows][4][128] with row stride q_row_stride; 16-B aligned */
@@ -127,7 +119,7 @@ typedef struct sel_problem {
 /* Message for a return code (static storage). */
 const char *sel_error_string(int code);
 
-/* ABI version of this header (major * 100 + minor): 200. */
+/* ABI version of this header (major * 100 + minor): 101. */
 int sel_version(void);
 
 /* Workspace (device bytes, 256-B aligned base) needed by sel_select / sel_score_paged
@@ -147,8 +139,7 @@ size_t sel_score_workspace_bytes(const sel_problem *p);
  * Accumulation is fp32 on the tensor cores in an order of the hardware's choosing
  * (exact for integer-valued inputs whose dot products stay below 2^24).
  * status: optional device int32 word (see SEL_ST_*). ws: workspace of at least
- * sel_score_workspace_bytes(p) bytes (zero-filled before its first use). Queues one kernel
- * per chunk of p->chunk_rows rows.
+ * sel_score_workspace_bytes(p) bytes.
  */
 int sel_score_paged(const sel_problem *p, float *scores, int64_t scores_ld, int32_t *status,
                     void *ws, size_t ws_bytes, sel_stream_t stream);
@@ -267,19 +258,18 @@ int32_t sel_maxsim_launch_count(int32_t lq, int32_t d);
  * sel_select -- the fused path (ReVolta PR #59, "Change": request segments built on the
  * device, the segmented scorer, the top-512 pools; the "flashinfer_mla_sparse_sm90" page,
  * _kv_lens_host: expansion with the trailing incomplete pool; the "sparse_utils" page,
- * triton_convert_req_index_to_global_index: the remap and the valid counts).
- * One cooperative kernel per chunk of chunk_rows rows plans the chunk's request segments,
- * scores the pools, and selects, expands and remaps every row, queued on `stream`.
+ * triton_convert_req_index_to_global_index: the remap and the valid counts): segment
+ * builder, segmented scorer, top-k with expansion and remap, per chunk of chunk_rows rows,
+ * all queued on `stream`.
  * slots [num_rows][out_width]: the remapped slots of each row's selected tokens in
  * ascending token order, then -1 (an out-of-bounds block gives -1 in place).
  * valid_counts [num_rows]: number of entries of the row that are not -1.
  * token_idx [num_rows][out_width] (optional): the selected token indices.
  * status (optional): device int32 word, see SEL_ST_*.
- * Requires out_width >= index_topk + kpool - 1, out_width % 4 == 0, slots, token_idx and
- * ws 16-B aligned, and a workspace of sel_workspace_bytes(p) bytes, zero-filled before its
- * first use (see the conventions above); calls that share one must not overlap on the GPU.
- * Each launch needs every CTA of its grid resident at once (a cooperative launch, one CTA
- * per SM): work from other streams that holds SMs delays it.
+ * Requires out_width >= index_topk + kpool - 1, out_width % 4 == 0, slots and
+ * token_idx 16-B aligned, and a workspace of sel_workspace_bytes(p) bytes.
+ * The workspace (caller-owned device memory) needs no initialisation and carries nothing
+ * from one call to the next; calls that share one must not overlap on the GPU.
  */
 int sel_select(const sel_problem *p, int32_t *slots, int32_t out_width, int32_t *valid_counts,
                int32_t *token_idx, int32_t *status, void *ws, size_t ws_bytes,
@@ -292,16 +282,17 @@ int sel_select(const sel_problem *p, int32_t *slots, int32_t out_width, int32_t 
  * published method has no counterpart of this entry point.
  * Arguments, layouts, results and the other error codes are those of sel_select. The
  * scratch is one file-scope device array of SEL_STATIC_WS_MAX_BYTES bytes, held by every
- * GPU that loads the library until the process exits; no call allocates or frees device
- * memory. Returns SEL_EWORKSPACE, queueing nothing, when sel_workspace_bytes(p) exceeds
+ * GPU that loads the library until the process exits (the driver places it when the
+ * library's module is loaded on a device; with lazy module loading, at the first call of
+ * this entry point there, which therefore adds SEL_STATIC_WS_MAX_BYTES to the device memory
+ * in use once); no call allocates or frees device memory. Returns SEL_EWORKSPACE, queueing nothing, when sel_workspace_bytes(p) exceeds
  * SEL_STATIC_WS_MAX_BYTES (a smaller p->chunk_rows lowers that size).
  * Outside stream capture every call looks up the array's address on the current device
  * (so the address stays right after a device reset reloads the module); a call inside a
  * capture uses the address found by the last call on that device outside capture, so make
  * one call on each device before capturing. Every call on a device uses the same array:
  * calls whose work overlaps on the GPU (unordered streams) race and give wrong results.
- * The array starts zero-filled and every launch leaves its counter words zero, so no
- * zeroing is needed between calls.
+ * The kernels clear every counter they rely on, so no zeroing is needed between calls.
  */
 #define SEL_STATIC_WS_MAX_BYTES (16u << 20)
 int sel_select_static(const sel_problem *p, int32_t *slots, int32_t out_width,
@@ -324,16 +315,29 @@ int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width
                     void *ws, size_t ws_bytes, sel_stream_t stream);
 
 /*
+ * Tracing hook. With n >= 4 events (cudaEvent_t handles, created by the caller with
+ * timing enabled), every following sel_select records, on `stream`: events[0] before its
+ * first segment-builder launch, events[1] after that builder (before the first scorer
+ * launch), events[2] after the last scorer launch and events[3] after the last row-select
+ * launch (exact top-k, expansion, remap). Inside stream capture the records
+ * become external event nodes. n == 0 switches tracing off. Calls to sel_select are
+ * serialised while tracing state is read.
+ */
+int sel_set_trace_events(void *const *events, int32_t n);
+
+/*
  * sel_debug_wait_limit -- failure-detection test hook (the published method has no
- * counterpart). Every later sel_select / sel_score_paged launch gives each of its bounded
- * waits wait_ns nanoseconds (default 1 s) and, with fault_tile >= 0, never loads the keys
- * of that tile, so the waits on it expire: the launch then sets SEL_ST_TIMEOUT, every role
- * leaves, and the workspace counters are returned to zero as after any launch. Call with
- * (-1, 1000000000) to restore normal operation. Not thread safe; for tests only.
+ * counterpart). Every later sel_select / sel_score_paged / sel_maxsim_rerank launch gives
+ * each of its bounded waits wait_ns nanoseconds (default 1 s) and, with fault_tile >= 0,
+ * never loads the data of that work item (the scorer's tile fault_tile; MaxSim's tile
+ * fault_tile of each CTA), so the waits on it expire: the launch sets SEL_ST_TIMEOUT, every
+ * role of the kernel leaves without touching the missing data, and the work counters of a
+ * MaxSim workspace are returned to zero as after any launch. Call with (-1, 1000000000) to
+ * restore normal operation. Process-wide and not thread safe: for tests only.
  */
 int sel_debug_wait_limit(int32_t fault_tile, int64_t wait_ns);
 
-/* Number of kernel launches sel_select queues for problem p (one per chunk of rows). */
+/* Number of kernel launches sel_select queues for problem p (for launch accounting). */
 int32_t sel_select_launch_count(const sel_problem *p);
 
 #ifdef __cplusplus

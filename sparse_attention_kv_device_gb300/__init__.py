@@ -25,6 +25,7 @@ from .sel import (  # noqa: F401
     sel_select_launch_count,
     sel_select_static,
     sel_debug_wait_limit,
+    sel_set_trace_events,
     sel_topk_expand,
     sel_version,
     sel_workspace_bytes,

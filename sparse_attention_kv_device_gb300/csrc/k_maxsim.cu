@@ -124,9 +124,10 @@ __device__ __forceinline__ MsSmem ms_carve(uint8_t* raw, int stages, int nq_pad,
 }
 
 // Waits on `bar` with lane 0 polling; every lane learns the outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, limit_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         // publishes the gathered tile (nc == 0: the end record)
         auto publish = [&]() -> bool {
             const int slot = n & (kMsRing - 1);
-            if (!warp_wait(&sm.sempty[slot], ((n / kMsRing) & 1) ^ 1u, abort_flag)) return false;
+            if (!warp_wait(&sm.sempty[slot], ((n / kMsRing) & 1) ^ 1u, abort_flag, a.wait_ns)) return false;
             int doc[4], row[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -374,14 +375,14 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 const int slot = n & (kMsRing - 1);
-                if (!mbar_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&sm.sfull[slot], (n / kMsRing) & 1, abort_flag, a.wait_ns)) { ok = false; break; }
                 int4 r[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int4*>(sm.ring + slot * kMsRec + 4 * c);
                 mbar_arrive(&sm.sempty[slot]);
                 // forward the chunks' {doc, info} (or the end) to the MMA thread and the epilogue
                 const int islot = n & (kMsInfo - 1);
-                if (!mbar_wait(&sm.iempty[islot], ((n / kMsInfo) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&sm.iempty[islot], ((n / kMsInfo) & 1) ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
                 {
                     int4* dst = reinterpret_cast<int4*>(sm.info + islot * 8);
                     dst[0] = make_int4(r[0].x, r[0].w < 0 ? -1 : r[0].y, r[1].x, r[1].y);
@@ -392,7 +393,11 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
                 const uint32_t bytes = static_cast<uint32_t>(max(r[0].w, 0) + max(r[1].w, 0) + max(r[2].w, 0) +
                                                              max(r[3].w, 0)) * 128u;
                 for (int g = 0; g < a.kslabs; ++g) {
-                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
+                    if (n == a.fault_tile) {  // the failure-detection test leaves this tile unloaded
+                        if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     mbar_expect_tx(&sm.full[stage], bytes);
                     uint8_t* dst = sm.a + static_cast<size_t>(stage) * kMsSlabBytes;
 #pragma unroll
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             if (ok) {
                 // drain: every stage's last copy consumed before the CTA leaves
                 for (int i = 0; i < a.stages && ok; ++i) {
-                    ok = mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag);
+                    ok = mbar_wait(&sm.empty[stage], phase ^ 1u, abort_flag, a.wait_ns);
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -421,8 +426,8 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
                 *abort_flag = 1;
                 report(a.status, kStTimeout);
                 for (int i = 0; i < a.stages; ++i)
-                    if (loaded & (1u << i)) mbar_wait(&sm.full[i], (last_parity >> i) & 1u, nullptr);
-                mbar_wait(sm.qfull, 0, nullptr);
+                    if (loaded & (1u << i)) mbar_wait(&sm.full[i], (last_parity >> i) & 1u, nullptr, a.wait_ns);
+                mbar_wait(sm.qfull, 0, nullptr, a.wait_ns);
             }
         }
     } else if (warp == kWarpMma) {
@@ -434,18 +439,18 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
             const uint32_t a_base = smem_u32(sm.a);
             const uint32_t q_base = smem_u32(sm.q);
             const uint32_t qslab = static_cast<uint32_t>(a.nq_pad) * 128u;
-            bool ok = mbar_wait(sm.qfull, 0, abort_flag);
+            bool ok = mbar_wait(sm.qfull, 0, abort_flag, a.wait_ns);
             for (int n = 0; ok; ++n) {
                 const int islot = n & (kMsInfo - 1);
-                if (!mbar_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag, a.wait_ns)) { ok = false; break; }
                 const bool end = sm.info[islot * 8 + 1] < 0;
                 mbar_arrive(&sm.iempty[islot]);
                 if (end) break;
-                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * 128);
                 for (int g = 0; g < a.kslabs; ++g) {
-                    if (!mbar_wait(&sm.full[stage], phase, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&sm.full[stage], phase, abort_flag, a.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     // A: query rows (rows past nq_pad read what follows in shared memory and only
                     // reach TMEM lanes no warp reads); B: the tile's 128 document rows
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
                 report(a.status, kStTimeout);
             }
             umma_commit(sm.done);
-            mbar_wait(sm.done, 0, nullptr);
+            mbar_wait(sm.done, 0, nullptr, a.wait_ns);
         }
     } else if (warp >= kWarpEpi && (warp & 3) < nwarps) {
         // ------------------------------------------------------------ epilogue
@@ -481,14 +486,14 @@ __global__ void __launch_bounds__(kMaxsimThreads, 1)
         bool ok = true;
         for (int n = 0;; ++n) {
             const int islot = n & (kMsInfo - 1);
-            if (!warp_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(&sm.ifull[islot], (n / kMsInfo) & 1, abort_flag, a.wait_ns)) { ok = false; break; }
             int2 r[4];  // {doc (-1: none), info} of chunks 0..3
 #pragma unroll
             for (int c = 0; c < 4; ++c) r[c] = *reinterpret_cast<const int2*>(sm.info + islot * 8 + 2 * c);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.iempty[islot]);
             if (r[0].y < 0) break;
-            if (!warp_wait(&sm.tfull[acc], acc_phase, abort_flag)) { ok = false; break; }
+            if (!warp_wait(&sm.tfull[acc], acc_phase, abort_flag, a.wait_ns)) { ok = false; break; }
             tc_fence_after();
             // per chunk: this row's best dot product over the chunk's valid rows
             float m[4];

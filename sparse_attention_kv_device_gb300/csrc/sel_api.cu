@@ -15,19 +15,15 @@
 
 using namespace sel;
 
-
 namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSegRows = 64;          // rows x 4 heads <= 256 = the MMA's largest N
-constexpr int kMaxChunkRows = kFusedMaxChunkRows;  // rows per launch of the fused kernel
-constexpr int kTopkMaxRows = 32768;      // rows per launch of the stand-alone top-k
+constexpr int kMaxChunkRows = 32768;
 constexpr int kTopkMaxBtCap = 8192;      // block-table entries a top-k CTA stages at most
-constexpr int kMaxBtCap = 4096;          // block-table entries a select group stages per row
-constexpr int kMaxStages = 6;            // key tiles in flight per CTA
 
-// Failure-detection test hook (sel_debug_wait_limit): a tile the next fused launches leave
-// unloaded, and the limit of every wait in them.
+// Failure-detection test hook (sel_debug_wait_limit): a tile the next launches leave
+// unloaded, and the limit of every bounded wait in them.
 int g_fault_tile = -1;
 uint64_t g_wait_ns = sel::kWaitLimitNs;
 
@@ -147,16 +143,18 @@ int plan_topk(int64_t max_context, int block_size, bool remap, int max_smem, Top
 
 struct Plan {
     int chunk_rows = 1, seg_rows = 1, max_segs = 1;
-    int64_t max_pools = 0, keys_ld = 4, grp_ld = 2;
-    int gcap = 0, cand_cap = 0, bt_cap = 0, K = 1;
-    size_t off_ctr = 0, ctr_bytes = 0, off_keys = 0, off_grp = 0;
+    int64_t max_pools = 0, scores_ld = 4;
+    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0,
+           off_scores = 0;
     size_t ws_score = 0, ws_select = 0;
     int npad_max = 16, stages = 2;
     uint32_t acc_cols = 32, tmem_cols = 64;
-    FusedLayout lay{};      // fused selection
-    FusedLayout lay_score{};  // scores only
-    int stages_score = 2;
+    size_t score_smem = 0;
+    TopkPlan topk;
     int sms = 0;
+    int bm_words = 1;
+    int stage_cap = 0;  // keys of a row the select kernel stages in shared memory
+    size_t sel_smem = 0;
 };
 
 // log2(v) when v is a power of two, else -1
@@ -194,25 +192,6 @@ int check_problem(const sel_problem* p) {
     return SEL_OK;
 }
 
-// Shared memory of the fused kernel for a segment size, with as many key stages as fit
-// (at least two); returns false when not even two fit.
-bool fit_layout(const Plan& pl, int seg_rows, int max_segs, bool select, int max_smem, FusedLayout* out,
-                int* stages_out, int* npad_out) {
-    const int npad = ((4 * seg_rows + 15) / 16) * 16;
-    for (int st = kMaxStages; st >= 2; --st) {
-        const FusedLayout L = select ? fused_layout(st, npad, max_segs, pl.chunk_rows, pl.bt_cap, pl.cand_cap,
-                                                    pl.gcap, pl.K)
-                                     : fused_layout(st, npad, max_segs, pl.chunk_rows, 0, 0, 0, 0);
-        if (L.total <= static_cast<uint32_t>(max_smem)) {
-            *out = L;
-            *stages_out = st;
-            *npad_out = npad;
-            return true;
-        }
-    }
-    return false;
-}
-
 int make_plan(const sel_problem* p, Plan* pl) {
     int rc = check_problem(p);
     if (rc != SEL_OK) return rc;
@@ -223,94 +202,148 @@ int make_plan(const sel_problem* p, Plan* pl) {
     pl->chunk_rows = std::min(std::min(rows, kMaxChunkRows), p->chunk_rows > 0 ? p->chunk_rows : 256);
     int sr = p->segment_rows;
     if (sr == 0) sr = p->max_q_len > 0 ? p->max_q_len : rows;
-    sr = std::max(1, std::min(sr, kMaxSegRows));
-    pl->K = p->index_topk / p->kpool;
+    pl->seg_rows = std::max(1, std::min(sr, kMaxSegRows));
+    pl->max_segs = std::min(std::max(p->num_reqs, 1), pl->chunk_rows) +
+                   static_cast<int>(ceil_div(pl->chunk_rows, pl->seg_rows)) + 1;
     pl->max_pools = p->max_context / p->kpool;
-    pl->keys_ld = (std::max<int64_t>(pl->max_pools, 1) + 3) & ~int64_t(3);
-    pl->gcap = static_cast<int>(((ceil_div(std::max<int64_t>(pl->max_pools, 1), 32)) + 1) & ~int64_t(1));
-    pl->grp_ld = pl->gcap;
-    pl->cand_cap = std::min(4096, std::max(1024, 2 * pl->K));
-    pl->bt_cap = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>({static_cast<int64_t>(kMaxBtCap), ceil_div(std::max(p->max_context, 1), p->block_size),
-                              static_cast<int64_t>(std::max(p->max_blocks_per_req, 1))})));
-    const int64_t tiles_per_seg = std::max<int64_t>(1, ceil_div(pl->max_pools, 128));
-    // segment size: the largest that leaves room for two key stages next to the select buffers
-    auto segs_for = [&](int srows) {
-        const int reqs = std::min(std::max(p->num_reqs, 1), pl->chunk_rows);
-        return std::min(pl->chunk_rows, reqs + static_cast<int>(ceil_div(pl->chunk_rows, srows))) + 1;
-    };
-    int npad = 16;
-    for (;;) {
-        const int ms = segs_for(sr);
-        if (fit_layout(*pl, sr, ms, true, di.max_smem_optin, &pl->lay, &pl->stages, &npad)) {
-            pl->max_segs = ms;
-            break;
-        }
-        if (sr <= 4) return SEL_EUNSUPPORTED;
-        sr = std::max(4, sr / 2);
-    }
-    pl->seg_rows = sr;
-    pl->npad_max = npad;
-    if (!fit_layout(*pl, sr, pl->max_segs, false, di.max_smem_optin, &pl->lay_score, &pl->stages_score, &npad))
-        return SEL_EUNSUPPORTED;
-    if (static_cast<int64_t>(pl->max_segs) * tiles_per_seg > INT32_MAX / 2) return SEL_EUNSUPPORTED;
-    pl->acc_cols = std::max<uint32_t>(32, next_pow2(static_cast<uint32_t>(pl->npad_max)));
-    pl->tmem_cols = 2 * pl->acc_cols;
+    pl->scores_ld = (std::max<int64_t>(pl->max_pools, 1) + 3) & ~int64_t(3);
+    const int64_t tiles = static_cast<int64_t>(pl->max_segs) * std::max<int64_t>(1, ceil_div(pl->max_pools, 128));
+    if (tiles > INT32_MAX / 2) return SEL_EUNSUPPORTED;  // tile ids and the tile counter are int32
 
     size_t off = 0;
-    pl->off_ctr = off;
-    static_assert(kFusedCtrHeader + (kMaxChunkRows + 1) + kMaxChunkRows <= kFusedCtrWords, "counter block");
-    pl->ctr_bytes = sizeof(int32_t) * static_cast<size_t>(kFusedCtrWords);
-    off = align256(off + pl->ctr_bytes);
+    pl->off_hdr = off;
+    off = align256(off + 16 * sizeof(int32_t));
+    pl->off_row_req = off;
+    off = align256(off + sizeof(int32_t) * pl->chunk_rows);
+    pl->off_row_ctx = off;
+    off = align256(off + sizeof(int32_t) * pl->chunk_rows);
+    pl->off_seg = off;
+    off = align256(off + sizeof(int4) * pl->max_segs);
+    pl->off_prefix = off;
+    off = align256(off + sizeof(int32_t) * (pl->max_segs + 1));
     pl->ws_score = off;
-    pl->off_keys = off;
-    off = align256(off + sizeof(uint32_t) * static_cast<size_t>(pl->chunk_rows) * pl->keys_ld);
-    pl->off_grp = off;
-    off = align256(off + sizeof(uint2) * static_cast<size_t>(pl->chunk_rows) * pl->grp_ld);
+    pl->off_scores = off;
+    off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
+    pl->bm_words = static_cast<int>((pl->max_pools + 31) / 32);
     pl->ws_select = off;
+
+    pl->npad_max = ((4 * pl->seg_rows + 15) / 16) * 16;
+    pl->acc_cols = std::max<uint32_t>(32, next_pow2(static_cast<uint32_t>(pl->npad_max)));
+    pl->tmem_cols = 2 * pl->acc_cols;
+    const size_t fixed = score_smem_bytes(0, pl->npad_max, pl->max_segs);
+    if (fixed + 2 * 32768 > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    pl->stages = static_cast<int>(std::min<size_t>(8, (di.max_smem_optin - fixed) / 32768));
+    while (pl->stages > 2 && score_smem_bytes(pl->stages, pl->npad_max, pl->max_segs) > static_cast<size_t>(di.max_smem_optin))
+        --pl->stages;
+    pl->score_smem = score_smem_bytes(pl->stages, pl->npad_max, pl->max_segs);
+    if ((rc = plan_topk(p->max_context, p->block_size, true, di.max_smem_optin, &pl->topk)) != SEL_OK) return rc;
+    // the select kernel stages as many of a row's keys as fit (longer rows read the rest from L2)
+    const int K = p->index_topk / p->kpool;
+    pl->stage_cap = static_cast<int>(std::min<int64_t>(kSelectMaxStage, (pl->max_pools + 3) & ~int64_t(3)));
+    const size_t fixed_sel = select_smem_bytes(0, pl->bm_words, K, pl->topk.bt_cap);
+    if (fixed_sel > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    const int64_t fit = ((static_cast<int64_t>(di.max_smem_optin) - static_cast<int64_t>(fixed_sel)) / 4) & ~int64_t(3);
+    pl->stage_cap = static_cast<int>(std::min<int64_t>(pl->stage_cap, fit));
+    pl->sel_smem = select_smem_bytes(pl->stage_cap, pl->bm_words, K, pl->topk.bt_cap);
     return SEL_OK;
 }
 
-// The arguments every launch of the fused kernel shares.
-FusedArgs fused_args(const sel_problem* p, const Plan& pl, void* ws, int32_t* status) {
+// ------------------------------------------------------------------ tracing
+std::mutex g_trace_mu;
+constexpr int kTraceEvents = 4;
+cudaEvent_t g_trace[kTraceEvents] = {};
+int g_trace_n = 0;
+
+void trace_record(int i, cudaStream_t s) {
+    if (g_trace_n < kTraceEvents || !g_trace[i]) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(g_trace[i], s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(g_trace[i], s);
+}
+
+// ------------------------------------------------------------------ shared launch path
+struct Ws {
+    int32_t* hdr;
+    int32_t* row_req;
+    int32_t* row_ctx;
+    int4* seg;
+    int32_t* prefix;
+    float* scores;
+};
+
+Ws carve_ws(void* ws, const Plan& pl) {
     uint8_t* b = static_cast<uint8_t*>(ws);
-    FusedArgs a{};
-    a.qsl = p->query_start_loc;
-    a.positions = p->positions;
-    a.num_reqs = p->num_reqs;
-    a.num_rows = p->num_rows;
-    a.seg_rows = pl.seg_rows;
-    a.max_segs = pl.max_segs;
-    a.topk = p->index_topk;
-    a.kpool = p->kpool;
-    a.max_context = p->max_context;
+    Ws w;
+    w.hdr = reinterpret_cast<int32_t*>(b + pl.off_hdr);
+    w.row_req = reinterpret_cast<int32_t*>(b + pl.off_row_req);
+    w.row_ctx = reinterpret_cast<int32_t*>(b + pl.off_row_ctx);
+    w.seg = reinterpret_cast<int4*>(b + pl.off_seg);
+    w.prefix = reinterpret_cast<int32_t*>(b + pl.off_prefix);
+    w.scores = reinterpret_cast<float*>(b + pl.off_scores);
+    return w;
+}
+
+// Builder + scorer for rows [c0, c1); scores row k of the chunk at scores + k*ld.
+int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int c1, int score_all,
+                         float* scores, int64_t ld, int64_t pool_cap, int32_t* status,
+                         const CUtensorMap& tk, const CUtensorMap& tq, cudaStream_t s) {
+    BuildArgs b{};
+    b.qsl = p->query_start_loc;
+    b.positions = p->positions;
+    b.key_page_table = p->key_page_table;
+    b.kpt_ld = p->kpt_ld;
+    b.max_key_pages = p->max_key_pages_per_req;
+    b.num_key_pages = p->num_key_pages;
+    b.num_reqs = p->num_reqs;
+    b.num_rows = p->num_rows;
+    b.row_begin = c0;
+    b.row_end = c1;
+    b.seg_rows = pl.seg_rows;
+    b.topk = p->index_topk;
+    b.kpool = p->kpool;
+    b.max_context = p->max_context;
+    b.score_all = score_all;
+    b.pool_cap = static_cast<int32_t>(std::min<int64_t>(pool_cap, INT32_MAX));
+    b.max_segs = pl.max_segs;
+    b.row_req = w.row_req;
+    b.row_ctx = w.row_ctx;
+    b.seg = w.seg;
+    b.seg_tile_prefix = w.prefix;
+    b.hdr = w.hdr;
+    b.status = status;
+    if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
+    if (c0 == 0 && !score_all) trace_record(1, s);
+
+    ScoreArgs a{};
+    a.seg = w.seg;
+    a.hdr = w.hdr;
+    a.seg_tile_prefix = w.prefix;
     a.key_page_table = p->key_page_table;
     a.kpt_ld = p->kpt_ld;
     a.max_key_pages = p->max_key_pages_per_req;
     a.num_key_pages = p->num_key_pages;
+    a.max_segs = pl.max_segs;
+    a.row_ctx = w.row_ctx;
+    a.row_begin = c0;
+    a.topk = p->index_topk;
+    a.kpool = p->kpool;
+    a.score_all = score_all;
+    a.pool_cap = b.pool_cap;
+    a.scores = scores;
+    a.scores_ld = ld;
+    a.as_keys = score_all ? 0 : 1;  // the fused selection (score_all = 0) works on ordered keys
     a.npad_max = pl.npad_max;
+    a.stages = pl.stages;
     a.tmem_cols = pl.tmem_cols;
     a.acc_cols = pl.acc_cols;
-    a.ctr = reinterpret_cast<int32_t*>(b + pl.off_ctr);
-    a.keys = reinterpret_cast<uint32_t*>(b + pl.off_keys);
-    a.keys_ld = pl.keys_ld;
-    a.grp = reinterpret_cast<uint2*>(b + pl.off_grp);
-    a.grp_ld = pl.grp_ld;
-    a.kpool_shift = log2_if_pow2(p->kpool);
-    a.bs_shift = log2_if_pow2(p->block_size);
-    a.block_table = p->block_table;
-    a.bt_ld = p->bt_ld;
-    a.max_blocks = p->max_blocks_per_req;
-    a.num_kv_blocks = p->num_kv_blocks;
-    a.block_size = p->block_size;
-    a.block_stride_rows = p->block_stride_rows;
-    a.bt_cap = pl.bt_cap;
-    a.cand_cap = pl.cand_cap;
-    a.gcap = pl.gcap;
     a.status = status;
     a.fault_tile = g_fault_tile;
     a.wait_ns = g_wait_ns;
-    return a;
+    if (launch_score(a, tk, tq, pl.sms, pl.score_smem, true, s) != cudaSuccess) return SEL_ECUDA;
+    return SEL_OK;
 }
 
 // Validates the arguments every remap mode shares and fills them in.
@@ -362,7 +395,7 @@ const char* sel_error_string(int code) {
     }
 }
 
-int sel_version(void) { return 200; }
+int sel_version(void) { return 101; }
 
 size_t sel_workspace_bytes(const sel_problem* p) {
     Plan pl;
@@ -386,18 +419,13 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     CUtensorMap tk, tq;
     if ((rc = encode_key_map(&tk, p->key_cache, p->num_key_pages, p->key_page_stride)) != SEL_OK) return rc;
     if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
-    FusedArgs a = fused_args(p, pl, ws, status);
-    a.select = 0;
-    a.score_all = 1;
-    a.pool_cap = static_cast<int32_t>(std::min<int64_t>(scores_ld, INT32_MAX));
-    a.scores_ld = scores_ld;
-    a.stages = pl.stages_score;
-    a.lay = pl.lay_score;
+    Ws w = carve_ws(ws, pl);
+    int32_t* st = status ? status : w.hdr + 8;
     for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
-        a.row_begin = c0;
-        a.row_end = std::min(p->num_rows, c0 + pl.chunk_rows);
-        a.scores = scores + static_cast<int64_t>(c0) * scores_ld;
-        if (launch_fused(a, tk, tq, pl.sms, s) != cudaSuccess) return SEL_ECUDA;
+        const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
+        rc = launch_chunk_scoring(p, pl, w, c0, c1, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
+                                  scores_ld, st, tk, tq, s);
+        if (rc != SEL_OK) return rc;
     }
     return SEL_OK;
 }
@@ -416,8 +444,8 @@ int sel_topk_expand(const float* scores, int64_t scores_ld, const int32_t* posit
     TopkPlan tp;
     if ((rc = plan_topk(0, 1, false, di.max_smem_optin, &tp)) != SEL_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (int c0 = 0; c0 < num_rows; c0 += kTopkMaxRows) {
-        const int rows = std::min(kTopkMaxRows, num_rows - c0);
+    for (int c0 = 0; c0 < num_rows; c0 += kMaxChunkRows) {
+        const int rows = std::min(kMaxChunkRows, num_rows - c0);
         TopkArgs a{};
         a.scores = scores + static_cast<int64_t>(c0) * scores_ld;
         a.scores_ld = scores_ld;
@@ -569,6 +597,8 @@ int sel_maxsim_rerank(const void* q, int32_t lq, int32_t d, int64_t q_stride, co
         a.tmem_cols = 256;
         a.counter = counter;
         a.status = status;
+        a.fault_tile = g_fault_tile;
+        a.wait_ns = g_wait_ns;
         if (launch_maxsim(a, maps, grid, smem, s) != cudaSuccess) return SEL_ECUDA;
     }
     return SEL_OK;
@@ -582,26 +612,49 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
     if (p->num_rows == 0) return SEL_OK;
     if (!slots || !ws) return SEL_EINVAL;
     if (out_width < p->index_topk + p->kpool - 1 || out_width % 4 != 0) return SEL_EINVAL;
-    if (!aligned16(slots) || (token_idx && !aligned16(token_idx)) || !aligned16(ws)) return SEL_EUNSUPPORTED;
+    if (!aligned16(slots) || (token_idx && !aligned16(token_idx))) return SEL_EUNSUPPORTED;
     if (ws_bytes < pl.ws_select) return SEL_EWORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap tk, tq;
     if ((rc = encode_key_map(&tk, p->key_cache, p->num_key_pages, p->key_page_stride)) != SEL_OK) return rc;
     if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
-    FusedArgs a = fused_args(p, pl, ws, status);
-    a.select = 1;
-    a.score_all = 0;
-    a.pool_cap = static_cast<int32_t>(std::min<int64_t>(pl.max_pools, INT32_MAX));
-    a.stages = pl.stages;
-    a.lay = pl.lay;
-    a.out_width = out_width;
-    a.slots = slots;
-    a.token_idx = token_idx;
-    a.counts = valid_counts;
+    Ws w = carve_ws(ws, pl);
+    int32_t* st = status ? status : w.hdr + 8;
+    std::lock_guard<std::mutex> g(g_trace_mu);
     for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
-        a.row_begin = c0;
-        a.row_end = std::min(p->num_rows, c0 + pl.chunk_rows);
-        if (launch_fused(a, tk, tq, pl.sms, s) != cudaSuccess) return SEL_ECUDA;
+        const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
+        const bool last = c1 == p->num_rows;
+        if (c0 == 0) trace_record(0, s);
+        rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
+        if (rc != SEL_OK) return rc;
+        if (last) trace_record(2, s);
+        const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);
+
+        RowSelectArgs ra{};
+        ra.keys = keys;
+        ra.keys_ld = pl.scores_ld;
+        ra.row_ctx = w.row_ctx;
+        ra.row_req = w.row_req;
+        ra.stage_cap = pl.stage_cap;
+        ra.bm_words = pl.bm_words;
+        ra.bt_cap = pl.topk.bt_cap;
+        ra.row_begin = c0;
+        ra.topk = p->index_topk;
+        ra.kpool = p->kpool;
+        ra.out_width = out_width;
+        ra.kpool_shift = log2_if_pow2(p->kpool);
+        ra.bs_shift = log2_if_pow2(p->block_size);
+        ra.slots = slots;
+        ra.token_idx = token_idx;
+        ra.counts = valid_counts;
+        ra.block_table = p->block_table;
+        ra.bt_ld = p->bt_ld;
+        ra.max_blocks = p->max_blocks_per_req;
+        ra.num_kv_blocks = p->num_kv_blocks;
+        ra.block_size = p->block_size;
+        ra.block_stride_rows = p->block_stride_rows;
+        if (launch_select_rows(ra, c1 - c0, pl.sel_smem, true, s) != cudaSuccess) return SEL_ECUDA;
+        if (last) trace_record(3, s);
     }
     return SEL_OK;
 }
@@ -609,7 +662,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
 int32_t sel_select_launch_count(const sel_problem* p) {
     Plan pl;
     if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
-    return static_cast<int32_t>(ceil_div(p->num_rows, pl.chunk_rows));
+    return static_cast<int32_t>(3 * ceil_div(p->num_rows, pl.chunk_rows));
 }
 
 size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {
@@ -685,6 +738,19 @@ int sel_debug_wait_limit(int32_t fault_tile, int64_t wait_ns) {
     if (fault_tile < -1 || wait_ns < 1000) return SEL_EINVAL;
     g_fault_tile = fault_tile;
     g_wait_ns = static_cast<uint64_t>(wait_ns);
+    return SEL_OK;
+}
+
+int sel_set_trace_events(void* const* events, int32_t n) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (n == 0) {
+        g_trace_n = 0;
+        for (int i = 0; i < kTraceEvents; ++i) g_trace[i] = nullptr;
+        return SEL_OK;
+    }
+    if (n < kTraceEvents || !events) return SEL_EINVAL;
+    for (int i = 0; i < kTraceEvents; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+    g_trace_n = kTraceEvents;
     return SEL_OK;
 }
 

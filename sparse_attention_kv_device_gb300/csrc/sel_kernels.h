@@ -9,71 +9,78 @@
 
 namespace sel {
 
-// Shared-memory layout of the fused kernel (byte offsets from a 1024-B aligned base),
-// computed on the host by fused_layout().
-struct FusedLayout {
-    uint32_t a, q, segs, prefix, rec_ring, tile_ring, bars, words;
-    uint32_t p_ctx, p_req, p_lim, p_triv;
-    uint32_t s_btab, s_hist, s_ckey, s_cidx, s_rec, s_list, s_small, s_scan, s_scratch;
-    uint32_t total;  // dynamic shared memory to request (includes the alignment slack)
-};
-
-// The fused selection over one chunk of rows [row_begin, row_end): every CTA plans the
-// chunk's request segments itself, scores tiles of 128 pools on the tensor cores, and
-// (select = 1) selects, expands and remaps each row once its segment is scored; with
-// select = 0 it only writes fp32 scores (sel_score_paged).
-struct FusedArgs {
+// Segment builder: one CTA turns query_start_loc / positions into per-row request
+// ids and contexts and a list of request segments (<= seg_rows rows of one request)
+// with the exclusive prefix of the 128-pool tiles each must score.
+struct BuildArgs {
     const int32_t* qsl;        // [num_reqs + 1]
     const int32_t* positions;  // [num_rows]
-    int32_t num_reqs, num_rows;
-    int32_t row_begin, row_end;
-    int32_t seg_rows, max_segs;
-    int32_t topk, kpool, max_context;
-    int32_t score_all;         // 1: score every row's complete pools; 0: only rows with ctx > topk
-    int32_t pool_cap;          // no row scores more pools than this
     const int32_t* key_page_table;
     int64_t kpt_ld;
     int32_t max_key_pages, num_key_pages;
-    int32_t npad_max;          // query lines per q buffer (multiple of 16, <= 256)
-    int32_t stages;
-    uint32_t tmem_cols, acc_cols;
-    float* scores;             // select = 0: fp32 scores of the chunk's rows
+    int32_t num_reqs, num_rows;
+    int32_t row_begin, row_end;  // the chunk of rows handled by this launch
+    int32_t seg_rows;
+    int32_t topk, kpool, max_context;
+    int32_t score_all;  // 1: score every row's complete pools; 0: only rows with ctx > topk
+    int32_t pool_cap;   // no row scores more pools than this (the score row length)
+    int32_t max_segs;
+    int32_t* row_req;          // [row_end - row_begin]
+    int32_t* row_ctx;          // [row_end - row_begin]; -1 = no output (padding, bad row)
+    int4* seg;                 // [max_segs] {req, first row, rows, pools to score}
+    int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
+    int32_t* hdr;              // [0] segments, [1] tiles, [2] scorer's dynamic-tile counter (set to 0)
+    int32_t* status;
+    // shared-memory staging plan (filled by launch_build)
+    int32_t smem_qsl, smem_rows, smem_segs;
+    int32_t smem_rows_off, smem_segs_off, smem_prefix_off;
+};
+
+// Segmented scorer (TMA + tcgen05): CTAs take static shares of the tiles, then single
+// tiles from an atomic counter; each CTA resolves a tile's segment and key pages itself.
+struct ScoreArgs {
+    const int4* seg;
+    const int32_t* seg_tile_prefix;  // [segments + 1]
+    int32_t* hdr;            // [0] segments, [1] tiles; [2] dynamic-tile counter (zeroed by the builder)
+    const int32_t* key_page_table;
+    int64_t kpt_ld;
+    int32_t max_key_pages, num_key_pages, max_segs;
+    const int32_t* row_ctx;  // chunk-local
+    int32_t row_begin;
+    int32_t topk, kpool, score_all, pool_cap;
+    float* scores;           // chunk-local rows
     int64_t scores_ld;
-    int32_t select;
-    uint32_t* keys;            // select = 1: ordered keys [chunk rows][keys_ld] (workspace)
+    int32_t as_keys;         // 1: store ordered_key(score) (uint32 bits) instead of the fp32 score
+    int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
+    int32_t stages;
+    uint32_t tmem_cols;      // TMEM columns allocated (power of two)
+    uint32_t acc_cols;       // columns per accumulator buffer
+    int32_t* status;
+    int32_t fault_tile;      // failure-detection test: this tile's keys are never loaded (-1: none)
+    uint64_t wait_ns;        // limit of every bounded wait
+};
+
+// Per-row exact top-k pools, expansion and remap on the scorer's keys (one CTA per row).
+struct RowSelectArgs {
+    const uint32_t* keys;      // chunk-local rows: ordered_key of every complete pool's score
     int64_t keys_ld;
-    uint2* grp;                // select = 1: group records [chunk rows][grp_ld] (workspace)
-    int64_t grp_ld;
-    int32_t* ctr;              // counter words (workspace): zero at launch, zero again at exit
-    int32_t out_width, kpool_shift, bs_shift;
-    int32_t* slots;
+    const int32_t* row_ctx;    // chunk-local (builder output)
+    const int32_t* row_req;    // chunk-local (builder output)
+    int32_t stage_cap;         // keys staged in shared memory per row (multiple of 4)
+    int32_t bm_words;          // bitmap words per row, >= ceil(max pools / 32)
+    int32_t bt_cap;            // block-table entries staged in shared memory per row
+    int32_t row_begin;
+    int32_t topk, kpool, out_width;
+    int32_t kpool_shift;       // log2(kpool) when kpool is a power of two, else -1
+    int32_t bs_shift;          // log2(block_size) when block_size is a power of two, else -1
+    int32_t* slots;            // [rows][out_width] global rows
     int32_t* token_idx;        // nullable
     int32_t* counts;           // nullable
     const int32_t* block_table;
     int64_t bt_ld;
     int32_t max_blocks, num_kv_blocks, block_size;
     int64_t block_stride_rows;
-    int32_t bt_cap, cand_cap, gcap;
-    int32_t* status;
-    int32_t fault_tile;        // failure-detection test: this tile is never loaded (-1: none)
-    uint64_t wait_ns;          // limit of every wait
-    FusedLayout lay;
 };
-
-constexpr int kFusedThreads = 480;   // warp 0 TMA, 1 MMA, 2-5 epilogue, 6 signal, 7-14 select
-constexpr int kFusedSelThreads = 256;
-constexpr int kFusedSelWarp0 = 7;
-constexpr int kFusedSignalWarp = 6;
-constexpr int kFusedCtrHeader = 8;   // counter words before the per-segment and per-job words
-// The counter block has this fixed size (and sits at the start of every workspace), so a
-// workspace reused for a problem of another shape still begins with zero words.
-constexpr int kFusedCtrWords = 2048;
-constexpr int kFusedMaxChunkRows = 512;  // rows of one launch (the kernel plans them in shared memory)
-
-FusedLayout fused_layout(int stages, int npad_max, int max_segs, int chunk_cap, int bt_cap, int cand_cap, int gcap,
-                         int K);
-cudaError_t launch_fused(const FusedArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
-                         cudaStream_t s);
 
 // Top-k pools + expansion (+ remap), one CTA per row.
 struct TopkArgs {
@@ -140,22 +147,34 @@ struct MaxsimArgs {
     uint32_t tmem_cols;      // 256: two 128-column accumulators
     int32_t* counter;        // [2] grab counter and finished-CTA count: zero at the start, zero again at the end
     int32_t* status;
+    int32_t fault_tile;      // failure-detection test: each CTA leaves its tile of this index unloaded (-1: none)
+    uint64_t wait_ns;        // limit of every bounded wait
 };
 
+constexpr int kBuildThreads = 1024;
+constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 2048;
 constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin listed per row
 constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
+constexpr int kSelectThreads = 1024;
+constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
 constexpr int kMaxsimThreads = 256;     // warp 1 schedule, 2 MMA + TMEM, 3 TMA, 4-7 epilogue, 0 idle
 
+size_t score_smem_bytes(int stages, int npad_max, int max_segs);
 size_t topk_smem_bytes(int bt_cap);
 
 // Launchers. With `pdl` the kernel is a programmatic dependent of the previous kernel
 // on the stream: its prologue may overlap that kernel, and it waits (griddepcontrol)
 // before reading what that kernel wrote.
+cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
+cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
+                         size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_remap(const RemapArgs& a, int rows, RemapMode mode, cudaStream_t s);
+size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
+cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
 size_t maxsim_smem_bytes(int stages, int nq_pad, int kslabs);
 // Tensor maps of one MaxSim launch: the packed tensor with boxes of 8, 16, 24, 32, 64, 96 and
 // 128 rows (64 columns each), and the query block.

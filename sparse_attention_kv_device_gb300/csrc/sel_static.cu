@@ -17,10 +17,9 @@
 // call on that device outside capture is used, so make one call on each device before
 // capturing.
 //
-// Zeroing: the kernels rely on counter words at the start of their workspace being zero
-// when a launch starts, and every launch returns them to zero when it finishes (also after
-// a timeout). A file-scope device array starts zero-filled when the module is loaded, so the
-// array needs no clearing between calls.
+// Zeroing: the launch sequence clears every counter it relies on before use (the segment
+// builder resets the tile header and counter of each chunk; the row kernel clears its own
+// shared-memory histograms), so the array needs no clearing between calls.
 //
 // Sharing: all calls on one device share the one array. Two calls whose kernels overlap on
 // the GPU (different streams, no ordering between them) race on it and give wrong results;

@@ -29,7 +29,6 @@ ST_KEYPAGE_OOB = 1
 ST_CTX_OVER_BOUND = 2
 ST_TIMEOUT = 4
 ST_BAD_QSL = 8
-ST_BAD_WORKSPACE = 16
 
 
 class SelError(RuntimeError):
@@ -77,6 +76,7 @@ def _load():
     lib.sel_host_stage_bytes.argtypes = [PP, I32]
     lib.sel_host_stage_bytes.restype = SZ
     lib.sel_select_host.argtypes = [PP, P, I32, P, P, P, SZ, P, SZ, P]
+    lib.sel_set_trace_events.argtypes = [C.POINTER(C.c_void_p), I32]
     lib.sel_debug_wait_limit.argtypes = [I32, I64]
     lib.sel_select_launch_count.argtypes = [PP]
     lib.sel_select_launch_count.restype = I32
@@ -87,7 +87,8 @@ def _load():
     lib.sel_maxsim_launch_count.restype = I32
     for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
               "sel_select",
-              "sel_select_static", "sel_select_host", "sel_debug_wait_limit", "sel_maxsim_rerank"):
+              "sel_select_static", "sel_select_host", "sel_set_trace_events", "sel_debug_wait_limit",
+              "sel_maxsim_rerank"):
         getattr(lib, f).restype = C.c_int
     return lib
 
@@ -97,7 +98,8 @@ _lib = _load()
 EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_workspace_bytes",
            "sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
            "sel_select",
-           "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_debug_wait_limit",
+           "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
+           "sel_debug_wait_limit",
            "sel_select_launch_count", "sel_maxsim_workspace_bytes", "sel_maxsim_rerank", "sel_maxsim_launch_count"]
 
 
@@ -239,8 +241,8 @@ def sel_score_workspace_bytes(problem: Problem) -> int:
 
 
 def new_workspace(nbytes, device):
-    """A device workspace of nbytes, zero-filled as the library requires before first use
-    (its kernels return the counter words to zero, so it can be kept across calls)."""
+    """A zero-filled device workspace of nbytes (the MaxSim workspace must start zero-filled;
+    the selection's needs no initialisation, and zeros do no harm)."""
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
 
 
@@ -391,10 +393,22 @@ def sel_select_host(problem: Problem, slots_host, counts_host, stage, ws, status
     return slots_host, counts_host
 
 
+def sel_set_trace_events(events) -> None:
+    """events: four torch.cuda.Event(enable_timing=True), or None to switch tracing off."""
+    if not events:
+        _check(_lib.sel_set_trace_events(None, 0), "sel_set_trace_events")
+        return
+    for e in events:
+        if not e.cuda_event:   # torch creates the CUDA event on its first record
+            e.record()
+    arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(_lib.sel_set_trace_events(arr, len(events)), "sel_set_trace_events")
+
+
 def sel_debug_wait_limit(fault_tile: int = -1, wait_ns: int = 1_000_000_000) -> None:
-    """Failure-detection test hook: later fused launches give every bounded wait wait_ns and
-    (fault_tile >= 0) never load that tile's keys, so their waits expire. The defaults
-    restore normal operation."""
+    """Failure-detection test hook: later launches give every bounded wait wait_ns and
+    (fault_tile >= 0) never load that tile, so the waits on it expire. The defaults restore
+    normal operation."""
     _check(_lib.sel_debug_wait_limit(int(fault_tile), int(wait_ns)), "sel_debug_wait_limit")
 
 

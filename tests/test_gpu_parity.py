@@ -428,8 +428,24 @@ def test_select_host_path_matches_device():
     np.testing.assert_array_equal(counts_h.numpy(), ref["counts"])
 
 
-def test_one_launch_per_chunk():
+def test_trace_events_time_the_kernels():
     sel = lib()
-    for name, want in (("decode128k", 1), ("tiny", 1), ("mixed", 17)):
+    w = workloads.make_workload("decode32k")
+    prob = sel.problem_from_workload(w, DEV)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    slots = torch.empty((w.num_rows, w.out_width), dtype=torch.int32, device=DEV)
+    counts = torch.empty(w.num_rows, dtype=torch.int32, device=DEV)
+    sel.sel_set_trace_events(ev)
+    try:
+        sel.sel_select(prob, slots, counts)
+    finally:
+        sel.sel_set_trace_events(None)
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
+
+
+def test_launch_count_three_per_chunk():
+    sel = lib()
+    for name, chunks in (("decode128k", 1), ("tiny", 1), ("mixed", 17)):
         w = workloads.make_workload(name)
-        assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == want, name
+        assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == 3 * chunks, name
