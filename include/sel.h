@@ -119,7 +119,7 @@ typedef struct sel_problem {
 /* Message for a return code (static storage). */
 const char *sel_error_string(int code);
 
-/* ABI version of this header (major * 100 + minor): 101. */
+/* ABI version of this header (major * 100 + minor): 102. */
 int sel_version(void);
 
 /* Workspace (device bytes, 256-B aligned base) needed by sel_select / sel_score_paged
@@ -253,6 +253,40 @@ int sel_maxsim_rerank(const void *q, int32_t lq, int32_t d, int64_t q_stride, co
                       void *ws, size_t ws_bytes, sel_stream_t stream);
 /* Kernel launches one sel_maxsim_rerank call with this lq and d queues. */
 int32_t sel_maxsim_launch_count(int32_t lq, int32_t d);
+
+/*
+ * sel_mla_decode -- sparse MLA decode attention over the selected slots (vLLM page
+ * "flashinfer_mla_sparse_sm90", _SM90State: the MLA wrapper planned with page size 1, so the
+ * selection's slots are the page table, and the exact kv_len of _kv_lens_host). For row r,
+ * head h and each entry j < kv_len[r] whose slot s = slots[r][j] lies in [0, num_slots):
+ *     logit_j = sm_scale * (q_nope[r][h] . ckv[s] + q_pe[r][h] . kpe[s])
+ *     out[r][h] = sum_j softmax(logit)_j * ckv[s_j]      lse[r][h] = ln sum_j exp(logit_j)
+ * A -1 or out-of-range slot inside kv_len contributes nothing; entries past kv_len (the -1
+ * tail) are never read, nor is the cache row of a bad slot. A row with no such entry gives
+ * out = 0 and lse = -inf. kv_len above width counts as width.
+ *   q_nope bf16 (uint16 bit patterns) [rows][heads][dc] at qn_row_stride / qn_head_stride
+ *     elements; q_pe bf16 [rows][heads][dr] likewise (unused when dr == 0, may be NULL);
+ *   ckv bf16: slot s's dc latent dims at s * ckv_stride; kpe bf16: its dr rotary dims at
+ *     s * kpe_stride (kpe may alias ckv + dc: one cache row of dc + dr);
+ *   slots int32 [rows][width], kv_len int32 [rows];
+ *   out fp32 [rows][heads][dc] and lse fp32 [rows][heads] (written, contiguous).
+ * Scores and products run on the tensor cores with bf16 operands and fp32 accumulation; the
+ * softmax weights enter the second product rounded to bf16 (and are normalised by the sum of
+ * the rounded weights), the log-sum-exp uses the unrounded fp32 weights.
+ * Requires heads == 16, dc == 512, dr in {0, 64}, 1 <= width <= 8192, num_slots <= INT32_MAX,
+ * strides multiples of 8 elements, q_nope / q_pe / ckv / kpe 16-B aligned, and a 16-B aligned
+ * device workspace of sel_mla_workspace_bytes(rows, width) bytes (needs no initialisation;
+ * calls sharing one must not overlap on the GPU). Queues two kernels (sel_mla_launch_count).
+ * status (optional): SEL_ST_TIMEOUT if a bounded wait expired.
+ */
+size_t sel_mla_workspace_bytes(int32_t rows, int32_t width);
+int sel_mla_decode(const void *q_nope, int64_t qn_row_stride, int64_t qn_head_stride, const void *q_pe,
+                   int64_t qp_row_stride, int64_t qp_head_stride, int32_t rows, int32_t heads, int32_t dc,
+                   int32_t dr, const void *ckv, int64_t ckv_stride, const void *kpe, int64_t kpe_stride,
+                   int64_t num_slots, const int32_t *slots, int32_t width, const int32_t *kv_len,
+                   float sm_scale, float *out, float *lse, int32_t *status, void *ws, size_t ws_bytes,
+                   sel_stream_t stream);
+int32_t sel_mla_launch_count(int32_t rows);
 
 /*
  * sel_select -- the fused path (ReVolta PR #59, "Change": request segments built on the

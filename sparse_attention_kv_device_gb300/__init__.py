@@ -15,6 +15,9 @@ from .sel import (  # noqa: F401
     sel_maxsim_launch_count,
     sel_maxsim_rerank,
     sel_maxsim_workspace_bytes,
+    sel_mla_decode,
+    sel_mla_launch_count,
+    sel_mla_workspace_bytes,
     sel_remap_dcp,
     sel_remap_global,
     sel_remap_workspace,

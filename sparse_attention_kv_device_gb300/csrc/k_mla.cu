@@ -1,0 +1,555 @@
+// K-e: sparse MLA decode attention over the selected slots (vLLM page
+// "flashinfer_mla_sparse_sm90", _SM90State: FlashInfer's MLA wrapper planned with page size 1,
+// so the selection's slots are the page table, and the exact kv_len of _kv_lens_host).
+//
+// For row r and head h, over the entries j < kv_len[r] whose slot s = slots[r][j] lies in
+// [0, num_slots) (a -1 or out-of-range slot inside kv_len contributes nothing, and nothing
+// past kv_len is read):
+//   logit_j = sm_scale * (q_nope[r][h] . ckv[s] + q_pe[r][h] . kpe[s])
+//   out[r][h] = sum_j softmax(logit)_j * ckv[s_j],   lse[r][h] = log sum_j exp(logit_j)
+// with 16 heads, 512 latent and 0 or 64 rotary dims, bf16 inputs, fp32 outputs.
+//
+// The rows' tiles of 128 entries are laid end to end and cut into one contiguous run per CTA,
+// so the job spreads evenly over the SMs even for a handful of rows. Per tile:
+//   warps 0-3 (one entry per thread) read the entry's slot and gather its 576 dims from the
+//     cache with 16-byte cp.async into 64-dim boxes in the 128-byte swizzle layout (latent
+//     boxes in pairs, a ring of 5 pairs; the rotary box in a ring of 2). An entry past
+//     kv_len or with a bad slot is zero-filled without touching the cache;
+//   warp 4 (one thread) issues S^T[128 entries x 16 heads] = K_tile . Q^T on the tensor
+//     cores into TMEM (kind::f16, bf16 operands, fp32 accumulation) and, once the softmax
+//     has written P, O^T[512 x 16] += V^T . P^T, the same latent boxes read as an MN-major
+//     operand (a latent row is both key and value);
+//   warps 5-8 (one entry per thread) read the tile's logits from TMEM, keep the running
+//     maximum per head -- raised only when a logit exceeds it by more than 2^8, which then
+//     rescales O in TMEM --, and write p = 2^(logit - max) rounded to bf16 for the second
+//     product; the sums of p are kept per thread and reduced once per row.
+// A row whose tiles all ran in one CTA is normalised and written by that CTA; a row split
+// between CTAs leaves one partial (unnormalised O, maximum, sums) per CTA, and k_mla_merge
+// combines them.
+#include <cuda_bf16.h>
+
+#include "sel_device.cuh"
+#include "sel_kernels.h"
+
+namespace sel {
+
+namespace {
+
+constexpr int kPairSlots = 5;                  // latent pair buffers (boxes 2k, 2k+1)
+constexpr int kRopeSlots = 2;
+constexpr uint32_t kBoxBytes16 = 128 * 128;    // 64 dims x 128 entries, bf16
+constexpr uint32_t kPairBytes = 2 * kBoxBytes16;
+constexpr uint32_t kQBox = 16 * 128;           // 16 heads x 64 dims
+constexpr uint32_t kPBuf = 16 * 128 * 2;       // 16 heads x 128 entries
+constexpr uint32_t kOffRope = kPairSlots * kPairBytes;
+constexpr uint32_t kOffQ = kOffRope + kRopeSlots * kBoxBytes16;
+constexpr uint32_t kOffP = kOffQ + 9 * kQBox;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;
+// barriers
+constexpr int kBPairFull = 0, kBPairEmpty = kBPairFull + kPairSlots, kBRopeFull = kBPairEmpty + kPairSlots,
+              kBRopeEmpty = kBRopeFull + kRopeSlots, kBQFull = kBRopeEmpty + kRopeSlots, kBQEmpty = kBQFull + 1,
+              kBSFull = kBQEmpty + 1, kBSEmpty = kBSFull + 2, kBPFull = kBSEmpty + 2, kBPEmpty = kBPFull + 2,
+              kBODone = kBPEmpty + 2, kBOEmpty = kBODone + 1, kBDone = kBOEmpty + 2, kNumBars = kBDone + 1;
+constexpr uint32_t kOffWords = kOffBar + kNumBars * 8;       // tmem base, abort flag
+constexpr uint32_t kOffRed = kOffWords + 16;                  // 2 x 4 warps x 16 floats
+constexpr uint32_t kSmemUsed = kOffRed + 2 * 4 * 16 * 4;
+constexpr uint32_t kColS = 0, kColO = 32, kTmemCols = 256;   // S: 2 x 16 columns; O: 2 x 64
+constexpr float kRaise = 8.0f;                                // log2 of the largest p kept unscaled
+constexpr int kSoftBar = 1;                                   // named barrier of the softmax warps
+
+struct Seg {
+    int row, tin_a, tin_b;  // tiles tin_a..tin_b of the row
+    int n_act;              // tiles holding an entry below kv_len (a prefix of the segment)
+};
+
+__device__ __forceinline__ Seg segment_of(const MlaArgs& a, int64_t t0, int64_t t1, int row) {
+    Seg s;
+    s.row = row;
+    const int64_t r0 = static_cast<int64_t>(row) * a.tiles_per_row;
+    const int64_t lo = t0 > r0 ? t0 : r0, hi = t1 < r0 + a.tiles_per_row ? t1 : r0 + a.tiles_per_row;
+    s.tin_a = static_cast<int>(lo - r0);
+    s.tin_b = static_cast<int>(hi - 1 - r0);
+    int kvl = __ldg(a.kv_len + row);
+    kvl = max(0, min(kvl, a.width));
+    const int tiles = (kvl + kMlaTile - 1) / kMlaTile;
+    s.n_act = max(0, min(s.tin_b + 1, tiles) - s.tin_a);
+    return s;
+}
+
+__device__ __forceinline__ int entry_slot(const MlaArgs& a, int row, int e) {
+    int kvl = __ldg(a.kv_len + row);
+    kvl = min(kvl, a.width);
+    if (e >= kvl) return -1;
+    const int s = __ldg(a.slots + static_cast<int64_t>(row) * a.width + e);
+    return (s >= 0 && s < a.num_slots) ? s : -1;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Max (op 0) or sum (op 1) per head over the 128 softmax threads; `red` alternates between
+// two halves so back-to-back reductions need one barrier each.
+template <int op>
+__device__ __forceinline__ void soft_reduce(float (&v)[16], float* red, int& half, int sw, int lane) {
+    float* r = red + half * 64;
+    half ^= 1;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+        const float x = op == 0 ? warp_max(v[h]) : warp_sum(v[h]);
+        if (lane == 0) r[sw * 16 + h] = x;
+    }
+    named_bar_sync(kSoftBar, 128);
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+        const float a0 = r[h], a1 = r[16 + h], a2 = r[32 + h], a3 = r[48 + h];
+        v[h] = op == 0 ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) : (a0 + a1) + (a2 + a3);
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    uint32_t* words = reinterpret_cast<uint32_t*>(sm + kOffWords);
+    float* red = reinterpret_cast<float*>(sm + kOffRed);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * a.total_tiles / G;
+    const int64_t t1 = static_cast<int64_t>(blockIdx.x + 1) * a.total_tiles / G;
+    const int row_a = static_cast<int>(t0 / a.tiles_per_row);
+    const int row_b = static_cast<int>((t1 - 1) / a.tiles_per_row);
+    const int nbox_r = a.dr > 0 ? 1 : 0;  // rotary boxes per tile
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPairSlots; ++i) {
+            mbar_init(&bar[kBPairFull + i], 128);
+            mbar_init(&bar[kBPairEmpty + i], 1);
+        }
+        for (int i = 0; i < kRopeSlots; ++i) {
+            mbar_init(&bar[kBRopeFull + i], 128);
+            mbar_init(&bar[kBRopeEmpty + i], 1);
+        }
+        mbar_init(&bar[kBQFull], 128);
+        mbar_init(&bar[kBQEmpty], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[kBSFull + i], 1);
+            mbar_init(&bar[kBSEmpty + i], 4);
+            mbar_init(&bar[kBPFull + i], 4);
+            mbar_init(&bar[kBPEmpty + i], 1);
+            mbar_init(&bar[kBOEmpty + i], 4);
+        }
+        mbar_init(&bar[kBODone], 1);
+        mbar_init(&bar[kBDone], 1);
+        words[1] = 0;  // abort flag
+        mbar_fence_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(&words[0], kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = words[0];
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
+    auto fail = [&]() {
+        *abort_flag = 1;
+        report(a.status, kStTimeout);
+    };
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ gather (one entry per thread)
+        const int i = threadIdx.x;
+        int64_t tile_no = 0;  // active tiles so far in this CTA
+        int q_loads = 0;
+        bool ok = true;
+        for (int row = row_a; row <= row_b && ok; ++row) {
+            const Seg sg = segment_of(a, t0, t1, row);
+            if (sg.n_act == 0) continue;
+            // the row's queries: 16 heads x 9 boxes of 64 dims, in the K-major swizzle layout
+            if (!mbar_wait(&bar[kBQEmpty], (q_loads & 1) ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
+            {
+                const int h = i >> 3, c = i & 7;
+                const uint16_t* qn = a.q_nope + static_cast<int64_t>(row) * a.qn_row + h * a.qn_head;
+                uint8_t* qd = sm + kOffQ + h * 128 + ((c ^ (h & 7)) << 4);
+#pragma unroll
+                for (int b = 0; b < 8; ++b) cp_async_16(qd + b * kQBox, qn + 64 * b + 8 * c);
+                if (a.dr > 0)
+                    cp_async_16(qd + 8 * kQBox, a.q_pe + static_cast<int64_t>(row) * a.qp_row + h * a.qp_head + 8 * c);
+                cp_async_mbar_arrive(&bar[kBQFull]);
+            }
+            ++q_loads;
+            for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
+                const int e = (sg.tin_a + tt) * kMlaTile + i;
+                const int slot = entry_slot(a, row, e);
+                const uint32_t nb = slot >= 0 ? 16u : 0u;
+                const uint16_t* src = a.ckv + (slot >= 0 ? static_cast<int64_t>(slot) * a.ckv_stride : 0);
+                const uint32_t sw = static_cast<uint32_t>(i & 7);
+                for (int pr = 0; pr < 4; ++pr) {
+                    const int64_t n = tile_no * 4 + pr;
+                    const int ps = static_cast<int>(n % kPairSlots);
+                    if (!mbar_wait(&bar[kBPairEmpty + ps], static_cast<uint32_t>((n / kPairSlots) & 1) ^ 1u, abort_flag,
+                                   a.wait_ns)) { ok = false; break; }
+                    uint8_t* dst = sm + ps * kPairBytes + i * 128;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            cp_async_16_zfill(dst + half * kBoxBytes16 + ((c ^ sw) << 4),
+                                              src + (2 * pr + half) * 64 + 8 * c, nb);
+                    cp_async_mbar_arrive(&bar[kBPairFull + ps]);
+                }
+                if (!ok) break;
+                if (nbox_r) {
+                    const int rs = static_cast<int>(tile_no % kRopeSlots);
+                    if (!mbar_wait(&bar[kBRopeEmpty + rs], static_cast<uint32_t>((tile_no / kRopeSlots) & 1) ^ 1u,
+                                   abort_flag, a.wait_ns)) { ok = false; break; }
+                    const uint16_t* srp = a.kpe + (slot >= 0 ? static_cast<int64_t>(slot) * a.kpe_stride : 0);
+                    uint8_t* dst = sm + kOffRope + rs * kBoxBytes16 + i * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) cp_async_16_zfill(dst + ((c ^ sw) << 4), srp + 8 * c, nb);
+                    cp_async_mbar_arrive(&bar[kBRopeFull + rs]);
+                }
+            }
+        }
+        if (!ok) fail();
+        cp_async_wait_all();  // nothing lands in shared memory after the CTA leaves
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = umma_idesc_bf16_f32(kMlaTile, kMlaHeads, 0);
+            const uint32_t idesc_o = umma_idesc_bf16_f32(kMlaTile, kMlaHeads, 1);
+            const uint32_t base = smem_u32(sm);
+            int64_t tile_no = 0;
+            int q_loads = 0, o_segs = 0;
+            bool ok = true;
+            for (int row = row_a; row <= row_b && ok; ++row) {
+                const Seg sg = segment_of(a, t0, t1, row);
+                if (sg.n_act == 0) continue;
+                if (!mbar_wait(&bar[kBQFull], q_loads & 1, abort_flag, a.wait_ns)) { ok = false; break; }
+                ++q_loads;
+                const int ob = o_segs & 1;
+                if (!mbar_wait(&bar[kBOEmpty + ob], static_cast<uint32_t>((o_segs >> 1) & 1) ^ 1u, abort_flag,
+                               a.wait_ns)) { ok = false; break; }
+                ++o_segs;
+                for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
+                    const int sb = static_cast<int>(tile_no & 1);
+                    const uint32_t use = static_cast<uint32_t>((tile_no >> 1) & 1);
+                    if (!mbar_wait(&bar[kBSEmpty + sb], use ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_s = tmem + kColS + 16u * sb;
+                    for (int pr = 0; pr < 4 && ok; ++pr) {
+                        const int64_t n = tile_no * 4 + pr;
+                        const int ps = static_cast<int>(n % kPairSlots);
+                        if (!mbar_wait(&bar[kBPairFull + ps], static_cast<uint32_t>((n / kPairSlots) & 1), abort_flag,
+                                       a.wait_ns)) { ok = false; break; }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = umma_desc_sw128(base + ps * kPairBytes + half * kBoxBytes16 + 32u * kk);
+                                const uint64_t bd = umma_desc_sw128(base + kOffQ + (2 * pr + half) * kQBox + 32u * kk);
+                                umma_f16(d_s, ad, bd, idesc_s, (pr | half | kk) ? 1u : 0u);
+                            }
+                    }
+                    if (!ok) break;
+                    if (nbox_r) {
+                        const int rs = static_cast<int>(tile_no % kRopeSlots);
+                        if (!mbar_wait(&bar[kBRopeFull + rs], static_cast<uint32_t>((tile_no / kRopeSlots) & 1),
+                                       abort_flag, a.wait_ns)) { ok = false; break; }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = umma_desc_sw128(base + kOffRope + rs * kBoxBytes16 + 32u * kk);
+                            const uint64_t bd = umma_desc_sw128(base + kOffQ + 8 * kQBox + 32u * kk);
+                            umma_f16(d_s, ad, bd, idesc_s, 1u);
+                        }
+                        umma_commit(&bar[kBRopeEmpty + rs]);
+                    }
+                    umma_commit(&bar[kBSFull + sb]);
+                    if (tt == sg.n_act - 1) umma_commit(&bar[kBQEmpty]);  // the row's queries are free
+                    // O^T += V^T . P^T once the softmax has written this tile's P
+                    if (!mbar_wait(&bar[kBPFull + sb], use, abort_flag, a.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t pb = base + kOffP + sb * kPBuf;
+                    for (int mb = 0; mb < 4; ++mb) {
+                        const int64_t n = tile_no * 4 + mb;
+                        const int ps = static_cast<int>(n % kPairSlots);
+                        const uint32_t d_o = tmem + kColO + 64u * ob + 16u * mb;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t ad = umma_desc_sw128_mn(base + ps * kPairBytes + 2048u * kk, kBoxBytes16);
+                            const uint64_t bd = umma_desc_sw128(pb + (kk >> 2) * 2048u + 32u * (kk & 3));
+                            umma_f16(d_o, ad, bd, idesc_o, (tt == 0 && kk == 0) ? 0u : 1u);
+                        }
+                        umma_commit(&bar[kBPairEmpty + ps]);
+                    }
+                    umma_commit(&bar[kBPEmpty + sb]);
+                    umma_commit(&bar[kBODone]);
+                }
+            }
+            if (!ok) fail();
+            umma_commit(&bar[kBDone]);  // every MMA issued has finished before teardown
+            mbar_wait(&bar[kBDone], 0, nullptr, a.wait_ns);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + output
+        const int sw = warp - 5;             // softmax warp 0..3
+        const int quarter = warp & 3;        // TMEM lanes this warp may access
+        const int j = quarter * 32 + lane;   // entry of the tile / dim within an O block
+        int64_t tile_no = 0;
+        int o_segs = 0, half = 0;
+        bool ok = true;
+        for (int row = row_a; row <= row_b && ok; ++row) {
+            const Seg sg = segment_of(a, t0, t1, row);
+            const bool whole = sg.tin_a == 0 && sg.tin_b == a.tiles_per_row - 1;
+            float m_run[16], l_bf[16], l_ex[16];
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+                m_run[h] = -INFINITY;
+                l_bf[h] = 0.0f;
+                l_ex[h] = 0.0f;
+            }
+            const int ob = o_segs & 1;
+            for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
+                const int sb = static_cast<int>(tile_no & 1);
+                const uint32_t use = static_cast<uint32_t>((tile_no >> 1) & 1);
+                const int e = (sg.tin_a + tt) * kMlaTile + j;
+                const bool valid = entry_slot(a, row, e) >= 0;
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(&bar[kBSFull + sb], use, abort_flag, a.wait_ns) ? 1 : 0;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }  // the four warps leave together
+                tc_fence_after();
+                uint32_t raw[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColS + 16u * sb, raw);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kBSEmpty + sb]);
+                float x[16];
+                bool need = tt == 0;
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    x[h] = valid ? __uint_as_float(raw[h]) * a.scale_log2 : -INFINITY;
+                    need |= x[h] > m_run[h] + kRaise;
+                }
+                need = bar_red_or(need, kSoftBar, 128);
+                if (need) {
+                    float t[16];
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) t[h] = x[h];
+                    soft_reduce<0>(t, red, half, sw, lane);
+                    float alpha[16];
+                    bool grow = false;
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) {
+                        const float mn = fmaxf(m_run[h], t[h]);
+                        alpha[h] = mn > m_run[h] ? exp2f(m_run[h] - mn) : 1.0f;
+                        grow |= mn > m_run[h];
+                        m_run[h] = mn;
+                    }
+                    if (grow && tt > 0) {
+                        // every earlier product of this row has finished: the MMA thread issued
+                        // them before this tile's scores, whose completion was awaited above
+#pragma unroll
+                        for (int h = 0; h < 16; ++h) {
+                            l_bf[h] *= alpha[h];
+                            l_ex[h] *= alpha[h];
+                        }
+                        for (int mb = 0; mb < 4; ++mb) {
+                            const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColO + 64u * ob +
+                                                16u * mb;
+                            uint32_t ov[16];
+                            tmem_ld16(ta, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int h = 0; h < 16; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                            tmem_st16(ta, ov);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                    }
+                }
+                // p = 2^(x - max), rounded to bf16 for the product; both sums kept per thread
+                uint16_t pb[16];
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    const float p = x[h] == -INFINITY ? 0.0f : exp2f(x[h] - m_run[h]);
+                    const __nv_bfloat16 b = __float2bfloat16_rn(p);
+                    pb[h] = __bfloat16_as_ushort(b);
+                    l_bf[h] += __bfloat162float(b);
+                    l_ex[h] += p;
+                }
+                if (lane == 0) okw = mbar_wait(&bar[kBPEmpty + sb], use ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }
+                uint8_t* pbase = sm + kOffP + sb * kPBuf + (j >> 6) * 2048 + (j & 7) * 2;
+                const uint32_t chunk = static_cast<uint32_t>((j & 63) >> 3);
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    *reinterpret_cast<uint16_t*>(pbase + h * 128 + ((chunk ^ (h & 7)) << 4)) = pb[h];
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kBPFull + sb]);
+            }
+            if (!ok) break;
+            // ---- the row's (or partial row's) result
+            soft_reduce<1>(l_bf, red, half, sw, lane);
+            soft_reduce<1>(l_ex, red, half, sw, lane);
+            const int pslot = 2 * static_cast<int>(blockIdx.x) + (row == row_a ? 0 : 1);
+            float* part = reinterpret_cast<float*>(a.part + static_cast<size_t>(pslot) * kMlaPartBytes);
+            if (sg.n_act > 0) {
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(&bar[kBODone], static_cast<uint32_t>((tile_no - 1) & 1), abort_flag,
+                                               a.wait_ns) ? 1 : 0;
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }
+                tc_fence_after();
+                for (int mb = 0; mb < 4; ++mb) {
+                    uint32_t ov[16];
+                    tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColO + 64u * ob + 16u * mb, ov);
+                    tmem_ld_wait();
+                    const int d = mb * 128 + j;
+                    if (whole) {
+                        float* o = a.out + static_cast<int64_t>(row) * (kMlaHeads * kMlaDc) + d;
+#pragma unroll
+                        for (int h = 0; h < 16; ++h)
+                            o[h * kMlaDc] = l_bf[h] > 0.0f ? __uint_as_float(ov[h]) / l_bf[h] : 0.0f;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 16; ++h) part[h * kMlaDc + d] = __uint_as_float(ov[h]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kBOEmpty + ob]);
+                ++o_segs;
+            } else if (whole) {
+                for (int d = j; d < kMlaDc; d += 128) {
+                    float* o = a.out + static_cast<int64_t>(row) * (kMlaHeads * kMlaDc) + d;
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) o[h * kMlaDc] = 0.0f;
+                }
+            }
+            // one thread per head: the row's log-sum-exp, or the partial's maximum and sums
+            if (sw == 0 && lane < 16) {
+                float mh = 0.0f, lb = 0.0f, le = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    if (h == lane) {
+                        mh = m_run[h];
+                        lb = l_bf[h];
+                        le = l_ex[h];
+                    }
+                if (whole) {
+                    a.lse[static_cast<int64_t>(row) * kMlaHeads + lane] =
+                        le > 0.0f ? (mh + log2f(le)) * 0.69314718055994531f : -INFINITY;
+                } else {
+                    part[kMlaHeads * kMlaDc + lane] = le > 0.0f ? mh : -INFINITY;
+                    part[kMlaHeads * kMlaDc + 16 + lane] = lb;
+                    part[kMlaHeads * kMlaDc + 32 + lane] = le;
+                }
+            }
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) {
+        __syncwarp();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// One CTA per row: a row whose tiles ran in more than one CTA gets the weighted combination
+// of their partials (weights 2^(m_c - max_c m_c)); other rows were written whole. A row has
+// at most 64 tiles (the host checks), so at most 64 partials.
+__global__ void __launch_bounds__(256) k_mla_merge(const MlaArgs a, int grid) {
+    const int row = blockIdx.x;
+    const int64_t tpr = a.tiles_per_row, total = a.total_tiles, G = grid;
+    const int64_t first = static_cast<int64_t>(row) * tpr, last = first + tpr - 1;
+    // CTA c runs tiles [c * total / G, (c + 1) * total / G): the CTA of tile t is the last c
+    // whose first tile is <= t
+    const int c_lo = static_cast<int>(((first + 1) * G - 1) / total);
+    const int c_hi = static_cast<int>(((last + 1) * G - 1) / total);
+    if (c_lo == c_hi) return;
+    __shared__ float wgt[64][16];
+    __shared__ float inv[16];
+    __shared__ float lse_s[16];
+    if (threadIdx.x < 16) {
+        const int h = threadIdx.x;
+        float mx = -INFINITY;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
+            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
+            mx = fmaxf(mx, p[kMlaHeads * kMlaDc + h]);
+        }
+        float lb = 0.0f, le = 0.0f;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
+            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
+            const float m = p[kMlaHeads * kMlaDc + h];
+            const float w = (m == -INFINITY) ? 0.0f : exp2f(m - mx);
+            if (c - c_lo < 64) wgt[c - c_lo][h] = w;
+            lb += w * p[kMlaHeads * kMlaDc + 16 + h];
+            le += w * p[kMlaHeads * kMlaDc + 32 + h];
+        }
+        inv[h] = lb > 0.0f ? 1.0f / lb : 0.0f;
+        lse_s[h] = le > 0.0f ? (mx + log2f(le)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) a.lse[static_cast<int64_t>(row) * kMlaHeads + threadIdx.x] = lse_s[threadIdx.x];
+    for (int idx = threadIdx.x; idx < kMlaHeads * kMlaDc; idx += blockDim.x) {
+        const int h = idx / kMlaDc;
+        float acc = 0.0f;
+        for (int c = c_lo; c <= c_hi && c - c_lo < 64; ++c) {
+            const float w = wgt[c - c_lo][h];
+            if (w == 0.0f) continue;
+            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
+            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
+            acc += w * p[idx];
+        }
+        a.out[static_cast<int64_t>(row) * (kMlaHeads * kMlaDc) + idx] = acc * inv[h];
+    }
+}
+
+size_t mla_smem_bytes() { return kSmemUsed + 1024; }
+
+cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s) {
+    static size_t configured[kMaxDevicesTracked] = {};
+    const size_t smem = mla_smem_bytes();
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_mla_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured[dev] = smem;
+    }
+    k_mla_decode<<<grid, kMlaThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s) {
+    k_mla_merge<<<a.rows, 256, 0, s>>>(a, grid);
+    return cudaGetLastError();
+}
+
+}  // namespace sel

@@ -395,7 +395,7 @@ const char* sel_error_string(int code) {
     }
 }
 
-int sel_version(void) { return 101; }
+int sel_version(void) { return 102; }
 
 size_t sel_workspace_bytes(const sel_problem* p) {
     Plan pl;
@@ -603,6 +603,85 @@ int sel_maxsim_rerank(const void* q, int32_t lq, int32_t d, int64_t q_stride, co
     }
     return SEL_OK;
 }
+
+// ------------------------------------------------------------------ sparse MLA decode
+namespace {
+int mla_grid(int32_t rows, int32_t width, int sms, int64_t* total) {
+    const int64_t tpr = ceil_div(width, kMlaTile);
+    *total = static_cast<int64_t>(rows) * tpr;
+    return static_cast<int>(std::min<int64_t>(sms, *total));
+}
+}  // namespace
+
+size_t sel_mla_workspace_bytes(int32_t rows, int32_t width) {
+    if (rows <= 0 || width <= 0) return 0;
+    DeviceInfo di;
+    if (current_device_info(&di) != SEL_OK) return 0;
+    int64_t total = 0;
+    const int grid = mla_grid(rows, width, di.sms, &total);
+    return static_cast<size_t>(2 * grid) * kMlaPartBytes;
+}
+
+int sel_mla_decode(const void* q_nope, int64_t qn_row_stride, int64_t qn_head_stride, const void* q_pe,
+                   int64_t qp_row_stride, int64_t qp_head_stride, int32_t rows, int32_t heads, int32_t dc, int32_t dr,
+                   const void* ckv, int64_t ckv_stride, const void* kpe, int64_t kpe_stride, int64_t num_slots,
+                   const int32_t* slots, int32_t width, const int32_t* kv_len, float sm_scale, float* out, float* lse,
+                   int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {
+    if (rows < 0 || width < 1 || num_slots < 0) return SEL_EINVAL;
+    if (rows == 0) return SEL_OK;
+    if (!q_nope || !ckv || !slots || !kv_len || !out || !lse || !ws) return SEL_EINVAL;
+    if (dr > 0 && (!q_pe || !kpe)) return SEL_EINVAL;
+    if (heads != kMlaHeads || dc != kMlaDc || (dr != 0 && dr != 64)) return SEL_EUNSUPPORTED;
+    if (ceil_div(width, kMlaTile) > 64 || num_slots > INT32_MAX) return SEL_EUNSUPPORTED;
+    if (qn_head_stride < dc || qn_row_stride < static_cast<int64_t>(heads) * qn_head_stride || ckv_stride < dc)
+        return SEL_EINVAL;
+    if (dr > 0 && (qp_head_stride < dr || qp_row_stride < static_cast<int64_t>(heads) * qp_head_stride || kpe_stride < dr))
+        return SEL_EINVAL;
+    auto a8 = [](int64_t v) { return v % 8 == 0; };
+    if (!a8(qn_row_stride) || !a8(qn_head_stride) || !a8(ckv_stride) || !aligned16(q_nope) || !aligned16(ckv) ||
+        (reinterpret_cast<uintptr_t>(ws) & 15u) != 0)
+        return SEL_EUNSUPPORTED;
+    if (dr > 0 && (!a8(qp_row_stride) || !a8(qp_head_stride) || !a8(kpe_stride) || !aligned16(q_pe) || !aligned16(kpe)))
+        return SEL_EUNSUPPORTED;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != SEL_OK) return rc;
+    if (mla_smem_bytes() > static_cast<size_t>(di.max_smem_optin)) return SEL_EUNSUPPORTED;
+    int64_t total = 0;
+    const int grid = mla_grid(rows, width, di.sms, &total);
+    if (ws_bytes < static_cast<size_t>(2 * grid) * kMlaPartBytes) return SEL_EWORKSPACE;
+    MlaArgs a{};
+    a.q_nope = static_cast<const uint16_t*>(q_nope);
+    a.qn_row = qn_row_stride;
+    a.qn_head = qn_head_stride;
+    a.q_pe = static_cast<const uint16_t*>(q_pe);
+    a.qp_row = qp_row_stride;
+    a.qp_head = qp_head_stride;
+    a.ckv = static_cast<const uint16_t*>(ckv);
+    a.ckv_stride = ckv_stride;
+    a.kpe = static_cast<const uint16_t*>(kpe);
+    a.kpe_stride = kpe_stride;
+    a.num_slots = num_slots;
+    a.slots = slots;
+    a.kv_len = kv_len;
+    a.width = width;
+    a.rows = rows;
+    a.dr = dr;
+    a.tiles_per_row = static_cast<int32_t>(ceil_div(width, kMlaTile));
+    a.total_tiles = total;
+    a.scale_log2 = sm_scale * 1.4426950408889634f;
+    a.out = out;
+    a.lse = lse;
+    a.part = static_cast<uint8_t*>(ws);
+    a.status = status;
+    a.wait_ns = g_wait_ns;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_mla(a, grid, s) != cudaSuccess) return SEL_ECUDA;
+    if (launch_mla_merge(a, grid, s) != cudaSuccess) return SEL_ECUDA;
+    return SEL_OK;
+}
+
+int32_t sel_mla_launch_count(int32_t rows) { return rows > 0 ? 2 : 0; }
 
 int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,
                int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {

@@ -151,6 +151,39 @@ struct MaxsimArgs {
     uint64_t wait_ns;        // limit of every bounded wait
 };
 
+// Sparse MLA decode attention over selected slots: one launch over all rows' tiles of 128
+// entries, each CTA a contiguous run of tiles (a row's tiles may span CTAs), then one merge
+// launch that combines the partial results of rows split between CTAs.
+struct MlaArgs {
+    const uint16_t* q_nope;    // bf16 [rows][16][512] at row / head strides (elements)
+    int64_t qn_row, qn_head;
+    const uint16_t* q_pe;      // bf16 [rows][16][dr]
+    int64_t qp_row, qp_head;
+    const uint16_t* ckv;       // bf16, slot s's 512 latent dims at s * ckv_stride
+    int64_t ckv_stride;
+    const uint16_t* kpe;       // bf16, slot s's dr rotary dims at s * kpe_stride
+    int64_t kpe_stride;
+    int64_t num_slots;
+    const int32_t* slots;      // [rows][width]
+    const int32_t* kv_len;     // [rows]
+    int32_t width, rows, dr, tiles_per_row;
+    int64_t total_tiles;
+    float scale_log2;          // sm_scale * log2(e): logits in base-2 units
+    float* out;                // fp32 [rows][16][512]
+    float* lse;                // fp32 [rows][16], natural logarithm
+    uint8_t* part;             // partial results: [2 * grid] slots of kMlaPartBytes
+    int32_t* status;
+    uint64_t wait_ns;
+};
+constexpr int kMlaHeads = 16;
+constexpr int kMlaDc = 512;
+constexpr int kMlaTile = 128;                   // entries per tile
+constexpr int kMlaThreads = 288;                // warps 0-3 gather, 4 MMA + TMEM, 5-8 softmax
+constexpr size_t kMlaPartBytes = 33024;         // O [16][512] fp32, m / l / l_exact [16] fp32
+size_t mla_smem_bytes();
+cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s);
+
 constexpr int kBuildThreads = 1024;
 constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 constexpr int kTopkThreads = 512;

@@ -84,6 +84,11 @@ def _load():
     lib.sel_maxsim_workspace_bytes.restype = SZ
     lib.sel_maxsim_rerank.argtypes = [P, I32, I32, I64, P, I64, I64, P, P, I32, P, P, P, SZ, P]
     lib.sel_maxsim_launch_count.argtypes = [I32, I32]
+    lib.sel_mla_workspace_bytes.argtypes = [I32, I32]
+    lib.sel_mla_workspace_bytes.restype = SZ
+    lib.sel_mla_decode.argtypes = [P, I64, I64, P, I64, I64, I32, I32, I32, I32, P, I64, P, I64, I64, P, I32, P,
+                                   C.c_float, P, P, P, P, SZ, P]
+    lib.sel_mla_launch_count.argtypes = [I32]
     lib.sel_maxsim_launch_count.restype = I32
     for f in ("sel_score_paged", "sel_topk_expand", "sel_remap_global", "sel_remap_workspace", "sel_remap_dcp",
               "sel_select",
@@ -100,7 +105,8 @@ EXPORTS = ["sel_error_string", "sel_version", "sel_workspace_bytes", "sel_score_
            "sel_select",
            "sel_select_static", "sel_host_stage_bytes", "sel_select_host", "sel_set_trace_events",
            "sel_debug_wait_limit",
-           "sel_select_launch_count", "sel_maxsim_workspace_bytes", "sel_maxsim_rerank", "sel_maxsim_launch_count"]
+           "sel_select_launch_count", "sel_maxsim_workspace_bytes", "sel_maxsim_rerank", "sel_maxsim_launch_count",
+           "sel_mla_workspace_bytes", "sel_mla_decode", "sel_mla_launch_count"]
 
 
 def library_path() -> str:
@@ -457,3 +463,59 @@ def sel_maxsim_rerank(q, docs, doc_offsets, doc_lengths, scores=None, status=Non
 
 def sel_maxsim_launch_count(lq: int, d: int) -> int:
     return int(_lib.sel_maxsim_launch_count(int(lq), int(d)))
+
+
+def sel_mla_workspace_bytes(rows: int, width: int) -> int:
+    return int(_lib.sel_mla_workspace_bytes(int(rows), int(width)))
+
+
+def sel_mla_decode(q_nope, q_pe, ckv, kpe, slots, kv_len, sm_scale, out=None, lse=None, status=None, ws=None,
+                   stream=None):
+    """Sparse MLA decode attention over the selected slots.
+
+    q_nope bf16 [rows, 16, 512]; q_pe bf16 [rows, 16, dr] with dr 0 or 64 (None for 0);
+    ckv bf16 [num_slots, >= 512] (row stride a multiple of 8); kpe bf16 [num_slots, >= dr]
+    (None for dr 0; may be a column slice of the same cache tensor); slots int32 [rows, width];
+    kv_len int32 [rows]. Returns (out fp32 [rows, 16, 512], lse fp32 [rows, 16])."""
+    _dev(q_nope, torch.bfloat16, "q_nope")
+    _dev(q_pe, torch.bfloat16, "q_pe")
+    _dev(ckv, torch.bfloat16, "ckv")
+    _dev(kpe, torch.bfloat16, "kpe")
+    _dev(slots, torch.int32, "slots")
+    _dev(kv_len, torch.int32, "kv_len")
+    _dev(status, torch.int32, "status")
+    _on_current_device("sel_mla_decode", q_nope, q_pe, ckv, kpe, slots, kv_len, out, lse, status, ws)
+    if q_nope.dim() != 3 or q_nope.stride(2) != 1:
+        raise ValueError("q_nope must be [rows, heads, dc] with unit dim stride")
+    rows, heads, dc = q_nope.shape
+    dr = 0 if q_pe is None else int(q_pe.shape[2])
+    if q_pe is not None and (q_pe.dim() != 3 or q_pe.shape[:2] != q_nope.shape[:2] or q_pe.stride(2) != 1):
+        raise ValueError("q_pe must be [rows, heads, dr] with unit dim stride")
+    if ckv.dim() != 2 or ckv.stride(1) != 1 or (kpe is not None and (kpe.dim() != 2 or kpe.stride(1) != 1)):
+        raise ValueError("ckv / kpe must be [num_slots, dims] with unit column stride")
+    if (dr > 0) != (kpe is not None):
+        raise ValueError("kpe is needed exactly when q_pe has rotary dims")
+    if slots.dim() != 2 or slots.shape[0] != rows or not slots.is_contiguous() or not kv_len.is_contiguous():
+        raise ValueError("slots must be contiguous [rows, width]; kv_len contiguous [rows]")
+    width = int(slots.shape[1])
+    if out is None:
+        out = torch.empty((rows, heads, dc), dtype=torch.float32, device=q_nope.device)
+    if lse is None:
+        lse = torch.empty((rows, heads), dtype=torch.float32, device=q_nope.device)
+    _dev(out, torch.float32, "out")
+    _dev(lse, torch.float32, "lse")
+    if not out.is_contiguous() or not lse.is_contiguous():
+        raise ValueError("out and lse must be contiguous")
+    ws = _workspace(ws, sel_mla_workspace_bytes(rows, width), q_nope.device)
+    _check(_lib.sel_mla_decode(_ptr(q_nope), int(q_nope.stride(0)), int(q_nope.stride(1)), _ptr(q_pe),
+                               int(q_pe.stride(0)) if q_pe is not None else 0,
+                               int(q_pe.stride(1)) if q_pe is not None else 0, int(rows), int(heads), int(dc),
+                               int(dr), _ptr(ckv), int(ckv.stride(0)), _ptr(kpe),
+                               int(kpe.stride(0)) if kpe is not None else 0, int(ckv.shape[0]), _ptr(slots), width,
+                               _ptr(kv_len), float(sm_scale), _ptr(out), _ptr(lse), _ptr(status), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "sel_mla_decode")
+    return out, lse
+
+
+def sel_mla_launch_count(rows: int) -> int:
+    return int(_lib.sel_mla_launch_count(int(rows)))

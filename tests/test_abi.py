@@ -46,7 +46,7 @@ def test_error_strings(lib):
     lib.sel_error_string.restype = C.c_char_p
     for code in (0, -1, -2, -3, -4, -99):
         assert lib.sel_error_string(code)
-    assert lib.sel_version() == 101
+    assert lib.sel_version() == 102
 
 
 def test_wait_limit_hook_validates_and_restores(lib):
