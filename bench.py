@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-remap", action="store_true", help="skip the stand-alone remap measurements")
     ap.add_argument("--no-maxsim", action="store_true", help="skip the MaxSim rerank measurement")
+    ap.add_argument("--no-mla", action="store_true", help="skip the sparse MLA decode measurement")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (profiling runs)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the ragged and mixed workloads measured beside the headline")
@@ -364,6 +365,66 @@ def maxsim_rerank(sel, torch, dev, stream, flush, peak, iters):
             "gpu_launches": sel.sel_maxsim_launch_count(lq, d)}
 
 
+def mla_decode(sel, torch, dev, stream, flush, peak, tpeak, iters):
+    """Sparse MLA decode attention over the selected slots of the 128K decode step: 40 rows x
+    16 heads, 2,048..2,051 entries per row gathered from a 2^20-slot bf16 cache (1.2 GB) of
+    512 latent + 64 rotary dims. CUDA-graph replay of the call (two kernels), L2 flushed before
+    each replay, CUDA events on the launching stream. Algorithmic bytes: every valid entry's
+    cache row once (1,152 B), the slot indices read (4 B per entry below kv_len), the queries,
+    out (fp32) and lse written. FLOPs: both products, 2 * 16 * (576 + 512) per entry."""
+    from workloads.mla import make_mla
+    w = make_mla("mla_decode128k")
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    cache = bf(w.cache)
+    qn, qp = bf(w.q_nope), bf(w.q_pe)
+    ckv, kpe = cache[:, :w.dc], cache[:, w.dc:]
+    slots = torch.from_numpy(w.slots).to(dev)
+    kv_len = torch.from_numpy(w.kv_len).to(dev)
+    rows, heads, dc = w.q_nope.shape
+    out = torch.empty((rows, heads, dc), dtype=torch.float32, device=dev)
+    lse = torch.empty((rows, heads), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = sel.new_workspace(sel.sel_mla_workspace_bytes(rows, w.slots.shape[1]), dev)
+    call = lambda: sel.sel_mla_decode(qn, qp, ckv, kpe, slots, kv_len, w.sm_scale, out=out, lse=lse,
+                                      status=status, ws=ws, stream=stream)
+    valid = 0
+    for r in range(rows):
+        s = w.slots[r, :int(w.kv_len[r])]
+        valid += int(((s >= 0) & (s < w.cache.shape[0])).sum())
+    entries = int(np.minimum(w.kv_len, w.slots.shape[1]).sum())
+    nbytes = (valid * (w.dc + w.dr) * 2 + entries * 4 + rows * 4 + rows * heads * (w.dc + w.dr) * 2
+              + rows * heads * (dc + 1) * 4)
+    flops = 2 * heads * (w.dc + w.dr + w.dc) * valid
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    with torch.cuda.stream(stream):
+        graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            flush()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the MLA decode")
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = float(np.mean(times))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"mla_decode128k: {rows} rows x {heads} heads, {entries} entries "
+                        f"({valid} valid), dc {w.dc} + dr {w.dr} bf16, 2^20 cache slots",
+            "algorithmic_bytes": nbytes, "us": ms * 1e3, "us_median": float(np.median(times)) * 1e3,
+            "rows_per_s": rows / (ms * 1e-3), "GB/s": gbs, "frac": gbs / peak, "bound": "hbm",
+            "algorithmic_flops": flops, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "tensor_frac": flops / (ms * 1e-3) / 1e12 / tpeak,
+            "traffic": recorded_traffic("k_mla.cu", "mla_decode128k"),
+            "gpu_launches": sel.sel_mla_launch_count(rows)}
+
+
 def eager_steps(sel, torch, prob, slots, counts, ws, stream, flush, rows, iters):
     """The same step launched eagerly (sel_select called from Python every step, no graph), L2
     flushed before each call, CUDA events on the stream around each call."""
@@ -587,6 +648,9 @@ def run_ours(args):
     maxsim = None
     if not args.no_maxsim:
         maxsim = auxiliary(lambda: maxsim_rerank(sel, torch, dev, stream, flush, peak, 20))
+    mla = None
+    if not args.no_mla:
+        mla = auxiliary(lambda: mla_decode(sel, torch, dev, stream, flush, peak, tpeak, 20))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -631,6 +695,8 @@ def run_ours(args):
             line["remap_modes"] = remap
         if maxsim:
             line["maxsim_rerank"] = maxsim
+        if mla:
+            line["mla_decode"] = mla
         if configs:
             line["configs"] = configs
         print(json.dumps(line), flush=True)

@@ -274,7 +274,7 @@ int32_t sel_maxsim_launch_count(int32_t lq, int32_t d);
  * softmax weights enter the second product rounded to bf16 (and are normalised by the sum of
  * the rounded weights), the log-sum-exp uses the unrounded fp32 weights.
  * Requires heads == 16, dc == 512, dr in {0, 64}, 1 <= width <= 8192, num_slots <= INT32_MAX,
- * strides multiples of 8 elements, q_nope / q_pe / ckv / kpe 16-B aligned, and a 16-B aligned
+ * strides multiples of 8 elements, q_nope / q_pe / ckv / kpe / out 16-B aligned, and a 16-B aligned
  * device workspace of sel_mla_workspace_bytes(rows, width) bytes (needs no initialisation;
  * calls sharing one must not overlap on the GPU). Queues two kernels (sel_mla_launch_count).
  * status (optional): SEL_ST_TIMEOUT if a bounded wait expired.

@@ -9,20 +9,24 @@
 //   out[r][h] = sum_j softmax(logit)_j * ckv[s_j],   lse[r][h] = log sum_j exp(logit_j)
 // with 16 heads, 512 latent and 0 or 64 rotary dims, bf16 inputs, fp32 outputs.
 //
-// The rows' tiles of 128 entries are laid end to end and cut into one contiguous run per CTA,
+// The rows' tiles of 64 entries are laid end to end and cut into one contiguous run per CTA,
 // so the job spreads evenly over the SMs even for a handful of rows. Per tile:
-//   warps 0-3 (one entry per thread) read the entry's slot and gather its 576 dims from the
-//     cache with 16-byte cp.async into 64-dim boxes in the 128-byte swizzle layout (latent
-//     boxes in pairs, a ring of 5 pairs; the rotary box in a ring of 2). An entry past
-//     kv_len or with a bad slot is zero-filled without touching the cache;
-//   warp 4 (one thread) issues S^T[128 entries x 16 heads] = K_tile . Q^T on the tensor
-//     cores into TMEM (kind::f16, bf16 operands, fp32 accumulation) and, once the softmax
-//     has written P, O^T[512 x 16] += V^T . P^T, the same latent boxes read as an MN-major
+//   warps 0-3 (eight lanes per 128-byte box row, four entries per warp-wide copy) read the
+//     entries' slots and gather their 576 dims from the cache with 16-byte cp.async into
+//     64-dim boxes in the 128-byte swizzle layout: the latent boxes in pairs (a ring of 11
+//     pairs, 2.75 tiles) that stay until the tile's output product, the rotary box in a ring
+//     of 2; meanwhile the next tile's rows are prefetched into L2 by the TMA engine. An
+//     entry past kv_len or with a bad slot is zero-filled without touching the cache;
+//   warp 4 (one thread) issues, for tile k, S^T = K . Q^T on the tensor cores into TMEM
+//     (kind::f16, bf16 operands, fp32 accumulation in four interleaved partial sums; the
+//     product runs 128 rows deep and its upper 64 rows, which read the neighbouring 8 KiB of
+//     shared memory, are ignored), then
+//     tile k-1's O^T[512 x 16] += V^T . P^T, the same latent boxes read as an MN-major
 //     operand (a latent row is both key and value);
-//   warps 5-8 (one entry per thread) read the tile's logits from TMEM, keep the running
-//     maximum per head -- raised only when a logit exceeds it by more than 2^8, which then
-//     rescales O in TMEM --, and write p = 2^(logit - max) rounded to bf16 for the second
-//     product; the sums of p are kept per thread and reduced once per row.
+//   warps 5-8 (one entry per thread of warps 5-6) read the tile's logits from TMEM, keep
+//     the running maximum per head -- raised only when a logit exceeds it by more than 2^8,
+//     which then rescales O in TMEM --, and write p = 2^(logit - max) rounded to bf16 for
+//     the output product; the sums of p are kept per thread and reduced once per row.
 // A row whose tiles all ran in one CTA is normalised and written by that CTA; a row split
 // between CTAs leaves one partial (unnormalised O, maximum, sums) per CTA, and k_mla_merge
 // combines them.
@@ -35,12 +39,12 @@ namespace sel {
 
 namespace {
 
-constexpr int kPairSlots = 5;                  // latent pair buffers (boxes 2k, 2k+1)
+constexpr int kPairSlots = 11;                 // latent pair buffers (boxes 2k, 2k+1 of one tile)
 constexpr int kRopeSlots = 2;
-constexpr uint32_t kBoxBytes16 = 128 * 128;    // 64 dims x 128 entries, bf16
+constexpr uint32_t kBoxBytes16 = 64 * 128;     // 64 dims x 64 entries, bf16
 constexpr uint32_t kPairBytes = 2 * kBoxBytes16;
 constexpr uint32_t kQBox = 16 * 128;           // 16 heads x 64 dims
-constexpr uint32_t kPBuf = 16 * 128 * 2;       // 16 heads x 128 entries
+constexpr uint32_t kPBuf = 16 * 128;           // 16 heads x 64 entries
 constexpr uint32_t kOffRope = kPairSlots * kPairBytes;
 constexpr uint32_t kOffQ = kOffRope + kRopeSlots * kBoxBytes16;
 constexpr uint32_t kOffP = kOffQ + 9 * kQBox;
@@ -49,17 +53,22 @@ constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;
 constexpr int kBPairFull = 0, kBPairEmpty = kBPairFull + kPairSlots, kBRopeFull = kBPairEmpty + kPairSlots,
               kBRopeEmpty = kBRopeFull + kRopeSlots, kBQFull = kBRopeEmpty + kRopeSlots, kBQEmpty = kBQFull + 1,
               kBSFull = kBQEmpty + 1, kBSEmpty = kBSFull + 2, kBPFull = kBSEmpty + 2, kBPEmpty = kBPFull + 2,
-              kBODone = kBPEmpty + 2, kBOEmpty = kBODone + 1, kBDone = kBOEmpty + 2, kNumBars = kBDone + 1;
+              kBOFull = kBPEmpty + 2, kBOEmpty = kBOFull + 2, kBODone = kBOEmpty + 2, kBDone = kBODone + 2,
+              kNumBars = kBDone + 1;
 constexpr uint32_t kOffWords = kOffBar + kNumBars * 8;       // tmem base, abort flag
 constexpr uint32_t kOffRed = kOffWords + 16;                  // 2 x 4 warps x 16 floats
 constexpr uint32_t kSmemUsed = kOffRed + 2 * 4 * 16 * 4;
-constexpr uint32_t kColS = 0, kColO = 32, kTmemCols = 256;   // S: 2 x 16 columns; O: 2 x 64
+// TMEM columns: S = 2 buffers x 4 partial accumulators x 16 heads (the score product's K
+// steps alternate between four accumulators so consecutive MMAs do not depend on each other;
+// the softmax adds the four), then O = 2 buffers x 4 dim-blocks x 16 heads.
+constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
 constexpr float kRaise = 8.0f;                                // log2 of the largest p kept unscaled
 constexpr int kSoftBar = 1;                                   // named barrier of the softmax warps
 
 struct Seg {
     int row, tin_a, tin_b;  // tiles tin_a..tin_b of the row
     int n_act;              // tiles holding an entry below kv_len (a prefix of the segment)
+    int kvl;                // the row's kv_len, clamped to [0, width]
 };
 
 __device__ __forceinline__ Seg segment_of(const MlaArgs& a, int64_t t0, int64_t t1, int row) {
@@ -71,16 +80,49 @@ __device__ __forceinline__ Seg segment_of(const MlaArgs& a, int64_t t0, int64_t 
     s.tin_b = static_cast<int>(hi - 1 - r0);
     int kvl = __ldg(a.kv_len + row);
     kvl = max(0, min(kvl, a.width));
+    s.kvl = kvl;
     const int tiles = (kvl + kMlaTile - 1) / kMlaTile;
     s.n_act = max(0, min(s.tin_b + 1, tiles) - s.tin_a);
     return s;
 }
 
-__device__ __forceinline__ int entry_slot(const MlaArgs& a, int row, int e) {
-    int kvl = __ldg(a.kv_len + row);
-    kvl = min(kvl, a.width);
-    if (e >= kvl) return -1;
-    const int s = __ldg(a.slots + static_cast<int64_t>(row) * a.width + e);
+// Walks the CTA's tiles that hold an entry below kv_len, row by row (rows without any are
+// skipped): the gather and MMA roles step through the same sequence.
+struct ActIter {
+    int row, row_b, tt;
+    Seg sg;
+    bool valid;
+    __device__ __forceinline__ void skip(const MlaArgs& a, int64_t t0, int64_t t1) {
+        while (row <= row_b && sg.n_act == 0) {
+            ++row;
+            if (row <= row_b) sg = segment_of(a, t0, t1, row);
+        }
+        valid = row <= row_b;
+    }
+    __device__ __forceinline__ void start(const MlaArgs& a, int64_t t0, int64_t t1, int ra, int rb) {
+        row = ra;
+        row_b = rb;
+        tt = 0;
+        sg = segment_of(a, t0, t1, row);
+        skip(a, t0, t1);
+    }
+    __device__ __forceinline__ void next(const MlaArgs& a, int64_t t0, int64_t t1) {
+        if (++tt == sg.n_act) {
+            tt = 0;
+            ++row;
+            if (row <= row_b) sg = segment_of(a, t0, t1, row);
+            skip(a, t0, t1);
+        }
+    }
+    __device__ __forceinline__ int entry0() const { return (sg.tin_a + tt) * kMlaTile; }
+};
+
+// The slot of entry e of a row with (clamped) kv_len kvl, or -1 (past kv_len, or a bad slot).
+// One load, predicated on e < kvl: its result is only needed by the caller's next step.
+__device__ __forceinline__ int raw_slot(const MlaArgs& a, int row, int kvl, int e) {
+    return e < kvl ? __ldg(a.slots + static_cast<int64_t>(row) * a.width + e) : -1;
+}
+__device__ __forceinline__ int checked_slot(const MlaArgs& a, int s) {
     return (s >= 0 && s < a.num_slots) ? s : -1;
 }
 
@@ -147,8 +189,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
             mbar_init(&bar[kBPFull + i], 4);
             mbar_init(&bar[kBPEmpty + i], 1);
             mbar_init(&bar[kBOEmpty + i], 4);
+            mbar_init(&bar[kBOFull + i], 1);
         }
         mbar_init(&bar[kBODone], 1);
+        mbar_init(&bar[kBODone + 1], 1);
         mbar_init(&bar[kBDone], 1);
         words[1] = 0;  // abort flag
         mbar_fence_init();
@@ -168,138 +212,204 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
     };
 
     if (warp < 4) {
-        // ------------------------------------------------------------ gather (one entry per thread)
+        // ------------------------------------------------------------ gather
+        // Thread i copies 16-byte chunk (i & 7) of the 128-byte box rows of entries
+        // (i >> 3) + 16 r, r < 4: eight consecutive lanes cover one entry's whole box row, so
+        // each warp-wide copy reads four full 128-byte lines. Per tile k: its four latent
+        // pairs and its rotary box go to shared memory; then tile k+1's rows are brought
+        // into L2 by bulk prefetches (TMA engine), and tile k+2's slot indices are loaded.
         const int i = threadIdx.x;
-        int64_t tile_no = 0;  // active tiles so far in this CTA
+        const int c = i & 7, eg = i >> 3;
+        auto load_raw = [&](const ActIter& t, int (&raw)[4]) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) raw[r] = t.valid ? raw_slot(a, t.row, t.sg.kvl, t.entry0() + eg + 16 * r) : -1;
+        };
+        auto prefetch_rows = [&](const int (&raw)[4]) {
+            if (c != 0) return;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int sl = checked_slot(a, raw[r]);
+                if (sl >= 0) {
+                    bulk_prefetch_l2(a.ckv + static_cast<int64_t>(sl) * a.ckv_stride, kMlaDc * 2);
+                    if (nbox_r) bulk_prefetch_l2(a.kpe + static_cast<int64_t>(sl) * a.kpe_stride, 128);
+                }
+            }
+        };
+        ActIter it;
+        it.start(a, t0, t1, row_a, row_b);
+        ActIter it1 = it;
+        if (it1.valid) it1.next(a, t0, t1);
+        int cur_raw[4], nxt_raw[4], far_raw[4];
+        load_raw(it, cur_raw);
+        load_raw(it1, nxt_raw);
+        int64_t seq = 0, k = 0;
         int q_loads = 0;
         bool ok = true;
-        for (int row = row_a; row <= row_b && ok; ++row) {
-            const Seg sg = segment_of(a, t0, t1, row);
-            if (sg.n_act == 0) continue;
-            // the row's queries: 16 heads x 9 boxes of 64 dims, in the K-major swizzle layout
-            if (!mbar_wait(&bar[kBQEmpty], (q_loads & 1) ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
-            {
-                const int h = i >> 3, c = i & 7;
-                const uint16_t* qn = a.q_nope + static_cast<int64_t>(row) * a.qn_row + h * a.qn_head;
+        while (ok && it.valid) {
+            ActIter it2 = it1;
+            if (it2.valid) it2.next(a, t0, t1);
+            load_raw(it2, far_raw);
+            if (it.tt == 0) {
+                // the row's queries: 16 heads x 9 boxes of 64 dims, K-major swizzle layout
+                if (!mbar_wait(&bar[kBQEmpty], (q_loads & 1) ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
+                const int h = i >> 3;
+                const uint16_t* qn = a.q_nope + static_cast<int64_t>(it.row) * a.qn_row + h * a.qn_head;
                 uint8_t* qd = sm + kOffQ + h * 128 + ((c ^ (h & 7)) << 4);
 #pragma unroll
                 for (int b = 0; b < 8; ++b) cp_async_16(qd + b * kQBox, qn + 64 * b + 8 * c);
                 if (a.dr > 0)
-                    cp_async_16(qd + 8 * kQBox, a.q_pe + static_cast<int64_t>(row) * a.qp_row + h * a.qp_head + 8 * c);
+                    cp_async_16(qd + 8 * kQBox,
+                                a.q_pe + static_cast<int64_t>(it.row) * a.qp_row + h * a.qp_head + 8 * c);
                 cp_async_mbar_arrive(&bar[kBQFull]);
+                ++q_loads;
             }
-            ++q_loads;
-            for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
-                const int e = (sg.tin_a + tt) * kMlaTile + i;
-                const int slot = entry_slot(a, row, e);
-                const uint32_t nb = slot >= 0 ? 16u : 0u;
-                const uint16_t* src = a.ckv + (slot >= 0 ? static_cast<int64_t>(slot) * a.ckv_stride : 0);
-                const uint32_t sw = static_cast<uint32_t>(i & 7);
-                for (int pr = 0; pr < 4; ++pr) {
-                    const int64_t n = tile_no * 4 + pr;
-                    const int ps = static_cast<int>(n % kPairSlots);
-                    if (!mbar_wait(&bar[kBPairEmpty + ps], static_cast<uint32_t>((n / kPairSlots) & 1) ^ 1u, abort_flag,
-                                   a.wait_ns)) { ok = false; break; }
-                    uint8_t* dst = sm + ps * kPairBytes + i * 128;
+            const uint16_t* src[4];
+            uint32_t nb[4];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
+            for (int r = 0; r < 4; ++r) {
+                const int sl = checked_slot(a, cur_raw[r]);
+                src[r] = a.ckv + (sl >= 0 ? static_cast<int64_t>(sl) * a.ckv_stride : 0) + 8 * c;
+                nb[r] = sl >= 0 ? 16u : 0u;
+            }
+            for (int pr = 0; pr < 4; ++pr, ++seq) {
+                const int ps = static_cast<int>(seq % kPairSlots);
+                if (!mbar_wait(&bar[kBPairEmpty + ps], static_cast<uint32_t>((seq / kPairSlots) & 1) ^ 1u, abort_flag,
+                               a.wait_ns)) { ok = false; break; }
+                uint8_t* dst = sm + ps * kPairBytes;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            cp_async_16_zfill(dst + half * kBoxBytes16 + ((c ^ sw) << 4),
-                                              src + (2 * pr + half) * 64 + 8 * c, nb);
-                    cp_async_mbar_arrive(&bar[kBPairFull + ps]);
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int e = eg + 16 * r;
+                        cp_async_16_zfill(dst + half * kBoxBytes16 + e * 128 + ((c ^ (e & 7)) << 4),
+                                          src[r] + (2 * pr + half) * 64, nb[r]);
+                    }
+                cp_async_mbar_arrive(&bar[kBPairFull + ps]);
+            }
+            if (!ok) break;
+            if (nbox_r) {
+                const int rs = static_cast<int>(k % kRopeSlots);
+                if (!mbar_wait(&bar[kBRopeEmpty + rs], static_cast<uint32_t>((k / kRopeSlots) & 1) ^ 1u, abort_flag,
+                               a.wait_ns)) { ok = false; break; }
+                uint8_t* dst = sm + kOffRope + rs * kBoxBytes16;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = eg + 16 * r;
+                    const int sl = checked_slot(a, cur_raw[r]);
+                    const uint16_t* srp = a.kpe + (sl >= 0 ? static_cast<int64_t>(sl) * a.kpe_stride : 0) + 8 * c;
+                    cp_async_16_zfill(dst + e * 128 + ((c ^ (e & 7)) << 4), srp, nb[r]);
                 }
-                if (!ok) break;
-                if (nbox_r) {
-                    const int rs = static_cast<int>(tile_no % kRopeSlots);
-                    if (!mbar_wait(&bar[kBRopeEmpty + rs], static_cast<uint32_t>((tile_no / kRopeSlots) & 1) ^ 1u,
-                                   abort_flag, a.wait_ns)) { ok = false; break; }
-                    const uint16_t* srp = a.kpe + (slot >= 0 ? static_cast<int64_t>(slot) * a.kpe_stride : 0);
-                    uint8_t* dst = sm + kOffRope + rs * kBoxBytes16 + i * 128;
+                cp_async_mbar_arrive(&bar[kBRopeFull + rs]);
+            }
+            prefetch_rows(nxt_raw);
+            it = it1;
+            it1 = it2;
+            ++k;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) cp_async_16_zfill(dst + ((c ^ sw) << 4), srp + 8 * c, nb);
-                    cp_async_mbar_arrive(&bar[kBRopeFull + rs]);
-                }
+            for (int r = 0; r < 4; ++r) {
+                cur_raw[r] = nxt_raw[r];
+                nxt_raw[r] = far_raw[r];
             }
         }
         if (!ok) fail();
         cp_async_wait_all();  // nothing lands in shared memory after the CTA leaves
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
+        // Step k: tile k's scores S^T = K . Q^T (latent pairs, then the rotary box),
+        // committed; then tile k-1's output O^T += V^T . P^T once the softmax has written
+        // P(k-1), which frees tile k-1's pairs. The commit of S(k) covers every product of
+        // tile k-2; O_DONE[t & 1] marks tile t's output products.
         if (lane == 0) {
-            const uint32_t idesc_s = umma_idesc_bf16_f32(kMlaTile, kMlaHeads, 0);
-            const uint32_t idesc_o = umma_idesc_bf16_f32(kMlaTile, kMlaHeads, 1);
+            const uint32_t idesc_s = umma_idesc_bf16_f32(128, kMlaHeads, 0);
+            const uint32_t idesc_o = umma_idesc_bf16_f32(128, kMlaHeads, 1);
             const uint32_t base = smem_u32(sm);
-            int64_t tile_no = 0;
-            int q_loads = 0, o_segs = 0;
+            ActIter it;
+            it.start(a, t0, t1, row_a, row_b);
+            bool have_prev = false, prev_first = false, prev_last = false;
+            int prev_ob = 0, prev_seg = 0, o_segs = 0, q_loads = 0;
+            int64_t k = 0;
             bool ok = true;
-            for (int row = row_a; row <= row_b && ok; ++row) {
-                const Seg sg = segment_of(a, t0, t1, row);
-                if (sg.n_act == 0) continue;
-                if (!mbar_wait(&bar[kBQFull], q_loads & 1, abort_flag, a.wait_ns)) { ok = false; break; }
-                ++q_loads;
-                const int ob = o_segs & 1;
-                if (!mbar_wait(&bar[kBOEmpty + ob], static_cast<uint32_t>((o_segs >> 1) & 1) ^ 1u, abort_flag,
-                               a.wait_ns)) { ok = false; break; }
-                ++o_segs;
-                for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
-                    const int sb = static_cast<int>(tile_no & 1);
-                    const uint32_t use = static_cast<uint32_t>((tile_no >> 1) & 1);
-                    if (!mbar_wait(&bar[kBSEmpty + sb], use ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_s = tmem + kColS + 16u * sb;
-                    for (int pr = 0; pr < 4 && ok; ++pr) {
-                        const int64_t n = tile_no * 4 + pr;
-                        const int ps = static_cast<int>(n % kPairSlots);
-                        if (!mbar_wait(&bar[kBPairFull + ps], static_cast<uint32_t>((n / kPairSlots) & 1), abort_flag,
+            while (ok && (it.valid || have_prev)) {
+                const bool have_cur = it.valid;
+                const bool cur_first = have_cur && it.tt == 0;
+                const bool cur_last = have_cur && it.tt == it.sg.n_act - 1;
+                const int sb = static_cast<int>(k & 1);
+                const int pb = static_cast<int>((k - 1) & 1);
+                if (have_cur) {
+                    if (cur_first) {
+                        if (!mbar_wait(&bar[kBQFull], q_loads & 1, abort_flag, a.wait_ns)) { ok = false; break; }
+                        ++q_loads;
+                    }
+                    if (!mbar_wait(&bar[kBSEmpty + sb], static_cast<uint32_t>((k >> 1) & 1) ^ 1u, abort_flag,
+                                   a.wait_ns)) { ok = false; break; }
+                    const uint32_t d_s = tmem + kColS + 64u * sb;  // + 16 * accumulator
+                    for (int pr = 0; pr < 4; ++pr) {
+                        const int64_t seq = 4 * k + pr;
+                        const int ps = static_cast<int>(seq % kPairSlots);
+                        if (!mbar_wait(&bar[kBPairFull + ps], static_cast<uint32_t>((seq / kPairSlots) & 1), abort_flag,
+                                       a.wait_ns)) { ok = false; break; }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t pair = base + ps * kPairBytes;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_f16(d_s + 16u * kk, umma_desc_sw128(pair + half * kBoxBytes16 + 32u * kk),
+                                         umma_desc_sw128(base + kOffQ + (2 * pr + half) * kQBox + 32u * kk), idesc_s,
+                                         (pr | half) ? 1u : 0u);
+                    }
+                    if (!ok) break;
+                    if (nbox_r) {
+                        const int rs = static_cast<int>(k % kRopeSlots);
+                        if (!mbar_wait(&bar[kBRopeFull + rs], static_cast<uint32_t>((k / kRopeSlots) & 1), abort_flag,
                                        a.wait_ns)) { ok = false; break; }
                         fence_proxy_async_smem();
                         tc_fence_after();
 #pragma unroll
-                        for (int half = 0; half < 2; ++half)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = umma_desc_sw128(base + ps * kPairBytes + half * kBoxBytes16 + 32u * kk);
-                                const uint64_t bd = umma_desc_sw128(base + kOffQ + (2 * pr + half) * kQBox + 32u * kk);
-                                umma_f16(d_s, ad, bd, idesc_s, (pr | half | kk) ? 1u : 0u);
-                            }
-                    }
-                    if (!ok) break;
-                    if (nbox_r) {
-                        const int rs = static_cast<int>(tile_no % kRopeSlots);
-                        if (!mbar_wait(&bar[kBRopeFull + rs], static_cast<uint32_t>((tile_no / kRopeSlots) & 1),
-                                       abort_flag, a.wait_ns)) { ok = false; break; }
-                        fence_proxy_async_smem();
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = umma_desc_sw128(base + kOffRope + rs * kBoxBytes16 + 32u * kk);
-                            const uint64_t bd = umma_desc_sw128(base + kOffQ + 8 * kQBox + 32u * kk);
-                            umma_f16(d_s, ad, bd, idesc_s, 1u);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16(d_s + 16u * kk, umma_desc_sw128(base + kOffRope + rs * kBoxBytes16 + 32u * kk),
+                                     umma_desc_sw128(base + kOffQ + 8 * kQBox + 32u * kk), idesc_s, 1u);
                         umma_commit(&bar[kBRopeEmpty + rs]);
                     }
                     umma_commit(&bar[kBSFull + sb]);
-                    if (tt == sg.n_act - 1) umma_commit(&bar[kBQEmpty]);  // the row's queries are free
-                    // O^T += V^T . P^T once the softmax has written this tile's P
-                    if (!mbar_wait(&bar[kBPFull + sb], use, abort_flag, a.wait_ns)) { ok = false; break; }
+                    if (cur_last) umma_commit(&bar[kBQEmpty]);  // the row's queries are free
+                }
+                if (have_prev) {
+                    // tile k-1's P, and for a row's first tile its O buffer free again
+                    if (!mbar_wait(&bar[kBPFull + pb], static_cast<uint32_t>(((k - 1) >> 1) & 1), abort_flag,
+                                   a.wait_ns)) { ok = false; break; }
+                    if (prev_first && !mbar_wait(&bar[kBOEmpty + prev_ob], static_cast<uint32_t>((prev_seg >> 1) & 1) ^ 1u,
+                                                 abort_flag, a.wait_ns)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t pb = base + kOffP + sb * kPBuf;
-                    for (int mb = 0; mb < 4; ++mb) {
-                        const int64_t n = tile_no * 4 + mb;
-                        const int ps = static_cast<int>(n % kPairSlots);
-                        const uint32_t d_o = tmem + kColO + 64u * ob + 16u * mb;
+                    const uint32_t p_base = base + kOffP + pb * kPBuf;
+                    // pair by pair, each freed as soon as its products finish
+                    for (int pr = 0; pr < 4; ++pr) {
+                        const int ps = static_cast<int>((4 * (k - 1) + pr) % kPairSlots);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t ad = umma_desc_sw128_mn(base + ps * kPairBytes + 2048u * kk, kBoxBytes16);
-                            const uint64_t bd = umma_desc_sw128(pb + (kk >> 2) * 2048u + 32u * (kk & 3));
-                            umma_f16(d_o, ad, bd, idesc_o, (tt == 0 && kk == 0) ? 0u : 1u);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16(tmem + kColO + 64u * prev_ob + 16u * pr,
+                                     umma_desc_sw128_mn(base + ps * kPairBytes + 2048u * kk, kBoxBytes16),
+                                     umma_desc_sw128(p_base + 32u * kk), idesc_o, (prev_first && kk == 0) ? 0u : 1u);
                         umma_commit(&bar[kBPairEmpty + ps]);
                     }
-                    umma_commit(&bar[kBPEmpty + sb]);
-                    umma_commit(&bar[kBODone]);
+                    umma_commit(&bar[kBPEmpty + pb]);
+                    umma_commit(&bar[kBODone + pb]);  // tile k-1's output products, by tile parity
+                    if (prev_last) umma_commit(&bar[kBOFull + prev_ob]);  // the row's O is complete
                 }
+                // tile k becomes the previous one
+                if (have_cur) {
+                    if (cur_first) {
+                        prev_seg = o_segs;
+                        prev_ob = o_segs & 1;
+                        ++o_segs;
+                    }
+                    prev_first = cur_first;
+                    prev_last = cur_last;
+                    it.next(a, t0, t1);
+                    ++k;
+                }
+                have_prev = have_cur;
             }
             if (!ok) fail();
             umma_commit(&bar[kBDone]);  // every MMA issued has finished before teardown
@@ -328,18 +438,30 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
                 const int sb = static_cast<int>(tile_no & 1);
                 const uint32_t use = static_cast<uint32_t>((tile_no >> 1) & 1);
                 const int e = (sg.tin_a + tt) * kMlaTile + j;
-                const bool valid = entry_slot(a, row, e) >= 0;
+                const int sraw = j < kMlaTile ? raw_slot(a, row, sg.kvl, e) : -1;  // lanes 64-127: unused rows
                 int okw = 1;
                 if (lane == 0) okw = mbar_wait(&bar[kBSFull + sb], use, abort_flag, a.wait_ns) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }  // the four warps leave together
                 tc_fence_after();
                 uint32_t raw[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColS + 16u * sb, raw);
-                tmem_ld_wait();
+                {
+                    const uint32_t ts = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColS + 64u * sb;
+                    uint32_t r0[16], r1[16], r2[16], r3[16];
+                    tmem_ld16(ts, r0);
+                    tmem_ld16(ts + 16, r1);
+                    tmem_ld16(ts + 32, r2);
+                    tmem_ld16(ts + 48, r3);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 16; ++h)
+                        raw[h] = __float_as_uint((__uint_as_float(r0[h]) + __uint_as_float(r1[h])) +
+                                                 (__uint_as_float(r2[h]) + __uint_as_float(r3[h])));
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kBSEmpty + sb]);
+                const bool valid = checked_slot(a, sraw) >= 0;
                 float x[16];
                 bool need = tt == 0;
 #pragma unroll
@@ -363,8 +485,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
                         m_run[h] = mn;
                     }
                     if (grow && tt > 0) {
-                        // every earlier product of this row has finished: the MMA thread issued
-                        // them before this tile's scores, whose completion was awaited above
+                        // the previous tile's output products must finish first: completion
+                        // (t-1) >> 1 of O_DONE[(t-1) & 1]. That barrier's previous completion
+                        // (tile t-3) was committed before this tile's scores, and its next one
+                        // (tile t+1) needs a P not yet written, so the parity names one phase.
+                        int okd = 1;
+                        if (lane == 0)
+                            okd = mbar_wait(&bar[kBODone + ((tile_no - 1) & 1)],
+                                            static_cast<uint32_t>(((tile_no - 1) >> 1) & 1), abort_flag, a.wait_ns)
+                                      ? 1 : 0;
+                        okd = __shfl_sync(0xffffffffu, okd, 0);
+                        if (bar_red_or(!okd, kSoftBar, 128)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
                         for (int h = 0; h < 16; ++h) {
                             l_bf[h] *= alpha[h];
@@ -397,11 +529,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
                 if (lane == 0) okw = mbar_wait(&bar[kBPEmpty + sb], use ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }
-                uint8_t* pbase = sm + kOffP + sb * kPBuf + (j >> 6) * 2048 + (j & 7) * 2;
-                const uint32_t chunk = static_cast<uint32_t>((j & 63) >> 3);
+                if (j < kMlaTile) {
+                    uint8_t* pbase = sm + kOffP + sb * kPBuf + (j & 7) * 2;
+                    const uint32_t chunk = static_cast<uint32_t>(j >> 3);
 #pragma unroll
-                for (int h = 0; h < 16; ++h)
-                    *reinterpret_cast<uint16_t*>(pbase + h * 128 + ((chunk ^ (h & 7)) << 4)) = pb[h];
+                    for (int h = 0; h < 16; ++h)
+                        *reinterpret_cast<uint16_t*>(pbase + h * 128 + ((chunk ^ (h & 7)) << 4)) = pb[h];
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -415,7 +549,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
             float* part = reinterpret_cast<float*>(a.part + static_cast<size_t>(pslot) * kMlaPartBytes);
             if (sg.n_act > 0) {
                 int okw = 1;
-                if (lane == 0) okw = mbar_wait(&bar[kBODone], static_cast<uint32_t>((tile_no - 1) & 1), abort_flag,
+                if (lane == 0) okw = mbar_wait(&bar[kBOFull + ob], static_cast<uint32_t>((o_segs >> 1) & 1), abort_flag,
                                                a.wait_ns) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }
@@ -478,11 +612,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
     }
 }
 
-// One CTA per row: a row whose tiles ran in more than one CTA gets the weighted combination
-// of their partials (weights 2^(m_c - max_c m_c)); other rows were written whole. A row has
-// at most 64 tiles (the host checks), so at most 64 partials.
-__global__ void __launch_bounds__(256) k_mla_merge(const MlaArgs a, int grid) {
-    const int row = blockIdx.x;
+// One CTA per (row, head): a row whose tiles ran in more than one CTA gets the weighted
+// combination of their partials (weights 2^(m_c - max_c m_c)); other rows were written whole.
+// A row has at most kMlaMaxTilesPerRow tiles (the host checks), so at most that many
+// partials. Each thread combines four consecutive dims with 16-byte loads, several partials'
+// loads in flight together.
+__global__ void __launch_bounds__(128) k_mla_merge(const MlaArgs a, int grid) {
+    const int row = blockIdx.x, h = blockIdx.y;
     const int64_t tpr = a.tiles_per_row, total = a.total_tiles, G = grid;
     const int64_t first = static_cast<int64_t>(row) * tpr, last = first + tpr - 1;
     // CTA c runs tiles [c * total / G, (c + 1) * total / G): the CTA of tile t is the last c
@@ -490,44 +626,51 @@ __global__ void __launch_bounds__(256) k_mla_merge(const MlaArgs a, int grid) {
     const int c_lo = static_cast<int>(((first + 1) * G - 1) / total);
     const int c_hi = static_cast<int>(((last + 1) * G - 1) / total);
     if (c_lo == c_hi) return;
-    __shared__ float wgt[64][16];
-    __shared__ float inv[16];
-    __shared__ float lse_s[16];
-    if (threadIdx.x < 16) {
-        const int h = threadIdx.x;
-        float mx = -INFINITY;
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
-            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
-            mx = fmaxf(mx, p[kMlaHeads * kMlaDc + h]);
-        }
-        float lb = 0.0f, le = 0.0f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
-            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
-            const float m = p[kMlaHeads * kMlaDc + h];
-            const float w = (m == -INFINITY) ? 0.0f : exp2f(m - mx);
-            if (c - c_lo < 64) wgt[c - c_lo][h] = w;
-            lb += w * p[kMlaHeads * kMlaDc + 16 + h];
-            le += w * p[kMlaHeads * kMlaDc + 32 + h];
-        }
-        inv[h] = lb > 0.0f ? 1.0f / lb : 0.0f;
-        lse_s[h] = le > 0.0f ? (mx + log2f(le)) * 0.69314718055994531f : -INFINITY;
+    const int n = c_hi - c_lo + 1;
+    __shared__ const float* src[kMlaMaxTilesPerRow];
+    __shared__ float mv[kMlaMaxTilesPerRow], lbv[kMlaMaxTilesPerRow], lev[kMlaMaxTilesPerRow], wv[kMlaMaxTilesPerRow];
+    __shared__ float inv_s;
+    const int t = threadIdx.x;
+    if (t < n) {
+        const int c = c_lo + t;
+        const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
+        const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
+        src[t] = p + h * kMlaDc;
+        mv[t] = p[kMlaHeads * kMlaDc + h];
+        lbv[t] = p[kMlaHeads * kMlaDc + 16 + h];
+        lev[t] = p[kMlaHeads * kMlaDc + 32 + h];
     }
     __syncthreads();
-    if (threadIdx.x < 16) a.lse[static_cast<int64_t>(row) * kMlaHeads + threadIdx.x] = lse_s[threadIdx.x];
-    for (int idx = threadIdx.x; idx < kMlaHeads * kMlaDc; idx += blockDim.x) {
-        const int h = idx / kMlaDc;
-        float acc = 0.0f;
-        for (int c = c_lo; c <= c_hi && c - c_lo < 64; ++c) {
-            const float w = wgt[c - c_lo][h];
-            if (w == 0.0f) continue;
-            const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
-            const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
-            acc += w * p[idx];
+    if (t == 0) {
+        float mx = -INFINITY;
+        for (int i = 0; i < n; ++i) mx = fmaxf(mx, mv[i]);
+        float lb = 0.0f, le = 0.0f;
+        for (int i = 0; i < n; ++i) {
+            const float w = mv[i] == -INFINITY ? 0.0f : exp2f(mv[i] - mx);
+            wv[i] = w;
+            lb += w * lbv[i];
+            le += w * lev[i];
         }
-        a.out[static_cast<int64_t>(row) * (kMlaHeads * kMlaDc) + idx] = acc * inv[h];
+        inv_s = lb > 0.0f ? 1.0f / lb : 0.0f;
+        a.lse[static_cast<int64_t>(row) * kMlaHeads + h] =
+            le > 0.0f ? (mx + log2f(le)) * 0.69314718055994531f : -INFINITY;
     }
+    __syncthreads();
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+        const float w = wv[i];
+        if (w != 0.0f) {  // a partial without entries was never written
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src[i]) + t);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+    }
+    const float inv = inv_s;
+    reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(row) * kMlaHeads + h) * kMlaDc)[t] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 size_t mla_smem_bytes() { return kSmemUsed + 1024; }
@@ -548,7 +691,7 @@ cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s) {
-    k_mla_merge<<<a.rows, 256, 0, s>>>(a, grid);
+    k_mla_merge<<<dim3(static_cast<unsigned>(a.rows), kMlaHeads), 128, 0, s>>>(a, grid);
     return cudaGetLastError();
 }
 

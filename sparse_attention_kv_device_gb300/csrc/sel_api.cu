@@ -632,14 +632,14 @@ int sel_mla_decode(const void* q_nope, int64_t qn_row_stride, int64_t qn_head_st
     if (!q_nope || !ckv || !slots || !kv_len || !out || !lse || !ws) return SEL_EINVAL;
     if (dr > 0 && (!q_pe || !kpe)) return SEL_EINVAL;
     if (heads != kMlaHeads || dc != kMlaDc || (dr != 0 && dr != 64)) return SEL_EUNSUPPORTED;
-    if (ceil_div(width, kMlaTile) > 64 || num_slots > INT32_MAX) return SEL_EUNSUPPORTED;
+    if (ceil_div(width, kMlaTile) > kMlaMaxTilesPerRow || num_slots > INT32_MAX) return SEL_EUNSUPPORTED;
     if (qn_head_stride < dc || qn_row_stride < static_cast<int64_t>(heads) * qn_head_stride || ckv_stride < dc)
         return SEL_EINVAL;
     if (dr > 0 && (qp_head_stride < dr || qp_row_stride < static_cast<int64_t>(heads) * qp_head_stride || kpe_stride < dr))
         return SEL_EINVAL;
     auto a8 = [](int64_t v) { return v % 8 == 0; };
     if (!a8(qn_row_stride) || !a8(qn_head_stride) || !a8(ckv_stride) || !aligned16(q_nope) || !aligned16(ckv) ||
-        (reinterpret_cast<uintptr_t>(ws) & 15u) != 0)
+        !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 15u) != 0)
         return SEL_EUNSUPPORTED;
     if (dr > 0 && (!a8(qp_row_stride) || !a8(qp_head_stride) || !a8(kpe_stride) || !aligned16(q_pe) || !aligned16(kpe)))
         return SEL_EUNSUPPORTED;

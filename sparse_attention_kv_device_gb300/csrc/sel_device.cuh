@@ -130,6 +130,11 @@ __device__ __forceinline__ void cp_async_16_zfill(void* smem, const void* gmem, 
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(src_bytes)
                  : "memory");
 }
+// Asks the TMA engine to bring `bytes` (a multiple of 16, from a 16-byte aligned address)
+// into L2; no completion is tracked and nothing is written to shared memory.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
 // Arrives once on `bar` when every cp.async issued so far by this thread has landed (the
 // barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {

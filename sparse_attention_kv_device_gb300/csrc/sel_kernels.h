@@ -151,7 +151,7 @@ struct MaxsimArgs {
     uint64_t wait_ns;        // limit of every bounded wait
 };
 
-// Sparse MLA decode attention over selected slots: one launch over all rows' tiles of 128
+// Sparse MLA decode attention over selected slots: one launch over all rows' tiles of 64
 // entries, each CTA a contiguous run of tiles (a row's tiles may span CTAs), then one merge
 // launch that combines the partial results of rows split between CTAs.
 struct MlaArgs {
@@ -177,7 +177,8 @@ struct MlaArgs {
 };
 constexpr int kMlaHeads = 16;
 constexpr int kMlaDc = 512;
-constexpr int kMlaTile = 128;                   // entries per tile
+constexpr int kMlaTile = 64;                    // entries per tile
+constexpr int kMlaMaxTilesPerRow = 128;         // width <= 8192
 constexpr int kMlaThreads = 288;                // warps 0-3 gather, 4 MMA + TMEM, 5-8 softmax
 constexpr size_t kMlaPartBytes = 33024;         // O [16][512] fp32, m / l / l_exact [16] fp32
 size_t mla_smem_bytes();
