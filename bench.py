@@ -284,15 +284,22 @@ def run_reference(args):
 # ---------------------------------------------------------------- GPU arm
 def remap_modes(sel, torch, dev, stream, flush, peak, iters):
     """The remap kernel's three modes (global slots, prefill workspace, one DCP rank with
-    compaction) on the mixed step's output shape: 4,112 rows x 2,052 tokens (33.8 MB in,
-    33.8 MB out), L2 flushed before each launch, CUDA events on the launching stream."""
+    compaction) on the mixed step's output: 16 decode rows at 128K context (one request
+    each) and 4,096 prefill rows of one request at contexts 60,001..64,096, 2,052 token
+    columns shaped like the selection's output (ascending pools of 4 plus the trailing
+    pool, -1 padding; 33.8 MB in, 33.8 MB out), a 2,048-block table row per request. Also
+    the global mode on uniformly random token columns (the worst case for the block-table
+    gather). L2 flushed before each launch, CUDA events on the launching stream."""
     rows, width, nreq, nb, nkv = 4112, 2052, 17, 2048, 40000
     rng = np.random.default_rng(77)
     bt = torch.from_numpy(rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)).to(dev)
-    req = torch.from_numpy(np.minimum(np.arange(rows) // 242, nreq - 1).astype(np.int32)).to(dev)
-    wsr = torch.from_numpy(np.where(np.arange(rows) < 16, -1, np.arange(rows) % 3).astype(np.int32)).to(dev)
-    starts = torch.tensor([0, 1 << 20, 2 << 20], dtype=torch.int32, device=dev)
-    tok = torch.from_numpy(workloads.random_token_indices(rows, width, nb * 64, seed=5)).to(dev)
+    req_np = np.where(np.arange(rows) < 16, np.arange(rows), 16).astype(np.int32)
+    ctx = np.where(np.arange(rows) < 16, 131072, 60001 + np.arange(rows) - 16)
+    req = torch.from_numpy(req_np).to(dev)
+    wsr = torch.from_numpy(np.where(np.arange(rows) < 16, -1, 0).astype(np.int32)).to(dev)
+    starts = torch.tensor([1 << 20], dtype=torch.int32, device=dev)
+    tok = torch.from_numpy(workloads.selection_token_indices(ctx, width, seed=5)).to(dev)
+    tok_rand = torch.from_numpy(workloads.random_token_indices(rows, width, nb * 64, seed=5)).to(dev)
     slots = torch.empty((rows, width), dtype=torch.int32, device=dev)
     counts = torch.empty(rows, dtype=torch.int32, device=dev)
     calls = {
@@ -302,9 +309,12 @@ def remap_modes(sel, torch, dev, stream, flush, peak, iters):
                                                      valid_counts=counts, stream=stream),
         "dcp_compact": lambda: sel.sel_remap_dcp(req, bt, tok, slots, num_kv_blocks=nkv, dcp_size=4, dcp_rank=1,
                                                  interleave=16, compact=True, valid_counts=counts, stream=stream),
+        "global_random_tokens": lambda: sel.sel_remap_global(req, bt, tok_rand, slots, num_kv_blocks=nkv,
+                                                             valid_counts=counts, stream=stream),
     }
     nbytes = 2 * rows * width * 4 + 3 * rows * 4 + nreq * nb * 4
-    out = {"shape": f"{rows} rows x {width} tokens", "algorithmic_bytes": nbytes}
+    out = {"shape": f"{rows} rows x {width} tokens (selection-shaped; the last mode: random tokens)",
+           "algorithmic_bytes": nbytes}
     with torch.cuda.stream(stream):
         for name, call in calls.items():
             for _ in range(3):

@@ -4,8 +4,9 @@
 // with -1 for t == -1 and for out-of-bounds blocks, columns kept in place, and the
 // per-row count of valid slots computed in the same pass. The page's _remap_tiling
 // notes that counting is the only reason column tiles would need to cooperate; here
-// one warp owns a whole row, so the count is a register reduction plus one store
-// (no atomics, no zero-initialised counter), and every load is an int4 (16 B).
+// one CTA owns a whole row, so the count is a block reduction plus one store (no atomics,
+// no zero-initialised counter); every load is an int4 (16 B), and a thread loads all its
+// vectors of the row before it uses any.
 //
 // The page's two other modes of the same conversion:
 //   prefill workspace (HAS_PREFILL_WORKSPACE): a row of prefill request w maps t to
@@ -14,8 +15,8 @@
 //       rank owns under a round-robin interleave of `interleave` tokens go through its
 //       dense block table, the rest become -1; with compaction the owned slots move to a
 //       contiguous prefix of the row. The page's kernel uses an atomic slot allocator and
-//       leaves the prefix order unspecified; here the warp places them with a prefix sum
-//       over its lanes, in ascending column order, without atomics.
+//       leaves the prefix order unspecified; here the CTA places them with block prefix
+//       sums, in ascending column order, without atomics.
 #include "sel_device.cuh"
 #include "sel_kernels.h"
 
@@ -61,11 +62,14 @@ __device__ __forceinline__ int32_t slot_of(int32_t t, const RemapArgs& a, const 
 
 }  // namespace
 
+constexpr int kCompactStage = 4096;  // columns of a compacted row assembled in shared memory
+
 template <int MODE>
 __global__ void __launch_bounds__(kRemapThreads) k_remap_rows(const RemapArgs a, int rows) {
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (kRemapThreads / 32) + (threadIdx.x >> 5);
-    if (row >= rows) return;  // whole warp
+    __shared__ uint32_t scratch[64];
+    __shared__ __align__(16) int32_t stage[MODE == kRemapDcp ? kCompactStage : 4];
+    const int tid = threadIdx.x;
+    const int row = blockIdx.x;
     const int req = a.req_id[row];
     const bool req_ok = req >= 0 && req < a.num_reqs;
     const int32_t* bt_row = a.block_table + static_cast<int64_t>(req_ok ? req : 0) * a.bt_ld;
@@ -82,57 +86,74 @@ __global__ void __launch_bounds__(kRemapThreads) k_remap_rows(const RemapArgs a,
     int32_t* out = a.slots + static_cast<int64_t>(row) * a.width;
     const int n4 = a.width >> 2;
     const bool compact = MODE == kRemapDcp && a.compact;
-    constexpr int U = 4;  // token vectors each lane has in flight before it uses any
-    uint32_t cnt = 0;
-    for (int base = 0; base < n4; base += 32 * U) {  // warp-uniform trip count
+    // a compacted row is assembled in shared memory and written out with 16-byte stores
+    const bool staged = compact && a.width <= kCompactStage;
+    int32_t* cdst = staged ? stage : out;
+    // every thread has all its vectors of a round in flight before it uses any: one round
+    // covers a row of up to kRemapThreads * U vectors (2,560 tokens)
+    constexpr int U = 5;
+    uint32_t cnt = 0;  // non-compact: this thread's valid slots; compact: the row's so far
+    for (int base = 0; base < n4; base += kRemapThreads * U) {  // block-uniform trip count
+        // vector of (round position u, thread): strided across the threads (coalesced) for
+        // the in-place modes; for compaction each thread owns U consecutive vectors, so one
+        // block scan per round orders the kept slots
+        auto vec = [&](int u) { return compact ? base + tid * U + u : base + u * kRemapThreads + tid; };
         int4 t[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int v = base + u * 32 + lane;
+            const int v = vec(u);
             t[u] = v < n4 ? __ldg(src + v) : make_int4(-1, -1, -1, -1);
+        }
+        if (compact) {
+            int4 sl[U];
+            uint32_t mine = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                sl[u].x = slot_of<MODE>(t[u].x, a, bt_row, req_ok, ws_start, ws_state);
+                sl[u].y = slot_of<MODE>(t[u].y, a, bt_row, req_ok, ws_start, ws_state);
+                sl[u].z = slot_of<MODE>(t[u].z, a, bt_row, req_ok, ws_start, ws_state);
+                sl[u].w = slot_of<MODE>(t[u].w, a, bt_row, req_ok, ws_start, ws_state);
+                mine += (sl[u].x != -1) + (sl[u].y != -1) + (sl[u].z != -1) + (sl[u].w != -1);
+            }
+            uint32_t total;
+            uint32_t pos = cnt + block_excl_scan(mine, scratch, &total);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (sl[u].x != -1) cdst[pos++] = sl[u].x;
+                if (sl[u].y != -1) cdst[pos++] = sl[u].y;
+                if (sl[u].z != -1) cdst[pos++] = sl[u].z;
+                if (sl[u].w != -1) cdst[pos++] = sl[u].w;
+            }
+            cnt += total;
+            continue;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int v = base + u * 32 + lane;
-            int4 s;
-            s.x = slot_of<MODE>(t[u].x, a, bt_row, req_ok, ws_start, ws_state);
-            s.y = slot_of<MODE>(t[u].y, a, bt_row, req_ok, ws_start, ws_state);
-            s.z = slot_of<MODE>(t[u].z, a, bt_row, req_ok, ws_start, ws_state);
-            s.w = slot_of<MODE>(t[u].w, a, bt_row, req_ok, ws_start, ws_state);
-            const uint32_t mine = (s.x != -1) + (s.y != -1) + (s.z != -1) + (s.w != -1);
-            if (!compact) {
-                if (v < n4) reinterpret_cast<int4*>(out)[v] = s;
-                cnt += mine;
-            } else {
-                // this lane's valid slots go to [cnt + slots of the lanes before it, ...): the
-                // row's columns are visited in ascending order, 128 at a time
-                uint32_t incl = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                uint32_t pos = cnt + incl - mine;
-                if (s.x != -1) out[pos++] = s.x;
-                if (s.y != -1) out[pos++] = s.y;
-                if (s.z != -1) out[pos++] = s.z;
-                if (s.w != -1) out[pos++] = s.w;
-                cnt += __shfl_sync(0xffffffffu, incl, 31);
-            }
+            const int v = vec(u);
+            int4 sl;
+            sl.x = slot_of<MODE>(t[u].x, a, bt_row, req_ok, ws_start, ws_state);
+            sl.y = slot_of<MODE>(t[u].y, a, bt_row, req_ok, ws_start, ws_state);
+            sl.z = slot_of<MODE>(t[u].z, a, bt_row, req_ok, ws_start, ws_state);
+            sl.w = slot_of<MODE>(t[u].w, a, bt_row, req_ok, ws_start, ws_state);
+            if (v < n4) reinterpret_cast<int4*>(out)[v] = sl;
+            cnt += (sl.x != -1) + (sl.y != -1) + (sl.z != -1) + (sl.w != -1);
         }
     }
     if (compact) {
-        for (int c = static_cast<int>(cnt) + lane; c < a.width; c += 32) out[c] = -1;
+        for (int c = static_cast<int>(cnt) + tid; c < a.width; c += kRemapThreads) cdst[c] = -1;
+        if (staged) {
+            __syncthreads();
+            for (int v = tid; v < n4; v += kRemapThreads)
+                reinterpret_cast<int4*>(out)[v] = reinterpret_cast<const int4*>(stage)[v];
+        }
     } else {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        cnt = block_sum(cnt, scratch);
     }
-    if (lane == 0 && a.counts) a.counts[row] = static_cast<int32_t>(cnt);
+    if (tid == 0 && a.counts) a.counts[row] = static_cast<int32_t>(cnt);
 }
 
 cudaError_t launch_remap(const RemapArgs& a, int rows, RemapMode mode, cudaStream_t s) {
-    const int rows_per_cta = kRemapThreads / 32;
-    const int grid = (rows + rows_per_cta - 1) / rows_per_cta;
+    const int grid = rows;  // one CTA per row
     switch (mode) {
         case kRemapWorkspace: k_remap_rows<kRemapWorkspace><<<grid, kRemapThreads, 0, s>>>(a, rows); break;
         case kRemapDcp: k_remap_rows<kRemapDcp><<<grid, kRemapThreads, 0, s>>>(a, rows); break;

@@ -72,3 +72,17 @@ def test_generators_are_deterministic():
     assert np.array_equal(a.slots, b.slots) and np.array_equal(a.q_nope, b.q_nope)
     m1, m2 = make_maxsim("maxsim_small"), make_maxsim("maxsim_small")
     assert np.array_equal(m1.offsets, m2.offsets) and np.array_equal(m1.docs, m2.docs)
+
+
+def test_selection_token_indices_shape_and_order():
+    t = workloads.selection_token_indices([131072, 60003, 1000, 2048], 2052, seed=3)
+    assert t.shape == (4, 2052) and t.dtype == np.int32
+    np.testing.assert_array_equal((t >= 0).sum(1), [2048, 2051, 1000, 2048])   # topk + ctx % kpool
+    for r in range(4):
+        v = t[r][t[r] >= 0]
+        assert np.all(np.diff(v) > 0)                                  # ascending, distinct
+        assert np.all(t[r][v.size:] == -1)                             # -1 tail
+    pools = t[0][t[0] >= 0].reshape(-1, 4)
+    assert np.all(pools[:, 0] % 4 == 0) and np.all(np.diff(pools, axis=1) == 1)   # whole pools
+    np.testing.assert_array_equal(t[1][2048:2051], [60000, 60001, 60002])         # trailing pool
+    np.testing.assert_array_equal(t[2][:1000], np.arange(1000))                   # ctx <= topk

@@ -246,3 +246,25 @@ def random_token_indices(rows: int, width: int, max_token: int, *, seed: int,
     t = rng.integers(0, max(1, max_token), size=(rows, width)).astype(np.int32)
     t[rng.random((rows, width)) < minus_one_frac] = -1
     return t
+
+
+def selection_token_indices(contexts, width: int, *, topk: int = 2048, kpool: int = 4, seed: int) -> np.ndarray:
+    """int32 token rows shaped like the selection's output for the given contexts: for
+    ctx <= topk the tokens 0..ctx-1; otherwise topk / kpool distinct complete pools drawn at
+    random, expanded to their kpool tokens, plus the trailing incomplete pool, ascending;
+    then -1 up to width. (Random pools stand in for the scored top pools; the remap only
+    sees the token order and density.)"""
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(contexts, dtype=np.int64)
+    out = np.full((ctx.size, width), -1, dtype=np.int32)
+    for r, c in enumerate(ctx):
+        if c <= topk:
+            toks = np.arange(c, dtype=np.int64)
+        else:
+            pools = c // kpool
+            pick = np.sort(rng.choice(pools, size=topk // kpool, replace=False))
+            toks = (pick[:, None] * kpool + np.arange(kpool)[None, :]).ravel()
+            toks = np.concatenate([toks, np.arange(pools * kpool, c)])
+        n = min(toks.size, width)
+        out[r, :n] = toks[:n]
+    return out
