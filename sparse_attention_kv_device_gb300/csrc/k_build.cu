@@ -115,20 +115,34 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
             const uint32_t s = first + k;
             if (s >= static_cast<uint32_t>(a.max_segs)) break;  // cannot happen with the host bound
             const int row0 = lo + static_cast<int>(k) * a.seg_rows;
-            const int nrows = min(a.seg_rows, hi - row0);
-            int pools = 0;
-            for (int rr = 0; rr < nrows; ++rr) {
-                const int32_t c = ctx[row0 + rr - a.row_begin];
-                if (c > 0 && (a.score_all || c > a.topk)) pools = max(pools, min(c / a.kpool, a.pool_cap));
-            }
-            const int4 d = make_int4(i, row0, nrows, pools);
-            seg[s] = d;
-            if (a.smem_segs) a.seg[s] = d;
+            seg[s] = make_int4(i, row0, min(a.seg_rows, hi - row0), 0);  // pools: below
         }
         carry += total;
         __syncthreads();
     }
     const int nseg = min(static_cast<int>(carry), a.max_segs);
+
+    // 3b. pools to score per segment: the largest over its rows, one warp per segment
+    //     (a segment has at most 64 rows: two per lane)
+    {
+        const int lane = tid & 31, nwarps = blockDim.x >> 5;
+        for (int s = tid >> 5; s < nseg; s += nwarps) {
+            const int4 d = seg[s];
+            int pools = 0;
+            for (int rr = lane; rr < d.z; rr += 32) {
+                const int32_t c = ctx[d.y + rr - a.row_begin];
+                if (c > 0 && (a.score_all || c > a.topk)) pools = max(pools, min(c / a.kpool, a.pool_cap));
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) pools = max(pools, __shfl_xor_sync(0xffffffffu, pools, o));
+            if (lane == 0) {
+                const int4 e = make_int4(d.x, d.y, d.z, pools);
+                seg[s] = e;
+                if (a.smem_segs) a.seg[s] = e;
+            }
+        }
+        __syncthreads();
+    }
 
     // 4. tiles of 128 pools per segment, exclusive prefix.
     uint32_t tcarry = 0;

@@ -12,9 +12,10 @@
 //   * one thread issues tcgen05.mma (M=128, N = rows*4 padded to 16, K=16, fp16 in,
 //     fp32 accumulate) with the keys as A and the segment's queries as B, into one
 //     of two TMEM accumulators;
-//   * four epilogue warps read the accumulator (one TMEM lane = one pool per thread),
-//     add each row's 4 head columns, and store the row scores coalesced (for the fused
-//     selection, the scores' order-preserving 32-bit keys instead);
+//   * eight epilogue warps (two per TMEM lane quarter, alternate groups of 8 rows) read
+//     the accumulator (one TMEM lane = one pool per thread), add each row's 4 head
+//     columns, and store the row scores coalesced (for the fused selection, the scores'
+//     order-preserving 32-bit keys instead);
 //   * every CTA takes a static share of the segments' tiles, and the rest through an
 //     atomic tile counter (segments may change inside a CTA's work, so the queries are
 //     double-buffered too).
@@ -42,7 +43,7 @@ struct ScoreSmem {
     uint64_t* qfull;     // [2]
     uint64_t* qempty;    // [2]
     uint64_t* sfull;     // [kSchedRing] schedule slot published
-    uint64_t* sempty;    // [kSchedRing] schedule slot read by the MMA thread and the 4 epilogue warps
+    uint64_t* sempty;    // [kSchedRing] schedule slot read by the MMA thread and the epilogue warps
     uint64_t* done;      // [1]
     uint32_t* tmem_base;
     int* abort_flag;
@@ -109,13 +110,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.tfull[i], 1);
-            mbar_init(&sm.tempty[i], 4 * 32);
+            mbar_init(&sm.tempty[i], kScoreEpiWarps * 32);
             mbar_init(&sm.qfull[i], 1);
             mbar_init(&sm.qempty[i], 1);
         }
         for (int i = 0; i < kSchedRing; ++i) {
             mbar_init(&sm.sfull[i], 1);
-            mbar_init(&sm.sempty[i], 1 + 4);
+            mbar_init(&sm.sempty[i], 1 + kScoreEpiWarps);
         }
         mbar_init(sm.done, 1);
         *sm.abort_flag = 0;
@@ -351,10 +352,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             mbar_wait(sm.done, 0, nullptr, a.wait_ns);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2-5)
+        // ------------------------------------------------------------ epilogue (warps 2-9)
         // Warp-local only: each warp waits on its own, holds the segment's per-row
-        // pool limits in its lanes, and never waits for the other epilogue warps.
+        // pool limits in its lanes, and never waits for the other epilogue warps. Two warps
+        // share each TMEM lane quarter (a tile's 128 pools); they take alternate groups of 8
+        // rows, so a 64-row segment's epilogue runs on two warps per SM sub-partition.
         const int quarter = warp & 3;             // TMEM lanes this warp may access
+        const int rg0 = (warp - 2) >> 2;          // first row group of this warp (0 or 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         int cur = -1;
@@ -402,7 +406,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc) * a.acc_cols;
             float* out = a.scores + static_cast<int64_t>(sd.y - a.row_begin) * a.scores_ld + j;
-            for (int rg = 0; rg * 8 < sd.z; ++rg) {
+            for (int rg = rg0; rg * 8 < sd.z; rg += 2) {
                 uint32_t v[32];
                 __syncwarp();
                 tmem_ld32(taddr + static_cast<uint32_t>(rg * 32), v);

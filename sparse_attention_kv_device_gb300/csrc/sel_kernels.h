@@ -186,7 +186,8 @@ cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s);
 
 constexpr int kBuildThreads = 1024;
-constexpr int kScoreThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kScoreEpiWarps = 8;    // two per TMEM lane quarter
+constexpr int kScoreThreads = 64 + 32 * kScoreEpiWarps;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 2048;
 constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin listed per row
