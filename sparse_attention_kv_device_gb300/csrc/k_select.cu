@@ -31,9 +31,6 @@ namespace sel {
 
 namespace {
 
-constexpr int T = kSelectThreads;
-static_assert(T * 2 == kTopkBins, "level 1 holds two histogram bins per thread");
-static_assert(T == 1024, "level 3 holds one of its 1024 bins per thread");
 
 struct SelSmem {
     uint32_t* keys;     // [stage_cap] the row's keys
@@ -113,7 +110,13 @@ __device__ __forceinline__ int32_t slot_of(const RowSelectArgs& a, const int32_t
 
 }  // namespace
 
-__global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSelectArgs a) {
+// T threads per row: 1,024 (one CTA per SM; rows up to the SM count) or 512 (two CTAs per SM,
+// for chunks with more rows than SMs, so a chunk's rows run in one wave).
+template <int T>
+__global__ void __launch_bounds__(T, T == 512 ? 2 : 1) k_select_rows(const RowSelectArgs a) {
+    constexpr int B1 = kTopkBins / T;  // level-1 / level-2 bins per thread
+    constexpr int B3 = 1024 / T;       // level-3 bins per thread
+    static_assert(B1 * T == kTopkBins && B3 * T == 1024, "the histograms split evenly over the threads");
     extern __shared__ __align__(16) uint32_t ssm[];
     const int tid = threadIdx.x;
     const int rl = blockIdx.x;
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
             sm.hist1[i] = 0;
             sm.hist[i] = 0;
         }
-        sm.hist3[tid] = 0;
+        for (int i = tid; i < 1024; i += T) sm.hist3[i] = 0;
         for (int w = tid; w < nwords; w += T) {
             sm.gbm[w] = 0;
             sm.ebm[w] = 0;
@@ -196,9 +199,11 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         }
         cp_async_wait_all();  // the block-table entries
         __syncthreads();
-        const uint32_t h1[2] = {sm.hist1[kTopkBins - 1 - 2 * tid], sm.hist1[kTopkBins - 2 - 2 * tid]};
+        uint32_t h1[B1];
+#pragma unroll
+        for (int i = 0; i < B1; ++i) h1[i] = sm.hist1[kTopkBins - 1 - B1 * tid - i];
         uint32_t b1, k1;
-        find_bin_desc<2>(h1, kTopkBins - 1 - 2 * tid, static_cast<uint32_t>(K), sm, b1, k1);
+        find_bin_desc<B1>(h1, kTopkBins - 1 - B1 * tid, static_cast<uint32_t>(K), sm, b1, k1);
 
         // ---- the one full sweep: keys below bin b1 (nearly all of them) cost a compare each.
         //      A thread first records which of its next 32 keys are at or above b1 in a mask,
@@ -243,8 +248,10 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         __syncthreads();
         uint32_t b2, k2;
         {
-            const uint32_t h2[2] = {sm.hist[kTopkBins - 1 - 2 * tid], sm.hist[kTopkBins - 2 - 2 * tid]};
-            find_bin_desc<2>(h2, kTopkBins - 1 - 2 * tid, k1, sm, b2, k2);
+            uint32_t h2[B1];
+#pragma unroll
+            for (int i = 0; i < B1; ++i) h2[i] = sm.hist[kTopkBins - 1 - B1 * tid - i];
+            find_bin_desc<B1>(h2, kTopkBins - 1 - B1 * tid, k1, sm, b2, k2);
         }
 
         // ---- level 3 and the marks at the threshold, on the bin-b1 keys of the bitmap words
@@ -264,8 +271,10 @@ __global__ void __launch_bounds__(kSelectThreads, 1) k_select_rows(const RowSele
         __syncthreads();
         uint32_t b3, need_eq;
         {
-            const uint32_t h3[1] = {sm.hist3[1023 - tid]};
-            find_bin_desc<1>(h3, 1023u - tid, k2, sm, b3, need_eq);
+            uint32_t h3[B3];
+#pragma unroll
+            for (int i = 0; i < B3; ++i) h3[i] = sm.hist3[1023 - B3 * tid - i];
+            find_bin_desc<B3>(h3, 1023u - B3 * tid, k2, sm, b3, need_eq);
         }
         const uint32_t thr = (pre22 << 10) | b3;
         const uint32_t n_eq = sm.hist3[b3];
@@ -355,19 +364,23 @@ size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap) {
                 p4(K) + p4(bt_cap) + 64 + 8);
 }
 
-cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s) {
-    static size_t configured[kMaxDevicesTracked] = {};
+cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s,
+                               int threads) {
+    static size_t configured[2][kMaxDevicesTracked] = {};
+    const int v = threads == 512 ? 1 : 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(k_select_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[v][dev]) {
+        cudaError_t e = v ? cudaFuncSetAttribute(k_select_rows<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem))
+                          : cudaFuncSetAttribute(k_select_rows<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured[dev] = smem;
+        configured[v][dev] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
-    cfg.blockDim = dim3(kSelectThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(v ? 512 : 1024), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -375,7 +388,7 @@ cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_select_rows, a);
+    return v ? cudaLaunchKernelEx(&cfg, k_select_rows<512>, a) : cudaLaunchKernelEx(&cfg, k_select_rows<1024>, a);
 }
 
 }  // namespace sel

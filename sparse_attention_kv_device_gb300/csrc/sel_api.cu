@@ -39,6 +39,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
     int sms = 0;
     int max_smem_optin = 0;
+    int smem_per_sm = 0;
 };
 
 int current_device_info(DeviceInfo* out) {
@@ -48,12 +49,14 @@ int current_device_info(DeviceInfo* out) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SEL_ECUDA;
     std::lock_guard<std::mutex> g(mu);
     if (cache[dev].sms == 0) {
-        int sms = 0, smem = 0;
+        int sms = 0, smem = 0, smem_sm = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
             return SEL_ECUDA;
         cache[dev].sms = sms;
         cache[dev].max_smem_optin = smem;
+        cache[dev].smem_per_sm = smem_sm;
     }
     *out = cache[dev];
     return SEL_OK;
@@ -155,6 +158,11 @@ struct Plan {
     int bm_words = 1;
     int stage_cap = 0;  // keys of a row the select kernel stages in shared memory
     size_t sel_smem = 0;
+    // the select kernel's 512-thread variant, two CTAs per SM (chunks with more rows than
+    // SMs): its own staging capacity and shared-memory size; sel2_ok when it fits
+    bool sel2_ok = false;
+    int stage_cap2 = 0;
+    size_t sel_smem2 = 0;
 };
 
 // log2(v) when v is a power of two, else -1
@@ -245,6 +253,13 @@ int make_plan(const sel_problem* p, Plan* pl) {
     const int64_t fit = ((static_cast<int64_t>(di.max_smem_optin) - static_cast<int64_t>(fixed_sel)) / 4) & ~int64_t(3);
     pl->stage_cap = static_cast<int>(std::min<int64_t>(pl->stage_cap, fit));
     pl->sel_smem = select_smem_bytes(pl->stage_cap, pl->bm_words, K, pl->topk.bt_cap);
+    // two CTAs per SM: each gets half the SM's shared memory less the 1 KiB the hardware
+    // reserves per CTA; worth it only if a useful share of a row still fits
+    const int64_t half = static_cast<int64_t>(di.smem_per_sm) / 2 - 1024;
+    const int64_t fit2 = ((half - static_cast<int64_t>(fixed_sel)) / 4) & ~int64_t(3);
+    pl->stage_cap2 = static_cast<int>(std::min<int64_t>(pl->stage_cap, fit2));
+    pl->sel2_ok = fit2 >= 4096;
+    pl->sel_smem2 = select_smem_bytes(pl->stage_cap2, pl->bm_words, K, pl->topk.bt_cap);
     return SEL_OK;
 }
 
@@ -714,7 +729,8 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         ra.keys_ld = pl.scores_ld;
         ra.row_ctx = w.row_ctx;
         ra.row_req = w.row_req;
-        ra.stage_cap = pl.stage_cap;
+        const bool two = pl.sel2_ok && c1 - c0 > pl.sms;  // more rows than SMs: 512 threads, two per SM
+        ra.stage_cap = two ? pl.stage_cap2 : pl.stage_cap;
         ra.bm_words = pl.bm_words;
         ra.bt_cap = pl.topk.bt_cap;
         ra.row_begin = c0;
@@ -732,7 +748,9 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         ra.num_kv_blocks = p->num_kv_blocks;
         ra.block_size = p->block_size;
         ra.block_stride_rows = p->block_stride_rows;
-        if (launch_select_rows(ra, c1 - c0, pl.sel_smem, true, s) != cudaSuccess) return SEL_ECUDA;
+        if (launch_select_rows(ra, c1 - c0, two ? pl.sel_smem2 : pl.sel_smem, true, s, two ? 512 : 1024) !=
+            cudaSuccess)
+            return SEL_ECUDA;
         if (last) trace_record(3, s);
     }
     return SEL_OK;

@@ -193,7 +193,7 @@ constexpr int kTopkBins = 2048;
 constexpr int kTopkListCap = 4096;   // keys at or above the threshold bin listed per row
 constexpr int kMaxDevicesTracked = 64;
 constexpr int kRemapThreads = 128;
-constexpr int kSelectThreads = 1024;
+constexpr int kSelectThreads = 1024;    // threads of the row select CTA (512 in its two-per-SM variant)
 constexpr int kSelectMaxStage = 32768;  // keys of a row staged in shared memory (128 KiB)
 constexpr int kMaxsimThreads = 256;     // warp 1 schedule, 2 MMA + TMEM, 3 TMA, 4-7 epilogue, 0 idle
 
@@ -209,7 +209,9 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_remap(const RemapArgs& a, int rows, RemapMode mode, cudaStream_t s);
 size_t select_smem_bytes(int stage_cap, int bm_words, int K, int bt_cap);
-cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s);
+// threads: 1024 or 512 (the 512-thread variant is meant to run two CTAs per SM)
+cudaError_t launch_select_rows(const RowSelectArgs& a, int rows, size_t smem, bool pdl, cudaStream_t s,
+                               int threads);
 size_t maxsim_smem_bytes(int stages, int nq_pad, int kslabs);
 // Tensor maps of one MaxSim launch: the packed tensor with boxes of 8, 16, 24, 32, 64, 96 and
 // 128 rows (64 columns each), and the query block.
