@@ -293,8 +293,8 @@ int32_t sel_mla_launch_count(int32_t rows);
  * device, the segmented scorer, the top-512 pools; the "flashinfer_mla_sparse_sm90" page,
  * _kv_lens_host: expansion with the trailing incomplete pool; the "sparse_utils" page,
  * triton_convert_req_index_to_global_index: the remap and the valid counts): segment
- * builder, segmented scorer, top-k with expansion and remap, per chunk of chunk_rows rows,
- * all queued on `stream`.
+ * builder (one launch that plans every chunk of chunk_rows rows), then per chunk the
+ * segmented scorer and the top-k with expansion and remap, all queued on `stream`.
  * slots [num_rows][out_width]: the remapped slots of each row's selected tokens in
  * ascending token order, then -1 (an out-of-bounds block gives -1 in place).
  * valid_counts [num_rows]: number of entries of the row that are not -1.
@@ -351,7 +351,7 @@ int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width
 /*
  * Tracing hook. With n >= 4 events (cudaEvent_t handles, created by the caller with
  * timing enabled), every following sel_select records, on `stream`: events[0] before its
- * first segment-builder launch, events[1] after that builder (before the first scorer
+ * segment-builder launch, events[1] after that builder (before the first scorer
  * launch), events[2] after the last scorer launch and events[3] after the last row-select
  * launch (exact top-k, expansion, remap). Inside stream capture the records
  * become external event nodes. n == 0 switches tracing off. Calls to sel_select are
@@ -371,7 +371,8 @@ int sel_set_trace_events(void *const *events, int32_t n);
  */
 int sel_debug_wait_limit(int32_t fault_tile, int64_t wait_ns);
 
-/* Number of kernel launches sel_select queues for problem p (for launch accounting). */
+/* Number of kernel launches sel_select queues for problem p (for launch accounting):
+ * one builder, then a scorer and a row select per chunk of chunk_rows rows. */
 int32_t sel_select_launch_count(const sel_problem *p);
 
 #ifdef __cplusplus

@@ -2,8 +2,11 @@
 //
 // ReVolta PR #59 ("Change") builds the segment descriptors on the device so the
 // selection call stays CUDA-graph safe; row contexts follow _kv_lens_host on the
-// vLLM flashinfer_mla_sparse_sm90 page (context = position + 1). One CTA reads
-// query_start_loc and positions for a chunk of rows and writes:
+// vLLM flashinfer_mla_sparse_sm90 page (context = position + 1). One launch plans
+// every chunk of a call, one CTA per chunk of chunk_rows rows, each into its own plan
+// block (plan_stride bytes apart), so the chunks' scorers and selects run back to back
+// with no builder between them. A CTA reads query_start_loc and positions for its
+// chunk and writes:
 //   row_req / row_ctx  per row (-1 ctx = no output: padding, out of bound, bad table)
 //   seg[]              {request, first row, rows (<= seg_rows), pools to score}
 //   seg_tile_prefix[]  exclusive prefix of ceil(pools / 128) over segments
@@ -29,10 +32,23 @@ __device__ __forceinline__ int last_le(const int32_t* v, int n, int x) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArgs a) {
+__global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArgs in) {
     extern __shared__ __align__(16) uint8_t bsm[];
     __shared__ uint32_t scratch[40];
     pdl_launch_dependents();  // the scorer may start its prologue now
+    // this CTA's chunk and plan block
+    BuildArgs a = in;
+    {
+        a.row_begin = in.row_begin + static_cast<int>(blockIdx.x) * in.chunk_rows;
+        a.row_end = min(in.row_end, a.row_begin + in.chunk_rows);
+        const int64_t off = static_cast<int64_t>(blockIdx.x) * in.plan_stride;
+        auto at = [off](auto* p) { return reinterpret_cast<decltype(p)>(reinterpret_cast<uint8_t*>(p) + off); };
+        a.row_req = at(in.row_req);
+        a.row_ctx = at(in.row_ctx);
+        a.seg = at(in.seg);
+        a.seg_tile_prefix = at(in.seg_tile_prefix);
+        a.hdr = at(in.hdr);
+    }
     const int tid = threadIdx.x;
     const int nchunk = a.row_end - a.row_begin;
 
@@ -175,7 +191,7 @@ size_t build_smem_bytes(const BuildArgs& a, BuildArgs* layout) {
     const size_t qsl_b = (static_cast<size_t>(a.num_reqs) + 1) * 4;
     layout->smem_qsl = qsl_b <= 64 * 1024;
     if (layout->smem_qsl) off += (qsl_b + 15) & ~size_t(15);
-    const size_t rows_b = static_cast<size_t>(a.row_end - a.row_begin) * 4;
+    const size_t rows_b = static_cast<size_t>(a.chunk_rows < a.row_end - a.row_begin ? a.chunk_rows : a.row_end - a.row_begin) * 4;
     layout->smem_rows = off + rows_b <= budget;
     layout->smem_rows_off = static_cast<int32_t>(off);
     if (layout->smem_rows) off += (rows_b + 15) & ~size_t(15);
@@ -200,7 +216,8 @@ cudaError_t launch_build(const BuildArgs& in, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured[dev] = static_cast<int>(smem);
     }
-    k_build_segments<<<1, kBuildThreads, smem, s>>>(a);
+    const int chunks = (a.row_end - a.row_begin + a.chunk_rows - 1) / a.chunk_rows;
+    k_build_segments<<<chunks, kBuildThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -145,9 +145,10 @@ int plan_topk(int64_t max_context, int block_size, bool remap, int max_smem, Top
 }
 
 struct Plan {
-    int chunk_rows = 1, seg_rows = 1, max_segs = 1;
+    int chunk_rows = 1, seg_rows = 1, max_segs = 1, chunks = 1;
     int64_t max_pools = 0, scores_ld = 4;
-    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0,
+    // one plan block per chunk (offsets inside a block, plan_bytes apart), then the scores
+    size_t off_hdr = 0, off_row_req = 0, off_row_ctx = 0, off_seg = 0, off_prefix = 0, plan_bytes = 0,
            off_scores = 0;
     size_t ws_score = 0, ws_select = 0;
     int npad_max = 16, stages = 2;
@@ -229,6 +230,9 @@ int make_plan(const sel_problem* p, Plan* pl) {
     off = align256(off + sizeof(int4) * pl->max_segs);
     pl->off_prefix = off;
     off = align256(off + sizeof(int32_t) * (pl->max_segs + 1));
+    pl->plan_bytes = off;
+    pl->chunks = static_cast<int>(ceil_div(rows, pl->chunk_rows));
+    off = pl->plan_bytes * static_cast<size_t>(pl->chunks);
     pl->ws_score = off;
     pl->off_scores = off;
     off = align256(off + sizeof(float) * static_cast<size_t>(pl->chunk_rows) * pl->scores_ld);
@@ -281,12 +285,25 @@ void trace_record(int i, cudaStream_t s) {
 
 // ------------------------------------------------------------------ shared launch path
 struct Ws {
-    int32_t* hdr;
+    int32_t* hdr;  // chunk 0's plan block; chunk k's is plan_bytes * k further
     int32_t* row_req;
     int32_t* row_ctx;
     int4* seg;
     int32_t* prefix;
     float* scores;
+    size_t plan_bytes;
+    // the plan block of chunk k
+    Ws chunk(int k) const {
+        const size_t off = plan_bytes * static_cast<size_t>(k);
+        auto at = [off](auto* p) { return reinterpret_cast<decltype(p)>(reinterpret_cast<uint8_t*>(p) + off); };
+        Ws w = *this;
+        w.hdr = at(hdr);
+        w.row_req = at(row_req);
+        w.row_ctx = at(row_ctx);
+        w.seg = at(seg);
+        w.prefix = at(prefix);
+        return w;
+    }
 };
 
 Ws carve_ws(void* ws, const Plan& pl) {
@@ -298,13 +315,13 @@ Ws carve_ws(void* ws, const Plan& pl) {
     w.seg = reinterpret_cast<int4*>(b + pl.off_seg);
     w.prefix = reinterpret_cast<int32_t*>(b + pl.off_prefix);
     w.scores = reinterpret_cast<float*>(b + pl.off_scores);
+    w.plan_bytes = pl.plan_bytes;
     return w;
 }
 
-// Builder + scorer for rows [c0, c1); scores row k of the chunk at scores + k*ld.
-int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int c1, int score_all,
-                         float* scores, int64_t ld, int64_t pool_cap, int32_t* status,
-                         const CUtensorMap& tk, const CUtensorMap& tq, cudaStream_t s) {
+// The builder: every chunk's plan in one launch, one CTA per chunk.
+int launch_plans(const sel_problem* p, const Plan& pl, const Ws& w, int score_all, int64_t pool_cap,
+                 int32_t* status, cudaStream_t s) {
     BuildArgs b{};
     b.qsl = p->query_start_loc;
     b.positions = p->positions;
@@ -314,8 +331,10 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     b.num_key_pages = p->num_key_pages;
     b.num_reqs = p->num_reqs;
     b.num_rows = p->num_rows;
-    b.row_begin = c0;
-    b.row_end = c1;
+    b.row_begin = 0;
+    b.row_end = p->num_rows;
+    b.chunk_rows = pl.chunk_rows;
+    b.plan_stride = static_cast<int64_t>(pl.plan_bytes);
     b.seg_rows = pl.seg_rows;
     b.topk = p->index_topk;
     b.kpool = p->kpool;
@@ -330,8 +349,15 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     b.hdr = w.hdr;
     b.status = status;
     if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
-    if (c0 == 0 && !score_all) trace_record(1, s);
+    if (!score_all) trace_record(1, s);
+    return SEL_OK;
+}
 
+// The scorer for rows [c0, c1), on that chunk's plan block w; scores row k of the chunk at
+// scores + k*ld.
+int launch_chunk_score(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int score_all, float* scores,
+                       int64_t ld, int64_t pool_cap, int32_t* status, const CUtensorMap& tk,
+                       const CUtensorMap& tq, cudaStream_t s) {
     ScoreArgs a{};
     a.seg = w.seg;
     a.hdr = w.hdr;
@@ -346,7 +372,7 @@ int launch_chunk_scoring(const sel_problem* p, const Plan& pl, const Ws& w, int 
     a.topk = p->index_topk;
     a.kpool = p->kpool;
     a.score_all = score_all;
-    a.pool_cap = b.pool_cap;
+    a.pool_cap = static_cast<int32_t>(std::min<int64_t>(pool_cap, INT32_MAX));
     a.scores = scores;
     a.scores_ld = ld;
     a.as_keys = score_all ? 0 : 1;  // the fused selection (score_all = 0) works on ordered keys
@@ -436,10 +462,10 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
     Ws w = carve_ws(ws, pl);
     int32_t* st = status ? status : w.hdr + 8;
-    for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
-        const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
-        rc = launch_chunk_scoring(p, pl, w, c0, c1, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
-                                  scores_ld, st, tk, tq, s);
+    if ((rc = launch_plans(p, pl, w, 1, scores_ld, st, s)) != SEL_OK) return rc;
+    for (int k = 0, c0 = 0; c0 < p->num_rows; ++k, c0 += pl.chunk_rows) {
+        rc = launch_chunk_score(p, pl, w.chunk(k), c0, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
+                                scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
     }
     return SEL_OK;
@@ -715,11 +741,13 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
     Ws w = carve_ws(ws, pl);
     int32_t* st = status ? status : w.hdr + 8;
     std::lock_guard<std::mutex> g(g_trace_mu);
-    for (int c0 = 0; c0 < p->num_rows; c0 += pl.chunk_rows) {
+    trace_record(0, s);
+    if ((rc = launch_plans(p, pl, w, 0, pl.scores_ld, st, s)) != SEL_OK) return rc;
+    for (int k = 0, c0 = 0; c0 < p->num_rows; ++k, c0 += pl.chunk_rows) {
         const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
         const bool last = c1 == p->num_rows;
-        if (c0 == 0) trace_record(0, s);
-        rc = launch_chunk_scoring(p, pl, w, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
+        const Ws wc = w.chunk(k);
+        rc = launch_chunk_score(p, pl, wc, c0, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
         const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);
@@ -727,8 +755,8 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         RowSelectArgs ra{};
         ra.keys = keys;
         ra.keys_ld = pl.scores_ld;
-        ra.row_ctx = w.row_ctx;
-        ra.row_req = w.row_req;
+        ra.row_ctx = wc.row_ctx;
+        ra.row_req = wc.row_req;
         const bool two = pl.sel2_ok && c1 - c0 > pl.sms;  // more rows than SMs: 512 threads, two per SM
         ra.stage_cap = two ? pl.stage_cap2 : pl.stage_cap;
         ra.bm_words = pl.bm_words;
@@ -759,7 +787,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
 int32_t sel_select_launch_count(const sel_problem* p) {
     Plan pl;
     if (make_plan(p, &pl) != SEL_OK || p->num_rows == 0) return 0;
-    return static_cast<int32_t>(3 * ceil_div(p->num_rows, pl.chunk_rows));
+    return static_cast<int32_t>(1 + 2 * ceil_div(p->num_rows, pl.chunk_rows));
 }
 
 size_t sel_host_stage_bytes(const sel_problem* p, int32_t out_width) {

@@ -19,14 +19,16 @@ struct BuildArgs {
     int64_t kpt_ld;
     int32_t max_key_pages, num_key_pages;
     int32_t num_reqs, num_rows;
-    int32_t row_begin, row_end;  // the chunk of rows handled by this launch
+    int32_t row_begin, row_end;  // the rows handled by this launch
+    int32_t chunk_rows;          // rows per CTA (one chunk each)
+    int64_t plan_stride;         // bytes between consecutive chunks' row_req .. hdr arrays
     int32_t seg_rows;
     int32_t topk, kpool, max_context;
     int32_t score_all;  // 1: score every row's complete pools; 0: only rows with ctx > topk
     int32_t pool_cap;   // no row scores more pools than this (the score row length)
     int32_t max_segs;
-    int32_t* row_req;          // [row_end - row_begin]
-    int32_t* row_ctx;          // [row_end - row_begin]; -1 = no output (padding, bad row)
+    int32_t* row_req;          // [chunk_rows] per chunk
+    int32_t* row_ctx;          // [chunk_rows] per chunk; -1 = no output (padding, bad row)
     int4* seg;                 // [max_segs] {req, first row, rows, pools to score}
     int32_t* seg_tile_prefix;  // [max_segs + 1] exclusive prefix of tiles per segment
     int32_t* hdr;              // [0] segments, [1] tiles, [2] scorer's dynamic-tile counter (set to 0)

@@ -444,8 +444,8 @@ def test_trace_events_time_the_kernels():
     assert all(ev[i].elapsed_time(ev[i + 1]) > 0 for i in range(3))
 
 
-def test_launch_count_three_per_chunk():
+def test_launch_count_one_builder_then_two_per_chunk():
     sel = lib()
     for name, chunks in (("decode128k", 1), ("tiny", 1), ("mixed", 17)):
         w = workloads.make_workload(name)
-        assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == 3 * chunks, name
+        assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == 1 + 2 * chunks, name
