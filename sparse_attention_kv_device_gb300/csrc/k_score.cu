@@ -12,10 +12,10 @@
 //   * one thread issues tcgen05.mma (M=128, N = rows*4 padded to 16, K=16, fp16 in,
 //     fp32 accumulate) with the keys as A and the segment's queries as B, into one
 //     of two TMEM accumulators;
-//   * eight epilogue warps (two per TMEM lane quarter, alternate groups of 8 rows) read
-//     the accumulator (one TMEM lane = one pool per thread), add each row's 4 head
-//     columns, and store the row scores coalesced (for the fused selection, the scores'
-//     order-preserving 32-bit keys instead);
+//   * eight epilogue warps (two per TMEM lane quarter, 32 rows each) read the
+//     accumulator (one TMEM lane = one pool per thread; a warp's 32 rows in one load),
+//     add each row's 4 head columns, and store the row scores coalesced (for the fused
+//     selection, the scores' order-preserving 32-bit keys instead);
 //   * every CTA takes a static share of the segments' tiles, and the rest through an
 //     atomic tile counter (segments may change inside a CTA's work, so the queries are
 //     double-buffered too).
@@ -91,10 +91,15 @@ __device__ __forceinline__ int row_pool_limit(const ScoreArgs& a, int row) {
 
 }  // namespace
 
+// At most 96 registers a thread (320 x 96 = 30,720): a CTA then fits on an SM beside the
+// segment builder's CTA (1,024 threads x 32 registers), so every scorer CTA can do its
+// prologue while the builder runs.
+constexpr int kScoreMaxRegs = 96;
+
 // Tile schedule: CTA g first takes the contiguous static share [g*S, g*S + S) with
 // S = floor(3/4 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
 // atomic counter, so CTAs that stream faster take more of the tail.
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __maxnreg__(kScoreMaxRegs)
     k_score_segments(const ScoreArgs a, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_q) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -355,15 +360,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // ------------------------------------------------------------ epilogue (warps 2-9)
         // Warp-local only: each warp waits on its own, holds the segment's per-row
         // pool limits in its lanes, and never waits for the other epilogue warps. Two warps
-        // share each TMEM lane quarter (a tile's 128 pools); they take alternate groups of 8
-        // rows, so a 64-row segment's epilogue runs on two warps per SM sub-partition.
+        // share each TMEM lane quarter (a tile's 128 pools): the first stores the segment's
+        // rows 0-31, the second rows 32-63. Where every row of the segment may score all of
+        // the warp's 32 pools (on an in-range key page) and the warp has all 32 of its rows,
+        // it reads them 16 rows (64 accumulator columns) per TMEM load and stores the rows
+        // back to back with no per-row check; otherwise 8 rows at a time, checked.
         const int quarter = warp & 3;             // TMEM lanes this warp may access
-        const int rg0 = (warp - 2) >> 2;          // first row group of this warp (0 or 1)
+        const int r0 = ((warp - 2) >> 2) * 32;    // first row of the segment this warp stores
         int acc = 0;
         uint32_t acc_phase = 0;
         int cur = -1;
         int4 sd = make_int4(0, 0, 0, 0);
-        int lim_lo = 0, lim_hi = 0;               // pools row `lane` / `lane + 32` may score
+        int lim_mine = 0;                         // pools row r0 + lane may score
+        int seg_min = 0;                          // the smallest such limit over the segment's rows
         int oob = 0;
         for (int n = 0;; ++n) {
             const int slot = n & (kSchedRing - 1);
@@ -384,8 +393,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             if (t < 0) break;
             if (rec.x != cur) {
                 sd = sm.segs[rec.x];
-                lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
-                lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
+                const int lim_lo = lane < sd.z ? row_pool_limit(a, sd.y + lane) : 0;
+                const int lim_hi = lane + 32 < sd.z ? row_pool_limit(a, sd.y + lane + 32) : 0;
+                lim_mine = r0 == 0 ? lim_lo : lim_hi;
+                int m = min(lane < sd.z ? lim_lo : 0x7fffffff, lane + 32 < sd.z ? lim_hi : 0x7fffffff);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, o));
+                seg_min = m;
                 cur = rec.x;
             }
             if (lane == 0) ok = mbar_wait(&sm.tfull[acc], acc_phase, abort_flag, a.wait_ns) ? 1 : 0;
@@ -401,32 +415,45 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             tc_fence_after();
             const int p_in_tile = quarter * 32 + lane;
             const int j = rec.y * kTilePools + p_in_tile;
-            const bool page_ok = (p_in_tile < kPagePools ? rec.z : rec.w) >= 0;
+            const bool page_ok = (quarter < 2 ? rec.z : rec.w) >= 0;  // the same for the whole warp
             if (!page_ok && j < sd.w) oob = 1;
+            const int nr = min(32, sd.z - r0);  // rows of this warp in the segment
+            const bool fast = page_ok && rec.y * kTilePools + quarter * 32 + 32 <= seg_min;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc) * a.acc_cols;
-            float* out = a.scores + static_cast<int64_t>(sd.y - a.row_begin) * a.scores_ld + j;
-            for (int rg = rg0; rg * 8 < sd.z; rg += 2) {
-                uint32_t v[32];
-                __syncwarp();
-                tmem_ld32(taddr + static_cast<uint32_t>(rg * 32), v);
-                tmem_ld_wait();
+                                   static_cast<uint32_t>(acc) * a.acc_cols + static_cast<uint32_t>(r0 * 4);
+            uint32_t* out = reinterpret_cast<uint32_t*>(a.scores) +
+                            static_cast<int64_t>(sd.y + r0 - a.row_begin) * a.scores_ld + j;
+            // a row's score from its 4 head columns, as stored: the order-preserving key for
+            // the fused selection, else the fp32 bits
+            auto word = [&](uint32_t h0, uint32_t h1, uint32_t h2, uint32_t h3) -> uint32_t {
+                const float sc = page_ok ? ((__uint_as_float(h0) + __uint_as_float(h1)) + __uint_as_float(h2)) +
+                                               __uint_as_float(h3)
+                                         : -__int_as_float(0x7f800000);
+                return a.as_keys ? ordered_key(sc) : __float_as_uint(sc);
+            };
+            if (nr == 32 && fast) {
+                for (int h = 0; h < 2; ++h) {  // 16 rows (64 columns) per TMEM load
+                    uint32_t v[64];
+                    __syncwarp();
+                    tmem_ld64_sync(taddr + static_cast<uint32_t>(h * 64), v);
+                    uint32_t* o = out + static_cast<int64_t>(h * 16) * a.scores_ld;
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int r = rg * 8 + rr;
-                    if (r >= sd.z) break;  // uniform over the warp
-                    const int lim = __shfl_sync(0xffffffffu, r < 32 ? lim_lo : lim_hi, r & 31);
-                    const bool okp = j < lim;
-                    const float h0 = __uint_as_float(v[4 * rr + 0]);
-                    const float h1 = __uint_as_float(v[4 * rr + 1]);
-                    const float h2 = __uint_as_float(v[4 * rr + 2]);
-                    const float h3 = __uint_as_float(v[4 * rr + 3]);
-                    const float sc = page_ok ? ((h0 + h1) + h2) + h3 : -__int_as_float(0x7f800000);
-                    if (okp) {
-                        if (a.as_keys)
-                            reinterpret_cast<uint32_t*>(out)[static_cast<int64_t>(r) * a.scores_ld] = ordered_key(sc);
-                        else
-                            out[static_cast<int64_t>(r) * a.scores_ld] = sc;
+                    for (int i = 0; i < 16; ++i)
+                        o[static_cast<int64_t>(i) * a.scores_ld] = word(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+            } else {
+                for (int g = 0; g * 8 < nr; ++g) {
+                    uint32_t v[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + static_cast<uint32_t>(g * 32), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int i = g * 8 + rr;
+                        if (i >= nr) break;  // uniform over the warp
+                        const int lim = __shfl_sync(0xffffffffu, lim_mine, i);
+                        if (fast || j < lim)
+                            out[static_cast<int64_t>(i) * a.scores_ld] = word(v[4 * rr], v[4 * rr + 1], v[4 * rr + 2], v[4 * rr + 3]);
                     }
                 }
             }
