@@ -99,6 +99,10 @@ constexpr int kScoreMaxRegs = 96;
 // Tile schedule: CTA g first takes the contiguous static share [g*S, g*S + S) with
 // S = floor(3/4 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
 // atomic counter, so CTAs that stream faster take more of the tail.
+// kEarly: the plan was complete before the preceding grid started (every chunk after the
+// first), so the CTA runs ahead of that grid's end (a separate instantiation, so the first
+// chunk's producer loop carries none of it).
+template <bool kEarly>
 __global__ void __maxnreg__(kScoreMaxRegs)
     k_score_segments(const ScoreArgs a, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_q) {
@@ -142,8 +146,12 @@ __global__ void __maxnreg__(kScoreMaxRegs)
     const uint32_t tmem = *sm.tmem_base;
     volatile int* abort_flag = sm.abort_flag;
 
-    pdl_wait();               // the builder's outputs are visible from here on
-    pdl_launch_dependents();  // the top-k grid may be scheduled as CTAs retire
+    // With the plan already complete (every chunk after the first), the CTA fetches its
+    // tiles and runs its first products while the preceding grid (the previous chunk's
+    // row select, which reads the score buffer) finishes; only the epilogue's stores wait
+    // for it. Otherwise the builder's outputs are needed first.
+    if (!kEarly) pdl_wait();  // the builder's outputs are visible from here on
+    pdl_launch_dependents();        // the row-select grid may be scheduled as CTAs retire
 
     if (warp == 0) {
         // ------------------------------------------------------------ scheduler + TMA producer
@@ -175,8 +183,20 @@ __global__ void __maxnreg__(kScoreMaxRegs)
         if (lane == 0) {
             int s_next = static_cast<int>(blockIdx.x) * share;
             const int s_end = s_next + share;
-            auto grab = [&]() -> int {
+            // A CTA that started early (beside the preceding grid) takes no shared tile before
+            // its epilogue may store, or it would hold the tile while its stores wait: until
+            // then a lookahead draw is deferred (kDeferred) and repeated when the tile is due.
+            constexpr int kDeferred = -3;
+            bool dyn_ok = !kEarly;
+            auto grab = [&](bool may_wait) -> int {
                 if (s_next < s_end) return s_next++;
+                if constexpr (kEarly) {
+                    if (!dyn_ok) {
+                        if (!may_wait) return kDeferred;
+                        pdl_wait();
+                        dyn_ok = true;
+                    }
+                }
                 const int t = dyn0 + atomicAdd(a.hdr + 2, 1);
                 return t < total ? t : -1;
             };
@@ -221,8 +241,8 @@ __global__ void __maxnreg__(kScoreMaxRegs)
                 return make_int4(r.seg, r.lt, pg0, pg1);
             };
             // two tiles ahead: their ids and page-table entries are in flight while the current one is issued
-            Pending t_a = take(grab());
-            Pending t_b = take(t_a.t >= 0 ? grab() : -1);
+            Pending t_a = take(grab(false));
+            Pending t_b = take(t_a.t >= 0 ? grab(false) : t_a.t);
 
             const uint64_t pol_k = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
@@ -234,10 +254,16 @@ __global__ void __maxnreg__(kScoreMaxRegs)
             uint32_t loaded = 0, last_parity = 0;  // stages holding a load, parity of their last load
             bool ok = true;
             for (int n = 0; ok; ++n) {
+                if constexpr (kEarly) {
+                    if (t_a.t == kDeferred) {  // the shared tiles are open once the preceding grid is done
+                        t_a = take(grab(true));
+                        t_b = take(t_a.t >= 0 ? grab(true) : -1);
+                    }
+                }
                 const int t = t_a.t;
                 const int4 rec = t >= 0 ? record(t_a) : make_int4(0, 0, 0, 0);
                 t_a = t_b;
-                t_b = take(t_a.t >= 0 ? grab() : -1);
+                t_b = take(t_a.t >= 0 ? grab(false) : t_a.t);
                 // publish the tile (or the end) to the MMA thread and the epilogue warps
                 const int slot = n & (kSchedRing - 1);
                 if (!mbar_wait(&sm.sempty[slot], ((n / kSchedRing) & 1) ^ 1u, abort_flag, a.wait_ns)) { ok = false; break; }
@@ -365,6 +391,7 @@ __global__ void __maxnreg__(kScoreMaxRegs)
         // the warp's 32 pools (on an in-range key page) and the warp has all 32 of its rows,
         // it reads them 16 rows (64 accumulator columns) per TMEM load and stores the rows
         // back to back with no per-row check; otherwise 8 rows at a time, checked.
+        if (kEarly) pdl_wait();                   // the preceding grid no longer reads the scores
         const int quarter = warp & 3;             // TMEM lanes this warp may access
         const int r0 = ((warp - 2) >> 2) * 32;    // first row of the segment this warp stores
         int acc = 0;
@@ -483,14 +510,17 @@ size_t score_smem_bytes(int stages, int npad_max, int max_segs) {
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
                          size_t smem, bool pdl, cudaStream_t s) {
-    static size_t configured[kMaxDevicesTracked] = {};
+    static size_t configured[2][kMaxDevicesTracked] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(k_score_segments, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    const int v = a.plan_ready ? 1 : 0;
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[v][dev]) {
+        cudaError_t e = v ? cudaFuncSetAttribute(k_score_segments<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem))
+                          : cudaFuncSetAttribute(k_score_segments<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured[dev] = smem;
+        configured[v][dev] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -502,7 +532,8 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_score_segments, a, tmap_k, tmap_q);
+    return v ? cudaLaunchKernelEx(&cfg, k_score_segments<true>, a, tmap_k, tmap_q)
+             : cudaLaunchKernelEx(&cfg, k_score_segments<false>, a, tmap_k, tmap_q);
 }
 
 }  // namespace sel

@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(T, T == 512 ? 2 : 1) k_select_rows(const RowSe
     const int r = a.row_begin + rl;
     const int K = a.topk / a.kpool;
     SelSmem sm = carve_sel(ssm, a.stage_cap, a.bm_words, K, a.bt_cap);
+    // the next chunk's scorer may launch once every CTA of this grid is resident: it fetches
+    // its tiles meanwhile and stores no score before this grid has finished
+    if (a.next_chunk) pdl_launch_dependents();
 
     // ---- before the wait: only inputs and data of grids that completed before this one
     //      could start (row descriptors from the segment builder, keys from the scorer)

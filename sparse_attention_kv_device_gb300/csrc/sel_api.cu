@@ -376,6 +376,10 @@ int launch_chunk_score(const sel_problem* p, const Plan& pl, const Ws& w, int c0
     a.scores = scores;
     a.scores_ld = ld;
     a.as_keys = score_all ? 0 : 1;  // the fused selection (score_all = 0) works on ordered keys
+    // chunk 0 follows the builder; every later chunk follows a grid that started only after
+    // the builder had finished (each grid of the chain lets its dependents launch only after
+    // its own dependency wait, and chunk 0's scorer waits for the builder)
+    a.plan_ready = c0 > 0 ? 1 : 0;
     a.npad_max = pl.npad_max;
     a.stages = pl.stages;
     a.tmem_cols = pl.tmem_cols;
@@ -776,6 +780,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         ra.num_kv_blocks = p->num_kv_blocks;
         ra.block_size = p->block_size;
         ra.block_stride_rows = p->block_stride_rows;
+        ra.next_chunk = last ? 0 : 1;
         if (launch_select_rows(ra, c1 - c0, two ? pl.sel_smem2 : pl.sel_smem, true, s, two ? 512 : 1024) !=
             cudaSuccess)
             return SEL_ECUDA;

@@ -53,6 +53,9 @@ struct ScoreArgs {
     float* scores;           // chunk-local rows
     int64_t scores_ld;
     int32_t as_keys;         // 1: store ordered_key(score) (uint32 bits) instead of the fp32 score
+    int32_t plan_ready;      // 1: the builder had finished before the preceding grid started, so
+                             //    only the score stores wait for that grid (it may still read the
+                             //    score buffer); 0: everything waits (the builder precedes it)
     int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
     int32_t stages;
     uint32_t tmem_cols;      // TMEM columns allocated (power of two)
@@ -82,6 +85,7 @@ struct RowSelectArgs {
     int64_t bt_ld;
     int32_t max_blocks, num_kv_blocks, block_size;
     int64_t block_stride_rows;
+    int32_t next_chunk;        // 1: another chunk's scorer follows (this grid lets it launch early)
 };
 
 // Top-k pools + expansion (+ remap), one CTA per row.
