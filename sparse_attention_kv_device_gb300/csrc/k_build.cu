@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArg
     // every input load of the kernel is issued here, before the first barrier
     if (a.smem_qsl)
         for (int i = tid; i <= a.num_reqs; i += blockDim.x) qsl[i] = a.qsl[i];
-    int32_t pos_reg[4];  // positions of rows tid, tid + 1024, ... (chunks of up to 4096 rows)
+    int32_t pos_reg[4];  // positions of rows tid, tid + kBuildThreads, ... (the first 4 x kBuildThreads rows)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int k = tid + j * kBuildThreads;
@@ -208,8 +208,17 @@ cudaError_t launch_build(const BuildArgs& in, cudaStream_t s) {
     BuildArgs a = in;
     const size_t smem = build_smem_bytes(in, &a);
     static int configured[kMaxDevicesTracked] = {};
+    static bool carved[kMaxDevicesTracked] = {};
     int dev = 0;
     cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevicesTracked && !carved[dev]) {
+        // the SM's largest shared-memory configuration, the one the scorer runs in: with a
+        // smaller one the SM holding the builder could take no scorer CTA until it is done
+        cudaError_t e = cudaFuncSetAttribute(k_build_segments, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+        if (e != cudaSuccess) return e;
+        carved[dev] = true;
+    }
     if (dev >= 0 && dev < kMaxDevicesTracked && static_cast<int>(smem) > configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(k_build_segments, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));

@@ -48,6 +48,7 @@ struct ScoreSmem {
     uint32_t* tmem_base;
     int* abort_flag;
     int* oob_flag;
+    int* plan_nseg;      // segments of a plan the CTA computed itself
 };
 
 __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_max, int max_segs) {
@@ -80,6 +81,7 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
     s.tmem_base = w;
     s.abort_flag = reinterpret_cast<int*>(w + 1);
     s.oob_flag = reinterpret_cast<int*>(w + 2);
+    s.plan_nseg = reinterpret_cast<int*>(w + 3);
     return s;
 }
 
@@ -87,6 +89,87 @@ __device__ __forceinline__ ScoreSmem carve(uint8_t* raw, int stages, int npad_ma
 __device__ __forceinline__ int row_pool_limit(const ScoreArgs& a, int row) {
     const int32_t c = __ldcg(a.row_ctx + row - a.row_begin);
     return (c > 0 && (a.score_all || c > a.topk)) ? min(c / a.kpool, a.pool_cap) : 0;
+}
+
+// The chunk's plan computed by the whole CTA from query_start_loc and positions with the
+// segment builder's rule (ReVolta PR #59, "Change"; contexts as in _kv_lens_host of the
+// flashinfer_mla_sparse_sm90 page): the chunk's rows of each request, cut every seg_rows rows,
+// each segment scoring the largest complete-pool count of its rows, then the exclusive prefix
+// of its 128-pool tiles. `scratch` holds num_reqs + 1 + rows + 33 words of shared memory that
+// nothing else uses before the first key copy. An invalid query_start_loc gives no segments
+// (the builder reports it). Ends with a block barrier.
+__device__ void plan_self(const ScoreArgs& a, const ScoreSmem& sm, int32_t* scratch) {
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int nrows = a.row_end - a.row_begin;
+    int32_t* qs = scratch;                                       // [num_reqs + 1]
+    int32_t* cx = scratch + a.num_reqs + 1;                      // [nrows] contexts, -1 = out of bound
+    uint32_t* red = reinterpret_cast<uint32_t*>(cx + nrows);     // [33] scan scratch
+    for (int i = tid; i <= a.num_reqs; i += T) qs[i] = __ldg(a.qsl + i);
+    for (int k = tid; k < nrows; k += T) {
+        const int64_t c64 = static_cast<int64_t>(__ldg(a.positions + a.row_begin + k)) + 1;
+        cx[k] = c64 > a.max_context ? -1 : static_cast<int32_t>(c64 > 0 ? c64 : 0);
+    }
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < a.num_reqs; i += T) bad |= qs[i] > qs[i + 1];
+    if (tid == 0) bad |= (qs[0] < 0) | (qs[a.num_reqs] > a.num_rows);
+    bad = __syncthreads_or(bad);
+    // segments: request i's rows inside the chunk, cut every seg_rows rows
+    uint32_t carry = 0;
+    for (int base = 0; !bad && base < a.num_reqs; base += T) {
+        const int i = base + tid;
+        int lo = 0, hi = 0;
+        uint32_t ns = 0;
+        if (i < a.num_reqs) {
+            lo = max(qs[i], a.row_begin);
+            hi = min(qs[i + 1], a.row_end);
+            if (hi > lo) ns = (hi - lo + a.seg_rows - 1) / a.seg_rows;
+        }
+        uint32_t total;
+        const uint32_t first = carry + block_excl_scan(ns, red, &total);
+        for (uint32_t k = 0; k < ns; ++k) {
+            const uint32_t sg = first + k;
+            if (sg >= static_cast<uint32_t>(a.max_segs)) break;  // cannot happen with the host bound
+            const int row0 = lo + static_cast<int>(k) * a.seg_rows;
+            sm.segs[sg] = make_int4(i, row0, min(a.seg_rows, hi - row0), 0);
+        }
+        carry += total;
+        __syncthreads();
+    }
+    const int nseg = min(static_cast<int>(carry), a.max_segs);
+    // pools to score per segment: the largest over its rows, one warp per segment
+    {
+        const int lane = tid & 31, nwarps = T >> 5;
+        for (int sg = tid >> 5; sg < nseg; sg += nwarps) {
+            const int4 d = sm.segs[sg];
+            int pools = 0;
+            for (int rr = lane; rr < d.z; rr += 32) {
+                const int32_t c = cx[d.y + rr - a.row_begin];
+                if (c > 0 && (a.score_all || c > a.topk)) pools = max(pools, min(c / a.kpool, a.pool_cap));
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) pools = max(pools, __shfl_xor_sync(0xffffffffu, pools, o));
+            if (lane == 0) sm.segs[sg] = make_int4(d.x, d.y, d.z, pools);
+        }
+        __syncthreads();
+    }
+    // tiles of 128 pools per segment, exclusive prefix
+    uint32_t tcarry = 0;
+    for (int base = 0; base < nseg; base += T) {
+        const int sg = base + tid;
+        const uint32_t t = sg < nseg ? static_cast<uint32_t>((sm.segs[sg].w + kTilePools - 1) / kTilePools) : 0u;
+        uint32_t total;
+        const uint32_t ex = tcarry + block_excl_scan(t, red, &total);
+        if (sg < nseg) sm.prefix[sg] = static_cast<int>(ex);
+        tcarry += total;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        sm.prefix[nseg] = static_cast<int>(tcarry);
+        *sm.plan_nseg = nseg;
+    }
+    fence_proxy_async_smem();  // the scratch (key stage 0) is next written by the tensor copies
+    __syncthreads();
 }
 
 }  // namespace
@@ -99,10 +182,10 @@ constexpr int kScoreMaxRegs = 96;
 // Tile schedule: CTA g first takes the contiguous static share [g*S, g*S + S) with
 // S = floor(3/4 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
 // atomic counter, so CTAs that stream faster take more of the tail.
-// kEarly: the plan was complete before the preceding grid started (every chunk after the
-// first), so the CTA runs ahead of that grid's end (a separate instantiation, so the first
-// chunk's producer loop carries none of it).
-template <bool kEarly>
+// kMode: how the CTA gets its plan (kPlanAfterBuilder, kPlanReady, kPlanSelf). In the last two
+// it runs ahead of the preceding grid's end; each mode is its own instantiation, so the plain
+// mode's producer loop carries none of that.
+template <int kMode>
 __global__ void __maxnreg__(kScoreMaxRegs)
     k_score_segments(const ScoreArgs a, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_q) {
@@ -110,6 +193,7 @@ __global__ void __maxnreg__(kScoreMaxRegs)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ScoreSmem sm = carve(smem_raw, a.stages, a.npad_max, a.max_segs);
     const uint32_t qhalf_bytes = static_cast<uint32_t>(a.npad_max) * 128u;
+    constexpr bool kEarly = kMode != kPlanAfterBuilder;
 
     // ---- prologue (overlaps the segment builder when launched as a dependent grid)
     if (threadIdx.x == 0) {
@@ -150,19 +234,27 @@ __global__ void __maxnreg__(kScoreMaxRegs)
     // tiles and runs its first products while the preceding grid (the previous chunk's
     // row select, which reads the score buffer) finishes; only the epilogue's stores wait
     // for it. Otherwise the builder's outputs are needed first.
-    if (!kEarly) pdl_wait();  // the builder's outputs are visible from here on
-    pdl_launch_dependents();        // the row-select grid may be scheduled as CTAs retire
+    if constexpr (kMode == kPlanSelf) plan_self(a, sm, reinterpret_cast<int32_t*>(sm.a));
+    if constexpr (kMode == kPlanAfterBuilder) pdl_wait();  // the builder's outputs are visible from here on
+    // the row-select grid may be scheduled as CTAs retire (with a plan of its own, the CTA lets
+    // it launch only once the builder, whose row descriptors it reads, has finished: below)
+    if constexpr (kMode != kPlanSelf) pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ scheduler + TMA producer
         // the builder's segments and tile prefix, staged once by the whole warp: every slot
         // up to max_segs is loaded together with the header (entries past the builder's
         // segment count are never used), so the loads overlap
-        const int nseg_raw = __ldcg(a.hdr + 0);
-        for (int i = lane; i < a.max_segs; i += 32) sm.segs[i] = __ldcg(a.seg + i);
-        for (int i = lane; i <= a.max_segs; i += 32) sm.prefix[i] = __ldcg(a.seg_tile_prefix + i);
-        const int nseg = min(nseg_raw, a.max_segs);
-        __syncwarp();
+        int nseg;
+        if constexpr (kMode == kPlanSelf) {
+            nseg = *sm.plan_nseg;
+        } else {
+            const int nseg_raw = __ldcg(a.hdr + 0);
+            for (int i = lane; i < a.max_segs; i += 32) sm.segs[i] = __ldcg(a.seg + i);
+            for (int i = lane; i <= a.max_segs; i += 32) sm.prefix[i] = __ldcg(a.seg_tile_prefix + i);
+            nseg = min(nseg_raw, a.max_segs);
+            __syncwarp();
+        }
         const int total = sm.prefix[nseg];
         const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
         const int dyn0 = share * static_cast<int>(gridDim.x);
@@ -392,6 +484,7 @@ __global__ void __maxnreg__(kScoreMaxRegs)
         // it reads them 16 rows (64 accumulator columns) per TMEM load and stores the rows
         // back to back with no per-row check; otherwise 8 rows at a time, checked.
         if (kEarly) pdl_wait();                   // the preceding grid no longer reads the scores
+        if constexpr (kMode == kPlanSelf) pdl_launch_dependents();  // the builder has finished
         const int quarter = warp & 3;             // TMEM lanes this warp may access
         const int r0 = ((warp - 2) >> 2) * 32;    // first row of the segment this warp stores
         int acc = 0;
@@ -510,17 +603,17 @@ size_t score_smem_bytes(int stages, int npad_max, int max_segs) {
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
                          size_t smem, bool pdl, cudaStream_t s) {
-    static size_t configured[2][kMaxDevicesTracked] = {};
+    static size_t configured[3][kMaxDevicesTracked] = {};
+    const int m = a.plan_mode;
+    if (m < kPlanAfterBuilder || m > kPlanSelf) return cudaErrorInvalidValue;
+    auto kernel = m == kPlanSelf ? k_score_segments<kPlanSelf>
+                                 : (m == kPlanReady ? k_score_segments<kPlanReady> : k_score_segments<kPlanAfterBuilder>);
     int dev = 0;
     cudaGetDevice(&dev);
-    const int v = a.plan_ready ? 1 : 0;
-    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[v][dev]) {
-        cudaError_t e = v ? cudaFuncSetAttribute(k_score_segments<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem))
-                          : cudaFuncSetAttribute(k_score_segments<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
+    if (dev >= 0 && dev < kMaxDevicesTracked && smem > configured[m][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured[v][dev] = smem;
+        configured[m][dev] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -532,8 +625,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return v ? cudaLaunchKernelEx(&cfg, k_score_segments<true>, a, tmap_k, tmap_q)
-             : cudaLaunchKernelEx(&cfg, k_score_segments<false>, a, tmap_k, tmap_q);
+    return cudaLaunchKernelEx(&cfg, kernel, a, tmap_k, tmap_q);
 }
 
 }  // namespace sel

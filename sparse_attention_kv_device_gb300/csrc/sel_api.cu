@@ -355,7 +355,7 @@ int launch_plans(const sel_problem* p, const Plan& pl, const Ws& w, int score_al
 
 // The scorer for rows [c0, c1), on that chunk's plan block w; scores row k of the chunk at
 // scores + k*ld.
-int launch_chunk_score(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int score_all, float* scores,
+int launch_chunk_score(const sel_problem* p, const Plan& pl, const Ws& w, int c0, int c1, int score_all, float* scores,
                        int64_t ld, int64_t pool_cap, int32_t* status, const CUtensorMap& tk,
                        const CUtensorMap& tq, cudaStream_t s) {
     ScoreArgs a{};
@@ -376,10 +376,23 @@ int launch_chunk_score(const sel_problem* p, const Plan& pl, const Ws& w, int c0
     a.scores = scores;
     a.scores_ld = ld;
     a.as_keys = score_all ? 0 : 1;  // the fused selection (score_all = 0) works on ordered keys
-    // chunk 0 follows the builder; every later chunk follows a grid that started only after
-    // the builder had finished (each grid of the chain lets its dependents launch only after
-    // its own dependency wait, and chunk 0's scorer waits for the builder)
-    a.plan_ready = c0 > 0 ? 1 : 0;
+    // Chunk 0 follows the builder: small problems plan the chunk in the scorer itself, larger
+    // ones wait for the builder's plan. Every later chunk follows a grid that started only
+    // after the builder had finished (no grid of the chain lets its dependents launch before
+    // the builder is done), so its plan is ready.
+    if (c0 > 0)
+        a.plan_mode = kPlanReady;
+    else if (p->num_reqs <= kSelfPlanMaxReqs && c1 - c0 <= kSelfPlanMaxRows)
+        a.plan_mode = kPlanSelf;
+    else
+        a.plan_mode = kPlanAfterBuilder;
+    a.qsl = p->query_start_loc;
+    a.positions = p->positions;
+    a.num_reqs = p->num_reqs;
+    a.num_rows = p->num_rows;
+    a.row_end = c1;
+    a.seg_rows = pl.seg_rows;
+    a.max_context = p->max_context;
     a.npad_max = pl.npad_max;
     a.stages = pl.stages;
     a.tmem_cols = pl.tmem_cols;
@@ -468,7 +481,8 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     int32_t* st = status ? status : w.hdr + 8;
     if ((rc = launch_plans(p, pl, w, 1, scores_ld, st, s)) != SEL_OK) return rc;
     for (int k = 0, c0 = 0; c0 < p->num_rows; ++k, c0 += pl.chunk_rows) {
-        rc = launch_chunk_score(p, pl, w.chunk(k), c0, 1, scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
+        rc = launch_chunk_score(p, pl, w.chunk(k), c0, std::min(p->num_rows, c0 + pl.chunk_rows), 1,
+                                scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
                                 scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
     }
@@ -751,7 +765,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
         const bool last = c1 == p->num_rows;
         const Ws wc = w.chunk(k);
-        rc = launch_chunk_score(p, pl, wc, c0, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
+        rc = launch_chunk_score(p, pl, wc, c0, c1, 0, w.scores, pl.scores_ld, pl.scores_ld, st, tk, tq, s);
         if (rc != SEL_OK) return rc;
         if (last) trace_record(2, s);
         const uint32_t* keys = reinterpret_cast<const uint32_t*>(w.scores);

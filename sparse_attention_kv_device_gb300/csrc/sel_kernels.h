@@ -40,6 +40,19 @@ struct BuildArgs {
 
 // Segmented scorer (TMA + tcgen05): CTAs take static shares of the tiles, then single
 // tiles from an atomic counter; each CTA resolves a tile's segment and key pages itself.
+// How a scorer launch gets its chunk's plan (segments and tile prefix):
+//   kPlanAfterBuilder  it reads the builder's plan after waiting for the builder;
+//   kPlanReady         the builder had finished before the preceding grid (the previous chunk's
+//                      row select, which reads the score buffer) started: the CTA reads the plan
+//                      and fetches its tiles at once, and only its score stores and its draws of
+//                      shared tiles wait for the preceding grid;
+//   kPlanSelf          every CTA computes the plan itself from query_start_loc and positions (the
+//                      builder's rule; small problems only), so it starts fetching tiles while the
+//                      builder runs; its epilogue (the builder's row contexts) and its draws of
+//                      shared tiles (the builder zeroes their counter) wait for the builder.
+constexpr int kPlanAfterBuilder = 0, kPlanReady = 1, kPlanSelf = 2;
+constexpr int kSelfPlanMaxReqs = 2048, kSelfPlanMaxRows = 1024;
+
 struct ScoreArgs {
     const int4* seg;
     const int32_t* seg_tile_prefix;  // [segments + 1]
@@ -53,9 +66,11 @@ struct ScoreArgs {
     float* scores;           // chunk-local rows
     int64_t scores_ld;
     int32_t as_keys;         // 1: store ordered_key(score) (uint32 bits) instead of the fp32 score
-    int32_t plan_ready;      // 1: the builder had finished before the preceding grid started, so
-                             //    only the score stores wait for that grid (it may still read the
-                             //    score buffer); 0: everything waits (the builder precedes it)
+    int32_t plan_mode;       // kPlanAfterBuilder, kPlanReady or kPlanSelf (above)
+    // kPlanSelf only: the inputs the chunk's plan is computed from
+    const int32_t* qsl;      // [num_reqs + 1]
+    const int32_t* positions;
+    int32_t num_reqs, num_rows, row_end, seg_rows, max_context;
     int32_t npad_max;        // query lines per q buffer (multiple of 16, <= 256)
     int32_t stages;
     uint32_t tmem_cols;      // TMEM columns allocated (power of two)
@@ -191,7 +206,7 @@ size_t mla_smem_bytes();
 cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s);
 
-constexpr int kBuildThreads = 1024;
+constexpr int kBuildThreads = 512;
 constexpr int kScoreEpiWarps = 8;    // two per TMEM lane quarter
 constexpr int kScoreThreads = 64 + 32 * kScoreEpiWarps;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
 constexpr int kTopkThreads = 512;
