@@ -180,7 +180,7 @@ __device__ void plan_self(const ScoreArgs& a, const ScoreSmem& sm, int32_t* scra
 constexpr int kScoreMaxRegs = 96;
 
 // Tile schedule: CTA g first takes the contiguous static share [g*S, g*S + S) with
-// S = floor(3/4 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
+// S = floor(31/32 * tiles / grid), then draws single tiles from [S*grid, tiles) through an
 // atomic counter, so CTAs that stream faster take more of the tail.
 // kMode: how the CTA gets its plan (kPlanAfterBuilder, kPlanReady, kPlanSelf). In the last two
 // it runs ahead of the preceding grid's end; each mode is its own instantiation, so the plain
@@ -256,7 +256,10 @@ __global__ void __maxnreg__(kScoreMaxRegs)
             __syncwarp();
         }
         const int total = sm.prefix[nseg];
-        const int share = static_cast<int>((static_cast<int64_t>(total) * 3 / 4) / gridDim.x);
+        // a large static share: each shared draw is an atomic round trip in the producer's
+        // lookahead (measured: shares of 1/2, 5/8, 3/4, 7/8, 15/16 of the tiles were slower, and
+        // so was no shared tail at all)
+        const int share = static_cast<int>((static_cast<int64_t>(total) * 31 / 32) / gridDim.x);
         const int dyn0 = share * static_cast<int>(gridDim.x);
         {
             // warm L2 with the page-table entries of this CTA's static share (one line per lane)
