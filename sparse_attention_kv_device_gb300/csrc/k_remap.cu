@@ -60,6 +60,36 @@ __device__ __forceinline__ int32_t slot_of(int32_t t, const RemapArgs& a, const 
     return remap_fast(t, a, bt_row, a.block_stride_rows);
 }
 
+// The slots of one int4 of tokens. Four consecutive tokens in one block (what the selection
+// writes: a pool of 4 consecutive tokens starts at a multiple of 4) take one block-table load
+// for the four, with consecutive slots; anything else goes token by token. The results are
+// those of slot_of for each token.
+template <int MODE>
+__device__ __forceinline__ int4 slots4(int4 t, const RemapArgs& a, const int32_t* bt_row, bool req_ok,
+                                      int32_t ws_start, int ws_state) {
+    // (the DCP mode keeps the token-by-token path: its local indices are consecutive only with
+    // an interleave of 4 or more, and the extra code costs its latency-bound loop registers)
+    if (MODE != kRemapDcp && ws_state == 0 && req_ok) {
+        const uint32_t x = static_cast<uint32_t>(t.x);
+        if (t.x >= 0 && x <= 0x7ffffffcu && static_cast<uint32_t>(t.y) == x + 1u &&
+            static_cast<uint32_t>(t.z) == x + 2u && static_cast<uint32_t>(t.w) == x + 3u) {
+            const int32_t b = div_by(t.x, a.block_size, a.bs_shift);
+            if (div_by(t.w, a.block_size, a.bs_shift) == b) {
+                if (b >= a.max_blocks) return make_int4(-1, -1, -1, -1);
+                const int32_t ph = __ldg(bt_row + b);
+                if (ph < 0 || ph >= a.num_kv_blocks) return make_int4(-1, -1, -1, -1);
+                const int32_t s0 = static_cast<int32_t>(static_cast<int64_t>(ph) * a.block_stride_rows) +
+                                   mod_by(t.x, a.block_size, a.bs_shift);
+                return make_int4(s0, s0 + 1, s0 + 2, s0 + 3);
+            }
+        }
+    }
+    return make_int4(slot_of<MODE>(t.x, a, bt_row, req_ok, ws_start, ws_state),
+                     slot_of<MODE>(t.y, a, bt_row, req_ok, ws_start, ws_state),
+                     slot_of<MODE>(t.z, a, bt_row, req_ok, ws_start, ws_state),
+                     slot_of<MODE>(t.w, a, bt_row, req_ok, ws_start, ws_state));
+}
+
 }  // namespace
 
 constexpr int kCompactStage = 4096;  // columns of a compacted row assembled in shared memory
@@ -109,10 +139,7 @@ __global__ void __launch_bounds__(kRemapThreads) k_remap_rows(const RemapArgs a,
             uint32_t mine = 0;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                sl[u].x = slot_of<MODE>(t[u].x, a, bt_row, req_ok, ws_start, ws_state);
-                sl[u].y = slot_of<MODE>(t[u].y, a, bt_row, req_ok, ws_start, ws_state);
-                sl[u].z = slot_of<MODE>(t[u].z, a, bt_row, req_ok, ws_start, ws_state);
-                sl[u].w = slot_of<MODE>(t[u].w, a, bt_row, req_ok, ws_start, ws_state);
+                sl[u] = slots4<MODE>(t[u], a, bt_row, req_ok, ws_start, ws_state);
                 mine += (sl[u].x != -1) + (sl[u].y != -1) + (sl[u].z != -1) + (sl[u].w != -1);
             }
             uint32_t total;
@@ -130,11 +157,7 @@ __global__ void __launch_bounds__(kRemapThreads) k_remap_rows(const RemapArgs a,
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int v = vec(u);
-            int4 sl;
-            sl.x = slot_of<MODE>(t[u].x, a, bt_row, req_ok, ws_start, ws_state);
-            sl.y = slot_of<MODE>(t[u].y, a, bt_row, req_ok, ws_start, ws_state);
-            sl.z = slot_of<MODE>(t[u].z, a, bt_row, req_ok, ws_start, ws_state);
-            sl.w = slot_of<MODE>(t[u].w, a, bt_row, req_ok, ws_start, ws_state);
+            const int4 sl = slots4<MODE>(t[u], a, bt_row, req_ok, ws_start, ws_state);
             if (v < n4) reinterpret_cast<int4*>(out)[v] = sl;
             cnt += (sl.x != -1) + (sl.y != -1) + (sl.z != -1) + (sl.w != -1);
         }

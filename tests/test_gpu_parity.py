@@ -41,6 +41,55 @@ def test_remap_matches_oracle(rows, width, stride):
     np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
 
 
+@pytest.mark.parametrize("mode", ["global", "workspace", "dcp", "dcp_compact"])
+@pytest.mark.parametrize("block_size,kpool", [(64, 4), (6, 4), (16, 3), (5, 4)])
+def test_remap_modes_on_selection_shaped_tokens(mode, block_size, kpool):
+    """Runs of consecutive tokens (the selection's pools): an int4 of four consecutive tokens in
+    one block takes one block-table load in the kernel; runs that cross a block, a short pool
+    (kpool 3) and tokens past the guarded blocks go token by token. Bit exact in every mode."""
+    sel = lib()
+    rows, width, nreq, nkv = 61, 2052, 5, 4000
+    rng = np.random.default_rng(block_size * 31 + kpool + len(mode))
+    nb = 3000 // block_size + 4
+    bt = rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32) if nreq * nb <= nkv else \
+        rng.integers(0, nkv, size=(nreq, nb)).astype(np.int32)
+    bt[1, 3] = -1
+    bt[2, 7] = nkv + 3
+    mb = nb - 2                                   # the last blocks are past max_blocks_per_req
+    ctx = rng.integers(1, nb * block_size + 3 * block_size, size=rows)
+    ctx[:3] = [1, 2048, nb * block_size]          # a short row, a row at topk, a full table
+    tok = workloads.selection_token_indices(ctx, width, topk=kpool * 256, kpool=kpool, seed=block_size + kpool)
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)
+    req[:8] = np.arange(8) % nreq
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    if mode == "global":
+        ref_slots, ref_counts = oracle.remap_rows(req, nreq, bt, mb, nkv, tok, block_size, 2 * block_size)
+        sel.sel_remap_global(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, block_size=block_size,
+                             block_stride_rows=2 * block_size, max_blocks_per_req=mb, valid_counts=counts)
+    elif mode == "workspace":
+        wsr = rng.choice(np.array([-1, -1, -1, 0, 1, 5], np.int32), size=rows)
+        starts = np.array([0, 90000], np.int32)
+        ref_slots, ref_counts = oracle.remap_ws_rows(req, nreq, bt, mb, nkv, wsr, starts, tok, block_size,
+                                                     2 * block_size)
+        sel.sel_remap_workspace(t(req), t(bt), t(wsr), t(starts), t(tok), slots, num_kv_blocks=nkv,
+                                block_size=block_size, block_stride_rows=2 * block_size, max_blocks_per_req=mb,
+                                valid_counts=counts)
+    else:
+        compact = mode == "dcp_compact"
+        dcp, rank = 2, 1
+        inter = {64: 16, 6: 6, 16: 8, 5: 5}[block_size]   # block_size % interleave == 0 (sel.h)
+        ref_slots, ref_counts = oracle.remap_dcp_rows(req, nreq, bt, mb, nkv, tok, block_size, dcp, rank, inter,
+                                                      compact)
+        sel.sel_remap_dcp(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, dcp_size=dcp, dcp_rank=rank,
+                          interleave=inter, compact=compact, block_size=block_size, max_blocks_per_req=mb,
+                          valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
 def test_remap_golden_worked_example():
     sel = lib()
     g = load("remap_worked_example.txt")
