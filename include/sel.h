@@ -339,9 +339,13 @@ int sel_select_static(const sel_problem *p, int32_t *slots, int32_t out_width,
  * (p->key_cache is a device pointer). p's query_start_loc, positions, q,
  * key_page_table and block_table are HOST pointers here; they are copied into the
  * device staging area `stage` (sel_host_stage_bytes(p, out_width) bytes), the
- * selection runs, and slots_host / counts_host (host) receive the results with
- * asynchronous copies on `stream`. The caller synchronises the stream before
- * reading the outputs. status (optional) is a device word.
+ * selection runs, and slots_host / counts_host (host) receive the results, all
+ * asynchronously on `stream`. When every one of these host buffers is pinned and
+ * mapped into the device's address space (cudaHostAlloc, cudaHostRegister), one kernel
+ * reads all the inputs over the host link and the selection writes slots and counts
+ * straight into slots_host / counts_host (one launch per call instead of seven
+ * copy-engine transfers); otherwise every buffer is copied by cudaMemcpyAsync. The caller synchronises the stream before reading the
+ * outputs. status (optional) is a device word.
  */
 size_t sel_host_stage_bytes(const sel_problem *p, int32_t out_width);
 int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width,

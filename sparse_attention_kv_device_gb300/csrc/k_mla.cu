@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();  // the merge grid may take its places now (it waits for this grid's end)
     const uint32_t tmem = words[0];
     volatile int* abort_flag = reinterpret_cast<volatile int*>(&words[1]);
     auto fail = [&]() {
@@ -618,6 +619,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
 // partials. Each thread combines four consecutive dims with 16-byte loads, several partials'
 // loads in flight together.
 __global__ void __launch_bounds__(128) k_mla_merge(const MlaArgs a, int grid) {
+    // launched as a dependent grid: its CTAs are in place when the decode kernel ends, and wait
+    // here for its partials and outputs
+    pdl_wait();
     const int row = blockIdx.x, h = blockIdx.y;
     const int64_t tpr = a.tiles_per_row, total = a.total_tiles, G = grid;
     const int64_t first = static_cast<int64_t>(row) * tpr, last = first + tpr - 1;
@@ -691,8 +695,17 @@ cudaError_t launch_mla(const MlaArgs& a, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_mla_merge(const MlaArgs& a, int grid, cudaStream_t s) {
-    k_mla_merge<<<dim3(static_cast<unsigned>(a.rows), kMlaHeads), 128, 0, s>>>(a, grid);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.rows), kMlaHeads, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_mla_merge, a, grid);
 }
 
 }  // namespace sel

@@ -438,6 +438,18 @@ int remap_args(const int32_t* req_id, int32_t num_reqs, const int32_t* block_tab
     return SEL_OK;
 }
 
+// The device's address of a pinned host buffer mapped into its address space, or null (a
+// pageable or device buffer: the caller then uses the copy engine).
+template <typename T>
+T* device_view(T* host) {
+    cudaPointerAttributes at{};
+    if (!host || cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer is not an error here
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? static_cast<T*>(at.devicePointer) : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -854,27 +866,59 @@ int sel_select_host(const sel_problem* p, int32_t* slots_host, int32_t out_width
     uint8_t* d_bt = take(sizeof(int32_t) * static_cast<size_t>(p->num_reqs) * p->bt_ld);
     uint8_t* d_slots = take(sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width);
     uint8_t* d_counts = take(n_pos);
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
-    if (cudaMemcpyAsync(d_qsl, p->query_start_loc, n_qsl, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(d_pos, p->positions, n_pos, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(d_q, p->q, n_q, h2d, s) != cudaSuccess ||
-        (n_kpt && cudaMemcpyAsync(d_kpt, p->key_page_table, n_kpt, h2d, s) != cudaSuccess) ||
-        (n_bt && cudaMemcpyAsync(d_bt, p->block_table, n_bt, h2d, s) != cudaSuccess))
-        return SEL_ECUDA;
+    DeviceInfo di;
+    if ((rc = current_device_info(&di)) != SEL_OK) return rc;
+    // Pinned, mapped host buffers are copied by one kernel each way (over the host link);
+    // any other host buffer goes through the copy engine, one transfer per buffer.
+    StageArgs in{};
+    auto add = [](StageArgs& g, const void* src, void* dst, size_t bytes) {
+        g.src[g.nseg] = src;
+        g.dst[g.nseg] = dst;
+        g.bytes[g.nseg] = static_cast<int64_t>(bytes);
+        ++g.nseg;
+    };
+    const void* m_qsl = device_view(p->query_start_loc);
+    const void* m_pos = device_view(p->positions);
+    const void* m_q = device_view(p->q);
+    const void* m_kpt = n_kpt ? device_view(p->key_page_table) : nullptr;
+    const void* m_bt = n_bt ? device_view(p->block_table) : nullptr;
+    if (m_qsl && m_pos && m_q && (!n_kpt || m_kpt) && (!n_bt || m_bt)) {
+        add(in, m_qsl, d_qsl, n_qsl);
+        add(in, m_pos, d_pos, n_pos);
+        add(in, m_q, d_q, n_q);
+        if (n_kpt) add(in, m_kpt, d_kpt, n_kpt);
+        if (n_bt) add(in, m_bt, d_bt, n_bt);
+        if (launch_stage_copy(in, di.sms, s) != cudaSuccess) return SEL_ECUDA;
+    } else {
+        const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+        if (cudaMemcpyAsync(d_qsl, p->query_start_loc, n_qsl, h2d, s) != cudaSuccess ||
+            cudaMemcpyAsync(d_pos, p->positions, n_pos, h2d, s) != cudaSuccess ||
+            cudaMemcpyAsync(d_q, p->q, n_q, h2d, s) != cudaSuccess ||
+            (n_kpt && cudaMemcpyAsync(d_kpt, p->key_page_table, n_kpt, h2d, s) != cudaSuccess) ||
+            (n_bt && cudaMemcpyAsync(d_bt, p->block_table, n_bt, h2d, s) != cudaSuccess))
+            return SEL_ECUDA;
+    }
+    // results: written by the row select straight into mapped host buffers, else copied back
+    const size_t n_slots = sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width;
+    int32_t* m_slots = device_view(slots_host);
+    int32_t* m_counts = device_view(counts_host);
+    const bool direct_out = m_slots && m_counts && aligned16(m_slots);
     sel_problem d = *p;
     d.query_start_loc = reinterpret_cast<const int32_t*>(d_qsl);
     d.positions = reinterpret_cast<const int32_t*>(d_pos);
     d.q = d_q;
     d.key_page_table = reinterpret_cast<const int32_t*>(d_kpt);
     d.block_table = reinterpret_cast<const int32_t*>(d_bt);
-    rc = sel_select(&d, reinterpret_cast<int32_t*>(d_slots), out_width, reinterpret_cast<int32_t*>(d_counts),
-                    nullptr, status, ws, ws_bytes, stream);
+    rc = sel_select(&d, direct_out ? m_slots : reinterpret_cast<int32_t*>(d_slots), out_width,
+                    direct_out ? m_counts : reinterpret_cast<int32_t*>(d_counts), nullptr, status, ws, ws_bytes,
+                    stream);
     if (rc != SEL_OK) return rc;
-    const cudaMemcpyKind d2h = cudaMemcpyDeviceToHost;
-    if (cudaMemcpyAsync(slots_host, d_slots, sizeof(int32_t) * static_cast<size_t>(p->num_rows) * out_width, d2h,
-                        s) != cudaSuccess ||
-        cudaMemcpyAsync(counts_host, d_counts, n_pos, d2h, s) != cudaSuccess)
-        return SEL_ECUDA;
+    if (!direct_out) {
+        const cudaMemcpyKind d2h = cudaMemcpyDeviceToHost;
+        if (cudaMemcpyAsync(slots_host, d_slots, n_slots, d2h, s) != cudaSuccess ||
+            cudaMemcpyAsync(counts_host, d_counts, n_pos, d2h, s) != cudaSuccess)
+            return SEL_ECUDA;
+    }
     return SEL_OK;
 }
 

@@ -80,6 +80,17 @@ struct ScoreArgs {
     uint64_t wait_ns;        // limit of every bounded wait
 };
 
+// Copies between host-mapped and device buffers by a kernel (the host-buffer entry point):
+// segment i moves bytes[i] bytes (a multiple of 4, 4-byte aligned ends) from src[i] to dst[i].
+constexpr int kStageMaxSegs = 5;
+struct StageArgs {
+    const void* src[kStageMaxSegs];
+    void* dst[kStageMaxSegs];
+    int64_t bytes[kStageMaxSegs];
+    int32_t nseg;
+};
+cudaError_t launch_stage_copy(const StageArgs& a, int sms, cudaStream_t s);
+
 // Per-row exact top-k pools, expansion and remap on the scorer's keys (one CTA per row).
 struct RowSelectArgs {
     const uint32_t* keys;      // chunk-local rows: ordered_key of every complete pool's score

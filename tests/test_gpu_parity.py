@@ -454,11 +454,17 @@ def test_graph_replay_after_inplace_changes():
         assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
 
 
-def test_select_host_path_matches_device():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_select_host_path_matches_device(pinned):
+    """Pinned host buffers go through one staging kernel each way; pageable ones through the
+    copy engine. Both give the oracle's slots and counts."""
     sel = lib()
     w = workloads.make_workload("tiny")
     dprob = sel.problem_from_workload(w, DEV)
-    hp = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    if pinned:
+        hp = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    else:
+        hp = lambda a: torch.from_numpy(np.ascontiguousarray(a).copy())
     hprob = sel.Problem(query_start_loc=hp(w.qsl), positions=hp(w.positions), q=hp(w.q),
                         key_cache=dprob.tensors[3], key_page_table=hp(w.key_page_table),
                         block_table=hp(w.block_table), index_topk=w.index_topk, kpool=w.kpool,
@@ -466,8 +472,10 @@ def test_select_host_path_matches_device():
                         num_key_pages=w.num_key_pages, num_kv_blocks=w.num_kv_blocks,
                         block_stride_rows=w.block_stride_rows, max_q_len=w.max_q_len,
                         host_inputs=True)
-    slots_h = torch.empty((w.num_rows, w.out_width), dtype=torch.int32).pin_memory()
-    counts_h = torch.empty(w.num_rows, dtype=torch.int32).pin_memory()
+    slots_h = torch.empty((w.num_rows, w.out_width), dtype=torch.int32)
+    counts_h = torch.empty(w.num_rows, dtype=torch.int32)
+    if pinned:
+        slots_h, counts_h = slots_h.pin_memory(), counts_h.pin_memory()
     stage = torch.empty(sel.sel_host_stage_bytes(hprob, w.out_width), dtype=torch.uint8, device=DEV)
     ws = sel.new_workspace(sel.sel_workspace_bytes(dprob), DEV)
     sel.sel_select_host(hprob, slots_h, counts_h, stage, ws)
