@@ -18,12 +18,11 @@
 //     of 2; meanwhile the next tile's rows are prefetched into L2 by the TMA engine. An
 //     entry past kv_len or with a bad slot is zero-filled without touching the cache;
 //   warp 4 (one thread) issues, for tile k, S^T = K . Q^T on the tensor cores into TMEM
-//     (kind::f16, bf16 operands, fp32 accumulation in four interleaved partial sums; the
-//     product runs 128 rows deep and its upper 64 rows, which read the neighbouring 8 KiB of
-//     shared memory, are ignored), then
+//     (kind::f16, bf16 operands, fp32 accumulation in four interleaved partial sums; M = 64,
+//     the tile's entries, whose results sit in lanes 0-15 of each TMEM lane quarter), then
 //     tile k-1's O^T[512 x 16] += V^T . P^T, the same latent boxes read as an MN-major
 //     operand (a latent row is both key and value);
-//   warps 5-8 (one entry per thread of warps 5-6) read the tile's logits from TMEM, keep
+//   warps 5-8 (one entry per lane 0-15 of each warp) read the tile's logits from TMEM, keep
 //     the running maximum per head -- raised only when a logit exceeds it by more than 2^8,
 //     which then rescales O in TMEM --, and write p = 2^(logit - max) rounded to bf16 for
 //     the output product; the sums of p are kept per thread and reduced once per row.
@@ -321,7 +320,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
         // P(k-1), which frees tile k-1's pairs. The commit of S(k) covers every product of
         // tile k-2; O_DONE[t & 1] marks tile t's output products.
         if (lane == 0) {
-            const uint32_t idesc_s = umma_idesc_bf16_f32(128, kMlaHeads, 0);
+            // the score product: M = 64 entries (a tile), so only the tile's own rows are read;
+            // its result rows land in TMEM lanes 0-15 of each 32-lane quarter
+            const uint32_t idesc_s = umma_idesc_bf16_f32(kMlaTile, kMlaHeads, 0);
             const uint32_t idesc_o = umma_idesc_bf16_f32(128, kMlaHeads, 1);
             const uint32_t base = smem_u32(sm);
             ActIter it;
@@ -420,7 +421,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
         // ------------------------------------------------------------ softmax + output
         const int sw = warp - 5;             // softmax warp 0..3
         const int quarter = warp & 3;        // TMEM lanes this warp may access
-        const int j = quarter * 32 + lane;   // entry of the tile / dim within an O block
+        const int j = quarter * 32 + lane;   // dim within an O block (TMEM lane of the output product)
+        // entry of the tile: the M = 64 score product puts entry 16q + i in lane i < 16 of quarter q
+        const bool has_entry = lane < 16;
+        const int je = quarter * 16 + lane;
         int64_t tile_no = 0;
         int o_segs = 0, half = 0;
         bool ok = true;
@@ -438,8 +442,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
             for (int tt = 0; tt < sg.n_act; ++tt, ++tile_no) {
                 const int sb = static_cast<int>(tile_no & 1);
                 const uint32_t use = static_cast<uint32_t>((tile_no >> 1) & 1);
-                const int e = (sg.tin_a + tt) * kMlaTile + j;
-                const int sraw = j < kMlaTile ? raw_slot(a, row, sg.kvl, e) : -1;  // lanes 64-127: unused rows
+                const int e = (sg.tin_a + tt) * kMlaTile + je;
+                const int sraw = has_entry ? raw_slot(a, row, sg.kvl, e) : -1;  // lanes 16-31: no entry
                 int okw = 1;
                 if (lane == 0) okw = mbar_wait(&bar[kBSFull + sb], use, abort_flag, a.wait_ns) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -530,9 +534,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
                 if (lane == 0) okw = mbar_wait(&bar[kBPEmpty + sb], use ^ 1u, abort_flag, a.wait_ns) ? 1 : 0;
                 okw = __shfl_sync(0xffffffffu, okw, 0);
                 if (bar_red_or(!okw, kSoftBar, 128)) { ok = false; break; }
-                if (j < kMlaTile) {
-                    uint8_t* pbase = sm + kOffP + sb * kPBuf + (j & 7) * 2;
-                    const uint32_t chunk = static_cast<uint32_t>(j >> 3);
+                if (has_entry) {
+                    uint8_t* pbase = sm + kOffP + sb * kPBuf + (je & 7) * 2;
+                    const uint32_t chunk = static_cast<uint32_t>(je >> 3);
 #pragma unroll
                     for (int h = 0; h < 16; ++h)
                         *reinterpret_cast<uint16_t*>(pbase + h * 128 + ((chunk ^ (h & 7)) << 4)) = pb[h];
