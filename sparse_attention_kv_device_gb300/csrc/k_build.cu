@@ -35,7 +35,11 @@ __device__ __forceinline__ int last_le(const int32_t* v, int n, int x) {
 __global__ void __launch_bounds__(kBuildThreads) k_build_segments(const BuildArgs in) {
     extern __shared__ __align__(16) uint8_t bsm[];
     __shared__ uint32_t scratch[40];
-    pdl_launch_dependents();  // the scorer may start its prologue now
+    // Launched as a dependent (the host-buffer entry point's staging kernel precedes it), the
+    // builder waits for its inputs here; otherwise the wait returns at once. The scorer, which
+    // reads query_start_loc and positions before any wait of its own, may start after this.
+    pdl_wait();
+    pdl_launch_dependents();
     // this CTA's chunk and plan block
     BuildArgs a = in;
     {
@@ -204,7 +208,7 @@ size_t build_smem_bytes(const BuildArgs& a, BuildArgs* layout) {
     return off;
 }
 
-cudaError_t launch_build(const BuildArgs& in, cudaStream_t s) {
+cudaError_t launch_build(const BuildArgs& in, bool pdl, cudaStream_t s) {
     BuildArgs a = in;
     const size_t smem = build_smem_bytes(in, &a);
     static int configured[kMaxDevicesTracked] = {};
@@ -226,8 +230,17 @@ cudaError_t launch_build(const BuildArgs& in, cudaStream_t s) {
         configured[dev] = static_cast<int>(smem);
     }
     const int chunks = (a.row_end - a.row_begin + a.chunk_rows - 1) / a.chunk_rows;
-    k_build_segments<<<chunks, kBuildThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(chunks), 1, 1);
+    cfg.blockDim = dim3(kBuildThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_build_segments, a);
 }
 
 }  // namespace sel

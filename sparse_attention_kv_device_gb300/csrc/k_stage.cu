@@ -11,6 +11,7 @@ namespace {
 
 // one word per thread and step; 16-byte words where both ends and the length allow it
 __global__ void __launch_bounds__(256) k_stage_copy(const StageArgs a) {
+    pdl_launch_dependents();  // the builder may take its place; it waits for this grid's end
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (int s = 0; s < a.nseg; ++s) {

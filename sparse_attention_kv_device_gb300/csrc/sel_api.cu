@@ -321,7 +321,7 @@ Ws carve_ws(void* ws, const Plan& pl) {
 
 // The builder: every chunk's plan in one launch, one CTA per chunk.
 int launch_plans(const sel_problem* p, const Plan& pl, const Ws& w, int score_all, int64_t pool_cap,
-                 int32_t* status, cudaStream_t s) {
+                 int32_t* status, bool after_stage, cudaStream_t s) {
     BuildArgs b{};
     b.qsl = p->query_start_loc;
     b.positions = p->positions;
@@ -348,7 +348,7 @@ int launch_plans(const sel_problem* p, const Plan& pl, const Ws& w, int score_al
     b.seg_tile_prefix = w.prefix;
     b.hdr = w.hdr;
     b.status = status;
-    if (launch_build(b, s) != cudaSuccess) return SEL_ECUDA;
+    if (launch_build(b, after_stage, s) != cudaSuccess) return SEL_ECUDA;
     if (!score_all) trace_record(1, s);
     return SEL_OK;
 }
@@ -491,7 +491,7 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     if ((rc = encode_q_map(&tq, p->q, p->num_rows, p->q_row_stride)) != SEL_OK) return rc;
     Ws w = carve_ws(ws, pl);
     int32_t* st = status ? status : w.hdr + 8;
-    if ((rc = launch_plans(p, pl, w, 1, scores_ld, st, s)) != SEL_OK) return rc;
+    if ((rc = launch_plans(p, pl, w, 1, scores_ld, st, false, s)) != SEL_OK) return rc;
     for (int k = 0, c0 = 0; c0 < p->num_rows; ++k, c0 += pl.chunk_rows) {
         rc = launch_chunk_score(p, pl, w.chunk(k), c0, std::min(p->num_rows, c0 + pl.chunk_rows), 1,
                                 scores + static_cast<int64_t>(c0) * scores_ld, scores_ld,
@@ -754,8 +754,11 @@ int sel_mla_decode(const void* q_nope, int64_t qn_row_stride, int64_t qn_head_st
 
 int32_t sel_mla_launch_count(int32_t rows) { return rows > 0 ? 2 : 0; }
 
-int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,
-               int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {
+// sel_select's work; after_stage: a staging kernel of the host-buffer entry point directly
+// precedes it on the stream, and the builder is launched as its dependent.
+static int select_queue(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts,
+                        int32_t* token_idx, int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream,
+                        bool after_stage) {
     Plan pl;
     int rc = make_plan(p, &pl);
     if (rc != SEL_OK) return rc;
@@ -772,7 +775,7 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
     int32_t* st = status ? status : w.hdr + 8;
     std::lock_guard<std::mutex> g(g_trace_mu);
     trace_record(0, s);
-    if ((rc = launch_plans(p, pl, w, 0, pl.scores_ld, st, s)) != SEL_OK) return rc;
+    if ((rc = launch_plans(p, pl, w, 0, pl.scores_ld, st, after_stage, s)) != SEL_OK) return rc;
     for (int k = 0, c0 = 0; c0 < p->num_rows; ++k, c0 += pl.chunk_rows) {
         const int c1 = std::min(p->num_rows, c0 + pl.chunk_rows);
         const bool last = c1 == p->num_rows;
@@ -813,6 +816,11 @@ int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t*
         if (last) trace_record(3, s);
     }
     return SEL_OK;
+}
+
+int sel_select(const sel_problem* p, int32_t* slots, int32_t out_width, int32_t* valid_counts, int32_t* token_idx,
+               int32_t* status, void* ws, size_t ws_bytes, sel_stream_t stream) {
+    return select_queue(p, slots, out_width, valid_counts, token_idx, status, ws, ws_bytes, stream, false);
 }
 
 int32_t sel_select_launch_count(const sel_problem* p) {
@@ -909,9 +917,9 @@ int sel_select_host(const sel_problem* p, int32_t* slots_host, int32_t out_width
     d.q = d_q;
     d.key_page_table = reinterpret_cast<const int32_t*>(d_kpt);
     d.block_table = reinterpret_cast<const int32_t*>(d_bt);
-    rc = sel_select(&d, direct_out ? m_slots : reinterpret_cast<int32_t*>(d_slots), out_width,
-                    direct_out ? m_counts : reinterpret_cast<int32_t*>(d_counts), nullptr, status, ws, ws_bytes,
-                    stream);
+    rc = select_queue(&d, direct_out ? m_slots : reinterpret_cast<int32_t*>(d_slots), out_width,
+                      direct_out ? m_counts : reinterpret_cast<int32_t*>(d_counts), nullptr, status, ws, ws_bytes,
+                      stream, in.nseg > 0);
     if (rc != SEL_OK) return rc;
     if (!direct_out) {
         const cudaMemcpyKind d2h = cudaMemcpyDeviceToHost;

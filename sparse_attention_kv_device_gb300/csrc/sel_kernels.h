@@ -235,7 +235,7 @@ size_t topk_smem_bytes(int bt_cap);
 // Launchers. With `pdl` the kernel is a programmatic dependent of the previous kernel
 // on the stream: its prologue may overlap that kernel, and it waits (griddepcontrol)
 // before reading what that kernel wrote.
-cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
+cudaError_t launch_build(const BuildArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, int grid,
                          size_t smem, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, bool remap, int rows, size_t smem, bool pdl, cudaStream_t s);
