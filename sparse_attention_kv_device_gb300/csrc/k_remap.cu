@@ -84,10 +84,33 @@ __device__ __forceinline__ int4 slots4(int4 t, const RemapArgs& a, const int32_t
             }
         }
     }
-    return make_int4(slot_of<MODE>(t.x, a, bt_row, req_ok, ws_start, ws_state),
-                     slot_of<MODE>(t.y, a, bt_row, req_ok, ws_start, ws_state),
-                     slot_of<MODE>(t.z, a, bt_row, req_ok, ws_start, ws_state),
-                     slot_of<MODE>(t.w, a, bt_row, req_ok, ws_start, ws_state));
+    if (MODE != kRemapDcp)  // token by token (the fewest registers: occupancy wins here)
+        return make_int4(slot_of<MODE>(t.x, a, bt_row, req_ok, ws_start, ws_state),
+                         slot_of<MODE>(t.y, a, bt_row, req_ok, ws_start, ws_state),
+                         slot_of<MODE>(t.z, a, bt_row, req_ok, ws_start, ws_state),
+                         slot_of<MODE>(t.w, a, bt_row, req_ok, ws_start, ws_state));
+    // DCP, token by token: the guards first, then the four table loads together (a load only
+    // where its guard passes), so their latencies overlap instead of adding up (the local-index
+    // arithmetic otherwise keeps them apart)
+    const int32_t tt[4] = {t.x, t.y, t.z, t.w};
+    int32_t e[4], b[4], ph[4], r[4];
+    bool ok[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        e[i] = MODE == kRemapDcp ? dcp_local(tt[i], a) : tt[i];
+        ok[i] = req_ok && e[i] >= 0;
+        b[i] = ok[i] ? div_by(e[i], a.block_size, a.bs_shift) : 0;
+        ok[i] = ok[i] && b[i] < a.max_blocks;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ph[i] = ok[i] ? __ldg(bt_row + b[i]) : -1;
+    const int64_t stride = MODE == kRemapDcp ? a.block_size : a.block_stride_rows;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        r[i] = ok[i] && ph[i] >= 0 && ph[i] < a.num_kv_blocks
+                   ? static_cast<int32_t>(static_cast<int64_t>(ph[i]) * stride) + mod_by(e[i], a.block_size, a.bs_shift)
+                   : -1;
+    return make_int4(r[0], r[1], r[2], r[3]);
 }
 
 }  // namespace
@@ -154,12 +177,25 @@ __global__ void __launch_bounds__(kRemapThreads) k_remap_rows(const RemapArgs a,
             cnt += total;
             continue;
         }
+        if constexpr (MODE == kRemapDcp) {
+            // every vector's slots first (their table loads all in flight), then the stores
+            int4 sl[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int v = vec(u);
-            const int4 sl = slots4<MODE>(t[u], a, bt_row, req_ok, ws_start, ws_state);
-            if (v < n4) reinterpret_cast<int4*>(out)[v] = sl;
-            cnt += (sl.x != -1) + (sl.y != -1) + (sl.z != -1) + (sl.w != -1);
+            for (int u = 0; u < U; ++u) sl[u] = slots4<MODE>(t[u], a, bt_row, req_ok, ws_start, ws_state);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = vec(u);
+                if (v < n4) reinterpret_cast<int4*>(out)[v] = sl[u];
+                cnt += (sl[u].x != -1) + (sl[u].y != -1) + (sl[u].z != -1) + (sl[u].w != -1);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = vec(u);
+                const int4 sl = slots4<MODE>(t[u], a, bt_row, req_ok, ws_start, ws_state);
+                if (v < n4) reinterpret_cast<int4*>(out)[v] = sl;
+                cnt += (sl.x != -1) + (sl.y != -1) + (sl.z != -1) + (sl.w != -1);
+            }
         }
     }
     if (compact) {
