@@ -348,6 +348,25 @@ def test_segmentation_invariance(seg_rows, chunk_rows):
     assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
 
 
+@pytest.mark.parametrize("case", ["chunk_of_1100_rows", "2100_requests"])
+def test_select_large_first_chunk_waits_for_the_builder(case):
+    """A first chunk of more than 1,024 rows, or a call with more than 2,048 requests, is too
+    large for the scorer to plan itself: it takes the builder's plan. Later chunks read their
+    plans while the previous chunk's select runs. Integer mode, every row bit exact."""
+    if case == "chunk_of_1100_rows":
+        w = workloads.build_workload([list(range(3000, 4100))], name=case, seed=31, integer_mode=True,
+                                     index_topk=256)
+        out = run_select(w, chunk_rows=2048)
+    else:
+        rng = np.random.default_rng(32)
+        w = workloads.build_workload([[int(c)] for c in rng.integers(200, 1200, size=2100)], name=case, seed=32,
+                                     integer_mode=True, index_topk=256)
+        out = run_select(w)
+    ref = oracle_select(w)
+    assert out["status"] == ref["status"] == 0
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
 def test_batching_invariance():
     """A request selected alone or inside a batch gives the same rows."""
     full = workloads.build_workload([list(range(5000, 5005)), [9000, 9001], [300]], name="b", seed=8,
