@@ -289,7 +289,10 @@ def remap_modes(sel, torch, dev, stream, flush, peak, iters):
     columns shaped like the selection's output (ascending pools of 4 plus the trailing
     pool, -1 padding; 33.8 MB in, 33.8 MB out), a 2,048-block table row per request. Also
     the global mode on uniformly random token columns (the worst case for the block-table
-    gather). L2 flushed before each launch, CUDA events on the launching stream."""
+    gather). CUDA events on the launching stream. `us`: per launch of a run of four
+    back-to-back launches over four distinct token/slot buffer pairs (270 MB, above L2: each
+    launch reads cold tokens), L2 flushed before each run; `us_single`: one launch between
+    its own events, L2 flushed before it (this adds the launch latency to the kernel)."""
     rows, width, nreq, nb, nkv = 4112, 2052, 17, 2048, 40000
     rng = np.random.default_rng(77)
     bt = torch.from_numpy(rng.permutation(nkv)[:nreq * nb].reshape(nreq, nb).astype(np.int32)).to(dev)
@@ -298,37 +301,54 @@ def remap_modes(sel, torch, dev, stream, flush, peak, iters):
     req = torch.from_numpy(req_np).to(dev)
     wsr = torch.from_numpy(np.where(np.arange(rows) < 16, -1, 0).astype(np.int32)).to(dev)
     starts = torch.tensor([1 << 20], dtype=torch.int32, device=dev)
+    run = 4  # buffer pairs of one timed run
     tok = torch.from_numpy(workloads.selection_token_indices(ctx, width, seed=5)).to(dev)
     tok_rand = torch.from_numpy(workloads.random_token_indices(rows, width, nb * 64, seed=5)).to(dev)
-    slots = torch.empty((rows, width), dtype=torch.int32, device=dev)
-    counts = torch.empty(rows, dtype=torch.int32, device=dev)
+    toks = [tok] + [tok.clone() for _ in range(run - 1)]
+    toks_rand = [tok_rand] + [tok_rand.clone() for _ in range(run - 1)]
+    slots = [torch.empty((rows, width), dtype=torch.int32, device=dev) for _ in range(run)]
+    counts = [torch.empty(rows, dtype=torch.int32, device=dev) for _ in range(run)]
     calls = {
-        "global": lambda: sel.sel_remap_global(req, bt, tok, slots, num_kv_blocks=nkv, valid_counts=counts,
-                                               stream=stream),
-        "workspace": lambda: sel.sel_remap_workspace(req, bt, wsr, starts, tok, slots, num_kv_blocks=nkv,
-                                                     valid_counts=counts, stream=stream),
-        "dcp_compact": lambda: sel.sel_remap_dcp(req, bt, tok, slots, num_kv_blocks=nkv, dcp_size=4, dcp_rank=1,
-                                                 interleave=16, compact=True, valid_counts=counts, stream=stream),
-        "global_random_tokens": lambda: sel.sel_remap_global(req, bt, tok_rand, slots, num_kv_blocks=nkv,
-                                                             valid_counts=counts, stream=stream),
+        "global": lambda i: sel.sel_remap_global(req, bt, toks[i], slots[i], num_kv_blocks=nkv,
+                                                 valid_counts=counts[i], stream=stream),
+        "workspace": lambda i: sel.sel_remap_workspace(req, bt, wsr, starts, toks[i], slots[i], num_kv_blocks=nkv,
+                                                       valid_counts=counts[i], stream=stream),
+        "dcp_compact": lambda i: sel.sel_remap_dcp(req, bt, toks[i], slots[i], num_kv_blocks=nkv, dcp_size=4,
+                                                   dcp_rank=1, interleave=16, compact=True, valid_counts=counts[i],
+                                                   stream=stream),
+        "global_random_tokens": lambda i: sel.sel_remap_global(req, bt, toks_rand[i], slots[i], num_kv_blocks=nkv,
+                                                               valid_counts=counts[i], stream=stream),
     }
     nbytes = 2 * rows * width * 4 + 3 * rows * 4 + nreq * nb * 4
     out = {"shape": f"{rows} rows x {width} tokens (selection-shaped; the last mode: random tokens)",
-           "algorithmic_bytes": nbytes}
+           "algorithmic_bytes": nbytes,
+           "timing": f"us: per launch of {run} back-to-back launches over {run} distinct buffer pairs "
+                     f"({run * 2 * rows * width * 4 / 1e6:.0f} MB, above L2), L2 flushed before each run; "
+                     "us_single: one launch between its own events after an L2 flush"}
     with torch.cuda.stream(stream):
         for name, call in calls.items():
-            for _ in range(3):
-                call()
+            for i in range(run):
+                call(i)
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
             for a, b in ev:
                 flush()
                 a.record(stream)
-                call()
+                for i in range(run):
+                    call(i)
                 b.record(stream)
             stream.synchronize()
-            ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+            ms = float(np.mean([a.elapsed_time(b) for a, b in ev])) / run
+            ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+            for a, b in ev1:
+                flush()
+                a.record(stream)
+                call(0)
+                b.record(stream)
+            stream.synchronize()
+            ms1 = float(np.mean([a.elapsed_time(b) for a, b in ev1]))
             gbs = nbytes / (ms * 1e-3) / 1e9
-            out[name] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak}
+            out[name] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peak, "us_single": ms1 * 1e3,
+                         "frac_single": nbytes / (ms1 * 1e-3) / 1e9 / peak}
     return out
 
 

@@ -138,8 +138,8 @@ size_t sel_score_workspace_bytes(const sel_problem *p);
  * scores: device fp32 [num_rows][scores_ld], scores_ld >= 1.
  * Accumulation is fp32 on the tensor cores in an order of the hardware's choosing
  * (exact for integer-valued inputs whose dot products stay below 2^24).
- * status: optional device int32 word (see SEL_ST_*). ws: workspace of at least
- * sel_score_workspace_bytes(p) bytes.
+ * status: optional device int32 word (see SEL_ST_*). ws: 16-B aligned workspace of at
+ * least sel_score_workspace_bytes(p) bytes (no initialisation needed).
  */
 int sel_score_paged(const sel_problem *p, float *scores, int64_t scores_ld, int32_t *status,
                     void *ws, size_t ws_bytes, sel_stream_t stream);
@@ -301,7 +301,7 @@ int32_t sel_mla_launch_count(int32_t rows);
  * token_idx [num_rows][out_width] (optional): the selected token indices.
  * status (optional): device int32 word, see SEL_ST_*.
  * Requires out_width >= index_topk + kpool - 1, out_width % 4 == 0, slots and
- * token_idx 16-B aligned, and a workspace of sel_workspace_bytes(p) bytes.
+ * token_idx 16-B aligned, and a 16-B aligned workspace of sel_workspace_bytes(p) bytes.
  * The workspace (caller-owned device memory) needs no initialisation and carries nothing
  * from one call to the next; calls that share one must not overlap on the GPU.
  */

@@ -484,6 +484,7 @@ int sel_score_paged(const sel_problem* p, float* scores, int64_t scores_ld, int3
     if (rc != SEL_OK) return rc;
     if (p->num_rows == 0) return SEL_OK;
     if (!scores || scores_ld < 1 || !ws) return SEL_EINVAL;
+    if (!aligned16(ws)) return SEL_EUNSUPPORTED;  // 16-B plan records
     if (ws_bytes < pl.ws_score) return SEL_EWORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap tk, tq;
@@ -765,7 +766,7 @@ static int select_queue(const sel_problem* p, int32_t* slots, int32_t out_width,
     if (p->num_rows == 0) return SEL_OK;
     if (!slots || !ws) return SEL_EINVAL;
     if (out_width < p->index_topk + p->kpool - 1 || out_width % 4 != 0) return SEL_EINVAL;
-    if (!aligned16(slots) || (token_idx && !aligned16(token_idx))) return SEL_EUNSUPPORTED;
+    if (!aligned16(slots) || (token_idx && !aligned16(token_idx)) || !aligned16(ws)) return SEL_EUNSUPPORTED;
     if (ws_bytes < pl.ws_select) return SEL_EWORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CUtensorMap tk, tq;

@@ -90,6 +90,37 @@ def test_remap_modes_on_selection_shaped_tokens(mode, block_size, kpool):
     np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
 
 
+@pytest.mark.parametrize("dcp,inter,rank", [(4, 4, 3), (3, 4, 1), (8, 64, 5), (4, 16, 1)])
+@pytest.mark.parametrize("compact", [False, True])
+def test_dcp_remap_on_selection_shaped_tokens(dcp, inter, rank, compact):
+    """Pools of four consecutive tokens under DCP: with power-of-two sizes and an interleave of 4
+    or more the kernel maps an aligned pool with one ownership test and one table load; a rank
+    count of 3 takes the division path. Guarded blocks included; bit exact against the oracle."""
+    sel = lib()
+    rows, width, nreq, nkv, bs = 67, 2052, 5, 6000, 64
+    rng = np.random.default_rng(dcp * 100 + inter + rank)
+    nb = 1100
+    bt = rng.integers(0, nkv, size=(nreq, nb)).astype(np.int32)
+    bt[1, 3] = -1
+    bt[2, 7] = nkv + 3
+    mb = nb - 2
+    ctx = rng.integers(1, nb * bs * dcp, size=rows)
+    ctx[:3] = [1, 2048, nb * bs * dcp]
+    tok = workloads.selection_token_indices(ctx, width, topk=2048, kpool=4, seed=dcp + inter)
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)
+    req[:8] = np.arange(8) % nreq
+    ref_slots, ref_counts = oracle.remap_dcp_rows(req, nreq, bt, mb, nkv, tok, bs, dcp, rank, inter, compact)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    sel.sel_remap_dcp(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, dcp_size=dcp, dcp_rank=rank,
+                      interleave=inter, compact=compact, block_size=bs, max_blocks_per_req=mb,
+                      valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
 def test_remap_golden_worked_example():
     sel = lib()
     g = load("remap_worked_example.txt")
@@ -525,3 +556,59 @@ def test_launch_count_one_builder_then_two_per_chunk():
     for name, chunks in (("decode128k", 1), ("tiny", 1), ("mixed", 17)):
         w = workloads.make_workload(name)
         assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == 1 + 2 * chunks, name
+
+
+@pytest.mark.parametrize("fill", ["ones", "one_word", "random"])
+def test_select_workspace_needs_no_initialisation(fill):
+    """The workspace needs no initialisation: the builder rewrites each chunk's plan header and
+    tile counter before any scorer draws from it. A workspace of any prior content (all bits
+    set; one repeated word; random bytes) gives bit-exact rows on the first call and on the
+    calls after it, in one chunk or three."""
+    sel = lib()
+    w = workloads.build_workload([list(range(20000, 20005)), [9000, 9001, 9002], [70000], [4100, 4101]],
+                                 name="ws", seed=41, integer_mode=True, index_topk=512)
+    ref = oracle_select(w)
+    for chunk_rows in (0, 4):
+        prob = sel.problem_from_workload(w, DEV, chunk_rows=chunk_rows)
+        n = sel.sel_workspace_bytes(prob)
+        if fill == "ones":
+            ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
+        elif fill == "one_word":
+            ws = torch.full(((n + 3) // 4,), 0x6A09E667, dtype=torch.int32, device=DEV).view(torch.uint8)
+        else:
+            g = torch.Generator(device="cpu").manual_seed(43)
+            ws = torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).to(DEV)
+        for _ in range(3):
+            slots = torch.full((w.num_rows, w.out_width), -7, dtype=torch.int32, device=DEV)
+            counts = torch.full((w.num_rows,), -7, dtype=torch.int32, device=DEV)
+            tok = torch.full_like(slots, -7)
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            sel.sel_select(prob, slots, counts, token_idx=tok, status=status, ws=ws)
+            torch.cuda.synchronize()
+            out = dict(slots=slots.cpu().numpy(), counts=counts.cpu().numpy(), token_idx=tok.cpu().numpy(),
+                       status=int(status.item()))
+            assert out["status"] == 0
+            assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
+def test_select_refuses_a_misaligned_workspace():
+    """The plan records are read as 16-byte vectors: a workspace that is not 16-B aligned is
+    refused with SEL_EUNSUPPORTED before anything is queued, by both entry points that take one."""
+    sel = lib()
+    w = workloads.make_workload("tiny")
+    prob = sel.problem_from_workload(w, DEV)
+    n = sel.sel_workspace_bytes(prob)
+    base = torch.zeros(n + 64, dtype=torch.uint8, device=DEV)
+    slots = torch.full((w.num_rows, w.out_width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((w.num_rows,), -7, dtype=torch.int32, device=DEV)
+    with pytest.raises(sel.SelError) as e:
+        sel.sel_select(prob, slots, counts, ws=base[8:8 + n])
+    assert e.value.code == -2  # SEL_EUNSUPPORTED
+    torch.cuda.synchronize()
+    assert (slots == -7).all() and (counts == -7).all()
+    ld = max(4, ((int(w.max_context) // int(w.kpool)) + 3) // 4 * 4)
+    scores = torch.zeros((w.num_rows, ld), dtype=torch.float32, device=DEV)
+    ns = sel.sel_score_workspace_bytes(prob)
+    with pytest.raises(sel.SelError) as e:
+        sel.sel_score_paged(prob, scores, ws=base[4:4 + ns])
+    assert e.value.code == -2  # SEL_EUNSUPPORTED
