@@ -6,6 +6,8 @@ exactly (the selection's score tolerance never comes into play). Two calls in a 
 check that the array carries nothing over from one call to the next. This file is
 collected last so that it also runs after every other GPU test in the same process."""
 
+import gc
+
 import pytest
 import torch
 
@@ -52,15 +54,18 @@ def test_static_entry_matches_sel_select_twice(name):
     sel.sel_select_static(prob, warm[0], warm[1], token_idx=warm[2], status=warm[3])
     torch.cuda.synchronize()
     # device memory as the driver counts it: a cudaMalloc inside the library would show here,
-    # not only in torch's own allocator statistics
+    # not only in torch's own allocator statistics. Tensors of earlier tests are collected
+    # first; the counts may still fall (a collection during the calls), never rise.
+    gc.collect()
+    torch.cuda.synchronize()
     free_before, _ = torch.cuda.mem_get_info()
     before = torch.cuda.memory_allocated()
     sel.sel_select_static(prob, first[0], first[1], token_idx=first[2], status=first[3])
     sel.sel_select_static(prob, second[0], second[1], token_idx=second[2], status=second[3])
     torch.cuda.synchronize()
-    assert torch.cuda.memory_allocated() == before
+    assert torch.cuda.memory_allocated() <= before
     free_after, _ = torch.cuda.mem_get_info()
-    assert free_after == free_before
+    assert free_after >= free_before
     _assert_same(first, ref)
     _assert_same(second, ref)
 
