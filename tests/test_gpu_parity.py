@@ -121,6 +121,41 @@ def test_dcp_remap_on_selection_shaped_tokens(dcp, inter, rank, compact):
     np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
 
 
+@pytest.mark.parametrize("width", [3000, 5124])
+@pytest.mark.parametrize("compact", [False, True])
+@pytest.mark.parametrize("shape", ["selection", "random"])
+def test_dcp_remap_rows_of_several_rounds(width, compact, shape):
+    """Rows wider than one round of the kernel (2,560 tokens): the compaction's warp totals
+    alternate between two buffers by round, and past 4,096 columns the compacted row goes
+    straight to global memory instead of through shared memory. Bit exact against the oracle."""
+    sel = lib()
+    rows, nreq, nkv, bs, dcp, inter, rank = 37, 4, 9000, 64, 4, 16, 1
+    rng = np.random.default_rng(width + compact + len(shape))
+    nb = 2100
+    bt = rng.integers(0, nkv, size=(nreq, nb)).astype(np.int32)
+    bt[0, 5] = -1
+    bt[3, 11] = nkv + 2
+    mb = nb - 2
+    if shape == "selection":
+        ctx = rng.integers(1, nb * bs * dcp, size=rows)
+        ctx[:2] = [nb * bs * dcp, 3 * width]
+        tok = workloads.selection_token_indices(ctx, width, topk=4 * ((width - 4) // 4), kpool=4, seed=width)
+    else:
+        tok = workloads.random_token_indices(rows, width, nb * bs * dcp + 100, seed=width)
+    req = rng.integers(-1, nreq + 1, size=rows).astype(np.int32)
+    req[:6] = np.arange(6) % nreq
+    ref_slots, ref_counts = oracle.remap_dcp_rows(req, nreq, bt, mb, nkv, tok, bs, dcp, rank, inter, compact)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    slots = torch.full((rows, width), -7, dtype=torch.int32, device=DEV)
+    counts = torch.full((rows,), -7, dtype=torch.int32, device=DEV)
+    sel.sel_remap_dcp(t(req), t(bt), t(tok), slots, num_kv_blocks=nkv, dcp_size=dcp, dcp_rank=rank,
+                      interleave=inter, compact=compact, block_size=bs, max_blocks_per_req=mb,
+                      valid_counts=counts)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    np.testing.assert_array_equal(counts.cpu().numpy(), ref_counts)
+
+
 def test_remap_golden_worked_example():
     sel = lib()
     g = load("remap_worked_example.txt")
