@@ -498,13 +498,14 @@ def graph_steps(sel, torch, prob, slots, counts, ws, stream, flush, iters, warmu
     return np.array([a.elapsed_time(b) for a, b in ev])
 
 
-def config_leg(sel, torch, dev, stream, flush, name, iters, peak, tpeak):
+def config_leg(sel, torch, dev, stream, flush, name, iters, peak, tpeak, chunk_rows=None):
     """One of the other workloads (ragged decode, the mixed step) timed like the headline:
     rows/s, time per step, algorithmic bytes and the fraction of the HBM copy peak; for a
     step with a large tensor-core share also the fraction of the tensor peak, and the
-    larger of the two as the roofline fraction."""
+    larger of the two as the roofline fraction. chunk_rows overrides the workload's logits
+    chunk (0: the library's own choice)."""
     w = workloads.make_workload(name)
-    prob = sel.problem_from_workload(w, dev)
+    prob = sel.problem_from_workload(w, dev, **({} if chunk_rows is None else {"chunk_rows": chunk_rows}))
     slots = torch.empty((w.num_rows, w.out_width), dtype=torch.int32, device=dev)
     counts = torch.empty(w.num_rows, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -672,6 +673,10 @@ def run_ours(args):
     if not args.no_configs:
         configs = {n: auxiliary(lambda n=n: config_leg(sel, torch, dev, stream, flush, n, 20, peak, tpeak))
                    for n in ("ragged", "mixed") if n != args.config}
+        # the mixed step again with the library's default chunking (larger than the workload's
+        # 256-row logits chunks; see chunk_rows in include/sel.h): for information, not the config
+        configs["mixed_library_chunks"] = auxiliary(
+            lambda: config_leg(sel, torch, dev, stream, flush, "mixed", 20, peak, tpeak, chunk_rows=0))
     remap = None
     if not args.no_remap:
         remap = auxiliary(lambda: remap_modes(sel, torch, dev, stream, flush, peak, 20))

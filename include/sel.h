@@ -107,7 +107,9 @@ typedef struct sel_problem {
     int64_t bt_ld;                 /* row stride of block_table, in elements */
     int64_t q_row_stride;          /* fp16 elements between query rows (>= 512, multiple of 8) */
     int32_t segment_rows;          /* rows of one request scored together (1..64; 0 = automatic) */
-    int32_t chunk_rows;            /* rows per score-workspace chunk (0 = 256) */
+    int32_t chunk_rows;            /* rows per score-workspace chunk (0: the library's choice,
+                                      four times the SM count, capped so one chunk's fp32
+                                      scores at max_context fill at most 3/4 of L2, >= 256) */
     const int32_t *query_start_loc; /* [num_reqs + 1] */
     const int32_t *positions;       /* [num_rows] */
     const void *q;                  /* fp16 [num_rows][4][128] with row stride q_row_stride; 16-B aligned */

@@ -100,17 +100,21 @@ def test_graph_replay_after_request_runs_and_page_tables_change():
 
 
 def test_select_mixed_every_row_and_repeat_calls():
-    """All 4,112 rows of the mixed step (17 chunks of 256 rows) under the parity rule,
-    compared against the oracle in batches of rows; repeated calls are identical."""
+    """All 4,112 rows of the mixed step (17 chunks of 256 rows, and again in the library's
+    default chunks) under the parity rule, compared against the oracle in batches of rows;
+    repeated calls are identical."""
     w = workloads.make_workload("mixed")
     first = run_select(w)
     assert first["status"] == 0
-    differing = 0
+    wide = run_select(w, chunk_rows=0)
+    assert wide["status"] == 0
+    differing = [0, 0]
     for lo in range(0, w.num_rows, 512):
         rows = np.arange(lo, min(w.num_rows, lo + 512), dtype=np.int32)
         ref = oracle_select(w, rows=rows, want_scores=True)
-        differing += assert_select_parity(w, first, ref, rows)
-    assert differing <= w.num_rows // 50, differing
+        differing[0] += assert_select_parity(w, first, ref, rows)
+        differing[1] += assert_select_parity(w, wide, ref, rows)
+    assert max(differing) <= w.num_rows // 50, differing
     for _ in range(2):
         again = run_select(w)
         for k in ("slots", "counts", "token_idx"):

@@ -591,6 +591,11 @@ def test_launch_count_one_builder_then_two_per_chunk():
     for name, chunks in (("decode128k", 1), ("tiny", 1), ("mixed", 17)):
         w = workloads.make_workload(name)
         assert sel.sel_select_launch_count(sel.problem_from_workload(w, DEV)) == 1 + 2 * chunks, name
+    # the library's own chunking (chunk_rows 0): four times the SM count here, fewer chunks
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    w = workloads.make_workload("mixed")
+    wide = sel.problem_from_workload(w, DEV, chunk_rows=0)
+    assert sel.sel_select_launch_count(wide) == 1 + 2 * -(-w.num_rows // (4 * sms))
 
 
 @pytest.mark.parametrize("fill", ["ones", "one_word", "random"])
