@@ -347,7 +347,8 @@ int sel_select_static(const sel_problem *p, int32_t *slots, int32_t out_width,
  * reads all the inputs over the host link and the selection writes slots and counts
  * straight into slots_host / counts_host (one launch per call instead of seven
  * copy-engine transfers); otherwise every buffer is copied by cudaMemcpyAsync. The caller synchronises the stream before reading the
- * outputs. status (optional) is a device word.
+ * outputs. status (optional) is a device word. `stage` and `ws` are device memory, 16-B
+ * aligned; ws holds sel_workspace_bytes(p) bytes, as for sel_select.
  */
 size_t sel_host_stage_bytes(const sel_problem *p, int32_t out_width);
 int sel_select_host(const sel_problem *p, int32_t *slots_host, int32_t out_width,

@@ -867,7 +867,10 @@ int sel_select_host(const sel_problem* p, int32_t* slots_host, int32_t out_width
     int rc = check_problem(p);
     if (rc != SEL_OK) return rc;
     if (p->num_rows == 0) return SEL_OK;
-    if (!slots_host || !counts_host || !stage) return SEL_EINVAL;
+    if (!slots_host || !counts_host || !stage || !ws) return SEL_EINVAL;
+    // the staged queries are read by tensor copies, the workspace holds 16-byte records: refuse
+    // misaligned buffers before any copy is queued
+    if (!aligned16(stage) || !aligned16(ws)) return SEL_EUNSUPPORTED;
     if (stage_bytes < sel_host_stage_bytes(p, out_width)) return SEL_EWORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* b = static_cast<uint8_t*>(stage);

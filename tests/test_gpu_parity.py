@@ -652,3 +652,23 @@ def test_select_refuses_a_misaligned_workspace():
     with pytest.raises(sel.SelError) as e:
         sel.sel_score_paged(prob, scores, ws=base[4:4 + ns])
     assert e.value.code == -2  # SEL_EUNSUPPORTED
+    # the host-buffer entry point: a misaligned staging area or workspace is refused before
+    # any input is copied or any output written
+    hp = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    hprob = sel.Problem(query_start_loc=hp(w.qsl), positions=hp(w.positions), q=hp(w.q),
+                        key_cache=prob.tensors[3], key_page_table=hp(w.key_page_table),
+                        block_table=hp(w.block_table), index_topk=w.index_topk, kpool=w.kpool,
+                        max_context=w.max_context, key_page_stride=w.key_page_stride,
+                        num_key_pages=w.num_key_pages, num_kv_blocks=w.num_kv_blocks,
+                        block_stride_rows=w.block_stride_rows, max_q_len=w.max_q_len,
+                        host_inputs=True)
+    slots_h = torch.full((w.num_rows, w.out_width), -7, dtype=torch.int32).pin_memory()
+    counts_h = torch.full((w.num_rows,), -7, dtype=torch.int32).pin_memory()
+    nst = sel.sel_host_stage_bytes(hprob, w.out_width)
+    stage_base = torch.zeros(nst + 64, dtype=torch.uint8, device=DEV)
+    for stage, ws in ((stage_base[4:4 + nst], base[:n]), (stage_base[:nst], base[8:8 + n])):
+        with pytest.raises(sel.SelError) as e:
+            sel.sel_select_host(hprob, slots_h, counts_h, stage, ws)
+        assert e.value.code == -2  # SEL_EUNSUPPORTED
+    torch.cuda.synchronize()
+    assert (slots_h == -7).all() and (counts_h == -7).all()
