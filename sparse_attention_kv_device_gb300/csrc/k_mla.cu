@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1) k_mla_decode(const MlaArgs a) 
 // One CTA per (row, head): a row whose tiles ran in more than one CTA gets the weighted
 // combination of their partials (weights 2^(m_c - max_c m_c)); other rows were written whole.
 // A row has at most kMlaMaxTilesPerRow tiles (the host checks), so at most that many
-// partials. Each thread combines four consecutive dims with 16-byte loads, several partials'
-// loads in flight together.
+// partials. Every thread loads its four dims of each partial together with the partials'
+// maxima and sums (one round of loads, no block barrier) and computes the weights itself.
 __global__ void __launch_bounds__(128) k_mla_merge(const MlaArgs a, int grid) {
     // launched as a dependent grid: its CTAs are in place when the decode kernel ends, and wait
     // here for its partials and outputs
@@ -635,50 +635,59 @@ __global__ void __launch_bounds__(128) k_mla_merge(const MlaArgs a, int grid) {
     const int c_hi = static_cast<int>(((last + 1) * G - 1) / total);
     if (c_lo == c_hi) return;
     const int n = c_hi - c_lo + 1;
-    __shared__ const float* src[kMlaMaxTilesPerRow];
-    __shared__ float mv[kMlaMaxTilesPerRow], lbv[kMlaMaxTilesPerRow], lev[kMlaMaxTilesPerRow], wv[kMlaMaxTilesPerRow];
-    __shared__ float inv_s;
     const int t = threadIdx.x;
-    if (t < n) {
-        const int c = c_lo + t;
+    auto part_of = [&](int i) {
+        const int c = c_lo + i;
         const int slot = 2 * c + ((c * total / G) < first ? 1 : 0);
-        const float* p = reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
-        src[t] = p + h * kMlaDc;
-        mv[t] = p[kMlaHeads * kMlaDc + h];
-        lbv[t] = p[kMlaHeads * kMlaDc + 16 + h];
-        lev[t] = p[kMlaHeads * kMlaDc + 32 + h];
-    }
-    __syncthreads();
-    if (t == 0) {
-        float mx = -INFINITY;
-        for (int i = 0; i < n; ++i) mx = fmaxf(mx, mv[i]);
-        float lb = 0.0f, le = 0.0f;
-        for (int i = 0; i < n; ++i) {
-            const float w = mv[i] == -INFINITY ? 0.0f : exp2f(mv[i] - mx);
-            wv[i] = w;
-            lb += w * lbv[i];
-            le += w * lev[i];
-        }
-        inv_s = lb > 0.0f ? 1.0f / lb : 0.0f;
-        a.lse[static_cast<int64_t>(row) * kMlaHeads + h] =
-            le > 0.0f ? (mx + log2f(le)) * 0.69314718055994531f : -INFINITY;
-    }
-    __syncthreads();
+        return reinterpret_cast<const float*>(a.part + static_cast<size_t>(slot) * kMlaPartBytes);
+    };
+    float mx = -INFINITY, lb = 0.0f, le = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 8
-    for (int i = 0; i < n; ++i) {
-        const float w = wv[i];
-        if (w != 0.0f) {  // a partial without entries was never written
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src[i]) + t);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+    constexpr int kB = 8;  // partials whose loads are in flight together
+    for (int i0 = 0; i0 < n; i0 += kB) {
+        float m[kB], b[kB], e[kB];
+        float4 v[kB];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            if (i0 + k < n) {
+                const float* p = part_of(i0 + k);
+                m[k] = __ldcg(p + kMlaHeads * kMlaDc + h);
+                b[k] = __ldcg(p + kMlaHeads * kMlaDc + 16 + h);
+                e[k] = __ldcg(p + kMlaHeads * kMlaDc + 32 + h);
+                v[k] = __ldcg(reinterpret_cast<const float4*>(p + h * kMlaDc) + t);
+            } else {
+                m[k] = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            if (m[k] == -INFINITY) continue;  // a partial without entries: its values were never written
+            // a running maximum: rescale what was summed so far when it rises
+            if (m[k] > mx) {
+                const float r = mx == -INFINITY ? 0.0f : exp2f(mx - m[k]);
+                lb *= r;
+                le *= r;
+                acc.x *= r;
+                acc.y *= r;
+                acc.z *= r;
+                acc.w *= r;
+                mx = m[k];
+            }
+            const float w = exp2f(m[k] - mx);
+            lb += w * b[k];
+            le += w * e[k];
+            acc.x += w * v[k].x;
+            acc.y += w * v[k].y;
+            acc.z += w * v[k].z;
+            acc.w += w * v[k].w;
         }
     }
-    const float inv = inv_s;
+    const float inv = lb > 0.0f ? 1.0f / lb : 0.0f;
     reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(row) * kMlaHeads + h) * kMlaDc)[t] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (t == 0)
+        a.lse[static_cast<int64_t>(row) * kMlaHeads + h] =
+            le > 0.0f ? (mx + log2f(le)) * 0.69314718055994531f : -INFINITY;
 }
 
 size_t mla_smem_bytes() { return kSmemUsed + 1024; }
