@@ -433,6 +433,19 @@ def test_select_large_first_chunk_waits_for_the_builder(case):
     assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
 
 
+def test_select_rows_longer_than_the_stage_bit_exact():
+    """Rows with more pools than the row select stages in shared memory (32,768 keys): 200K and
+    256K rows and a 400K row (100,000 pools), whose keys past the stage are read from global
+    memory in every phase. Integer mode (many equal scores, so the lowest-index rule decides at
+    the threshold): every row bit exact."""
+    w = workloads.build_workload([[262144], [200001, 200003], [400003]], name="long", seed=77,
+                                 integer_mode=True, index_topk=2048)
+    out = run_select(w)
+    ref = oracle_select(w)
+    assert out["status"] == ref["status"] == 0
+    assert_select_bitexact(w, out, ref, np.arange(w.num_rows))
+
+
 def test_batching_invariance():
     """A request selected alone or inside a batch gives the same rows."""
     full = workloads.build_workload([list(range(5000, 5005)), [9000, 9001], [300]], name="b", seed=8,
